@@ -1,0 +1,23 @@
+"""Independent fp64 CPU oracle of the chunked TTT fast-weight layer.
+
+Test infrastructure only: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it; the product path never does.
+It shares no code with the CUDA path.
+
+Parity status of each function (what pins it is in tests/test_oracle_pins.py):
+  swiglu_apply, linear_apply  - pinned (torch fp64 library forward; zero-update case)
+  swiglu_grad, linear_grad    - pinned (central finite differences; torch autograd;
+                                per-token sum)
+  newton_schulz               - pinned (closed form through the SVD)
+  weight_norm                 - pinned (row-norm and direction invariants)
+  ttt_head / ttt_layer        - pinned in the special cases with closed forms
+                                (delta rule, block-shifted linear attention,
+                                single-chunk linear attention, zero update) and by
+                                invariants (causality, resume, permutation);
+                                the full SwiGLU + Muon + weight-norm chain has no
+                                printed values to check against: parity unpinned
+                                beyond those compositions.
+"""
+from .ttt_oracle import (OracleCfg, chunk_grad, linear_apply, linear_grad,  # noqa: F401
+                         newton_schulz, row_norms, sigmoid, swiglu_apply, swiglu_grad,
+                         ttt_head, ttt_layer, update, weight_norm)

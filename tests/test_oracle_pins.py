@@ -1,0 +1,380 @@
+"""Pins of the fp64 oracle against things fixed outside of it.
+
+No page prints a worked numeric example of the layer, so every pin here is a
+closed form, an invariant, a library routine the oracle does not use, or brute
+force (finite differences). Each one is chosen so that a plausible slip in the
+oracle (a dropped term, a sign, a transposed operand, a mean instead of a sum,
+apply/update in the wrong order, a wrong norm axis) fails at least one test.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import ttt_oracle as orc
+
+RNG = np.random.default_rng(1234)
+
+
+def _rand_weights(fast_net, d, dh, rng, scale=1.0):
+    if fast_net == "swiglu":
+        return (rng.standard_normal((dh, d)) * scale / np.sqrt(d),
+                rng.standard_normal((d, dh)) * scale / np.sqrt(dh),
+                rng.standard_normal((dh, d)) * scale / np.sqrt(d))
+    return (rng.standard_normal((d, d)) / np.sqrt(d),)
+
+
+def _loss_from_definition(fast_net, loss, W, K, V, eta):
+    """sum_t eta_t l_t with l_t = -f(k_t).v_t or 1/2 ||f(k_t) - v_t||^2."""
+    f = orc.swiglu_apply(W, K) if fast_net == "swiglu" else orc.linear_apply(W, K)
+    if loss == "ip":
+        per = -(f * V).sum(axis=1)
+    else:
+        per = 0.5 * ((f - V) ** 2).sum(axis=1)
+    return float((eta * per).sum())
+
+
+@pytest.mark.parametrize("fast_net", ["swiglu", "linear"])
+@pytest.mark.parametrize("loss", ["ip", "mse"])
+def test_gradient_matches_central_differences(fast_net, loss):
+    """Brute force: every gradient entry against a central difference (h = 1e-6)."""
+    rng = np.random.default_rng(7)
+    d, dh, C = 4, 8, 3
+    W = _rand_weights(fast_net, d, dh, rng, scale=1.5)
+    K = rng.standard_normal((C, d))
+    V = rng.standard_normal((C, d))
+    eta = rng.uniform(0.1, 1.0, C)
+    fn = orc.swiglu_grad if fast_net == "swiglu" else orc.linear_grad
+    G = fn(W, K, V, eta, loss)
+    h = 1e-6
+    for j, Wj in enumerate(W):
+        fd = np.zeros_like(Wj)
+        for idx in np.ndindex(*Wj.shape):
+            Wp = [w.copy() for w in W]
+            Wm = [w.copy() for w in W]
+            Wp[j][idx] += h
+            Wm[j][idx] -= h
+            fd[idx] = (_loss_from_definition(fast_net, loss, Wp, K, V, eta)
+                       - _loss_from_definition(fast_net, loss, Wm, K, V, eta)) / (2 * h)
+        err = np.abs(fd - G[j]).max() / np.abs(G[j]).max()
+        assert err < 1e-7, (j, err)
+
+
+@pytest.mark.parametrize("loss", ["ip", "mse"])
+def test_swiglu_gradient_matches_torch_autograd(loss):
+    """torch (a different library, with its own silu) differentiates the same loss."""
+    rng = np.random.default_rng(11)
+    d, dh, C = 6, 10, 9
+    W = _rand_weights("swiglu", d, dh, rng, scale=2.0)
+    K = rng.standard_normal((C, d))
+    V = rng.standard_normal((C, d))
+    eta = rng.uniform(0.0, 0.3, C)
+    tw = [torch.tensor(w, dtype=torch.float64, requires_grad=True) for w in W]
+    tk, tv, te = (torch.tensor(x, dtype=torch.float64) for x in (K, V, eta))
+    f = F.linear(F.silu(F.linear(tk, tw[0])) * F.linear(tk, tw[2]), tw[1])
+    per = -(f * tv).sum(1) if loss == "ip" else 0.5 * ((f - tv) ** 2).sum(1)
+    (te * per).sum().backward()
+    G = orc.swiglu_grad(W, K, V, eta, loss)
+    for j in range(3):
+        ref = tw[j].grad.numpy()
+        assert np.abs(G[j] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_swiglu_forward_matches_torch():
+    rng = np.random.default_rng(3)
+    d, dh = 16, 40
+    W = _rand_weights("swiglu", d, dh, rng, scale=3.0)
+    X = rng.standard_normal((25, d))
+    tw = [torch.tensor(w, dtype=torch.float64) for w in W]
+    tx = torch.tensor(X, dtype=torch.float64)
+    ref = F.linear(F.silu(F.linear(tx, tw[0])) * F.linear(tx, tw[2]), tw[1]).numpy()
+    assert np.abs(orc.swiglu_apply(W, X) - ref).max() <= 1e-13 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("fast_net", ["swiglu", "linear"])
+def test_chunk_gradient_is_sum_of_token_gradients(fast_net):
+    """LaCT page §2.1: the update uses the gradient SUMMED over the chunk's tokens."""
+    rng = np.random.default_rng(5)
+    d, dh, C = 8, 16, 37
+    W = _rand_weights(fast_net, d, dh, rng)
+    K = rng.standard_normal((C, d))
+    V = rng.standard_normal((C, d))
+    eta = rng.uniform(0, 0.1, C)
+    cfg = orc.OracleCfg(chunk=C, fast_net=fast_net, loss="mse")
+    G = orc.chunk_grad(cfg, W, K, V, eta)
+    Gb = orc.chunk_grad(cfg, W, K, V, eta, block=5)
+    per = [orc.chunk_grad(cfg, W, K[t:t + 1], V[t:t + 1], eta[t:t + 1]) for t in range(C)]
+    for j in range(len(W)):
+        s = sum(p[j] for p in per)
+        assert np.abs(G[j] - s).max() <= 1e-12 * np.abs(s).max()
+        assert np.abs(Gb[j] - s).max() <= 1e-12 * np.abs(s).max()
+
+
+def test_linear_mse_chunk1_is_delta_rule():
+    """Chunk of one token, linear net, MSE, plain SGD: the delta rule
+    W <- W - eta (W k - v) k^T, with o_t read from W before token t's update."""
+    rng = np.random.default_rng(9)
+    d, T = 5, 23
+    W0 = rng.standard_normal((d, d)) / np.sqrt(d)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.2, T)
+    cfg = orc.OracleCfg(chunk=1, fast_net="linear", loss="mse", muon=False, wnorm=False)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    W = W0.copy()
+    Oref = np.zeros((T, d))
+    for t in range(T):
+        Oref[t] = W @ Q[t]
+        W = W - eta[t] * np.outer(W @ K[t] - V[t], K[t])
+    assert np.abs(O - Oref).max() <= 1e-12
+    assert np.abs(Wf - W).max() <= 1e-12
+
+
+@pytest.mark.parametrize("mask", [None, [1, 0, 1, 1, 0], [0, 1, 0, 1, 0]])
+def test_linear_ip_is_block_shifted_linear_attention(mask):
+    """Linear net, inner-product loss, SGD: o_t = W0 q_t + sum over tokens s of
+    UPDATED chunks strictly before t's chunk of eta_s v_s (k_s . q_t)."""
+    rng = np.random.default_rng(21)
+    d, C, T = 6, 4, 19     # ragged last chunk
+    W0 = rng.standard_normal((d, d))
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.5, T)
+    cfg = orc.OracleCfg(chunk=C, fast_net="linear", loss="ip", muon=False, wnorm=False,
+                        mask=mask)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    m = mask or [1] * 5
+    upd = np.array([m[s // C] for s in range(T)], dtype=float)
+    Oref = np.zeros((T, d))
+    for t in range(T):
+        start = (t // C) * C
+        acc = W0 @ Q[t]
+        for s in range(start):
+            acc = acc + upd[s] * eta[s] * V[s] * (K[s] @ Q[t])
+        Oref[t] = acc
+    assert np.abs(O - Oref).max() <= 1e-12
+    Wref = W0 + sum(upd[s] * eta[s] * np.outer(V[s], K[s]) for s in range(T))
+    assert np.abs(Wf - Wref).max() <= 1e-12
+
+
+def test_linear_ip_single_chunk_is_noncausal_linear_attention():
+    """Single-chunk update-then-apply (LaCT page §3.1): every query sees every key."""
+    rng = np.random.default_rng(22)
+    d, T = 7, 30
+    W0 = rng.standard_normal((d, d))
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.5, T)
+    cfg = orc.OracleCfg(chunk=T, fast_net="linear", loss="ip", mode="single",
+                        muon=False, wnorm=False)
+    O, _ = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    Oref = Q @ W0.T + ((Q @ K.T) * eta[None, :]) @ V
+    assert np.abs(O - Oref).max() <= 1e-12
+
+
+NS = (3.4445, -4.7750, 2.0315)
+
+
+def _phi5(x):
+    a, b, c = NS
+    for _ in range(5):
+        x = a * x + b * x ** 3 + c * x ** 5
+    return x
+
+
+@pytest.mark.parametrize("shape", [(8, 20), (20, 8), (12, 12), (64, 128)])
+def test_newton_schulz_closed_form_through_svd(shape):
+    """The iteration acts on singular values only: G = U S V^T gives
+    NS5(G) = U phi^5(S / (||G||_F + eps)) V^T, phi(x) = a x + b x^3 + c x^5."""
+    rng = np.random.default_rng(shape[0] * 100 + shape[1])
+    G = rng.standard_normal(shape) * 0.01
+    U, S, Vt = np.linalg.svd(G, full_matrices=False)
+    ref = (U * _phi5(S / (np.linalg.norm(S) + 1e-7))) @ Vt
+    out = orc.newton_schulz(G, 5, *NS, 1e-7)
+    assert np.abs(out - ref).max() <= 1e-10 * np.abs(ref).max()
+
+
+def test_newton_schulz_singular_values_near_one():
+    """LaCT page §2.2.1: Muon turns the gradient into an (approximately)
+    orthogonal matrix. phi^5 maps [3e-3, 1] into [0.6, 1.25]; real chunk
+    gradients of the workload shapes land there."""
+    xs = np.linspace(3e-3, 1.0, 20001)
+    y = _phi5(xs)
+    assert y.min() > 0.6 and y.max() < 1.25
+    rng = np.random.default_rng(2)
+    d, dh, C = 32, 64, 256
+    W = _rand_weights("swiglu", d, dh, rng)
+    K = rng.standard_normal((C, d))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = rng.standard_normal((C, d))
+    eta = 0.01 / (1 + np.exp(-rng.standard_normal(C)))
+    for Gj in orc.swiglu_grad(W, K, V, eta, "ip"):
+        s_in = np.linalg.svd(Gj, compute_uv=False)
+        s_in = s_in / (np.linalg.norm(s_in) + 1e-7)
+        s_out = np.linalg.svd(orc.newton_schulz(Gj, 5, *NS, 1e-7), compute_uv=False)
+        keep = s_in >= 3e-3
+        assert keep.sum() >= min(Gj.shape) // 2
+        assert s_out[keep].min() > 0.6 and s_out[keep].max() < 1.25
+
+
+@pytest.mark.parametrize("shape", [(6, 5), (5, 5), (4, 7)])
+def test_weight_norm_restores_row_norms_and_keeps_directions(shape):
+    rng = np.random.default_rng(4)
+    W = (rng.standard_normal(shape),)
+    G = (rng.standard_normal(shape),)
+    n0 = [np.abs(rng.standard_normal(shape[0])) + 0.1]
+    cfg = orc.OracleCfg(chunk=1, fast_net="linear", muon=False, wnorm=True, step=0.7)
+    (Wn,) = orc.update(cfg, W, G, n0)
+    raw = W[0] - 0.7 * G[0]
+    assert np.abs(np.linalg.norm(Wn, axis=1) - n0[0]).max() <= 1e-13
+    ratio = Wn / raw
+    assert (ratio > 0).all()
+    assert np.abs(ratio - ratio[:, :1]).max() <= 1e-12   # one positive scale per row
+
+
+@pytest.mark.parametrize("muon", [False, True])
+def test_layer_keeps_every_row_norm_of_w0(muon):
+    rng = np.random.default_rng(6)
+    d, dh, C, T = 8, 16, 5, 23
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=C, muon=muon, wnorm=True)
+    _, Wf = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    for w0, wf in zip(W0, Wf):
+        assert np.abs(np.linalg.norm(wf, axis=1) - np.linalg.norm(w0, axis=1)).max() <= 1e-12
+        assert np.abs(wf - w0).max() > 1e-3            # it did move
+
+
+def test_one_sgd_chunk_steps_against_the_brute_force_gradient():
+    """Update direction and step: W1 = W0 - step * grad, grad by finite differences."""
+    rng = np.random.default_rng(8)
+    d, dh, C = 3, 5, 4
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((C, d)) for _ in range(3))
+    eta = rng.uniform(0.1, 0.5, C)
+    cfg = orc.OracleCfg(chunk=C, muon=False, wnorm=False, step=0.5)
+    _, Wf = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    h = 1e-6
+    for j in range(3):
+        fd = np.zeros_like(W0[j])
+        for idx in np.ndindex(*W0[j].shape):
+            Wp = [w.copy() for w in W0]
+            Wm = [w.copy() for w in W0]
+            Wp[j][idx] += h
+            Wm[j][idx] -= h
+            fd[idx] = (_loss_from_definition("swiglu", "ip", Wp, K, V, eta)
+                       - _loss_from_definition("swiglu", "ip", Wm, K, V, eta)) / (2 * h)
+        assert np.abs(Wf[j] - (W0[j] - 0.5 * fd)).max() <= 1e-8
+
+
+@pytest.mark.parametrize("muon", [False, True])
+def test_shifted_chunks_do_not_leak_the_future(muon):
+    """LaCT page §3.2 (shifted block-causal mask): outputs of chunks before j do
+    not change when anything of chunk j changes, and chunk j's own outputs do
+    not see its own keys and values."""
+    rng = np.random.default_rng(10)
+    d, dh, C, T = 8, 16, 6, 30
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=C, muon=muon, wnorm=True)
+    O, _ = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    j = 3
+    sl = slice(j * C, (j + 1) * C)
+    Q2, K2, V2 = Q.copy(), K.copy(), V.copy()
+    K2[sl] += 1.0
+    V2[sl] -= 2.0
+    O2, _ = orc.ttt_head(cfg, Q2, K2, V2, eta, W0)
+    assert np.array_equal(O2[:(j + 1) * C], O[:(j + 1) * C])
+    assert np.abs(O2[(j + 1) * C:] - O[(j + 1) * C:]).max() > 1e-6
+    Q2[sl] += 1.0
+    O3, _ = orc.ttt_head(cfg, Q2, K2, V2, eta, W0)
+    assert np.array_equal(O3[:j * C], O[:j * C])
+
+
+def test_no_update_is_the_plain_swiglu_mlp():
+    rng = np.random.default_rng(12)
+    d, dh, C, T = 8, 16, 4, 16
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=C, mask=[0, 0, 0, 0])
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    tw = [torch.tensor(w) for w in W0]
+    ref = F.linear(F.silu(F.linear(torch.tensor(Q), tw[0])) * F.linear(torch.tensor(Q), tw[2]),
+                   tw[1]).numpy()
+    assert np.abs(O - ref).max() <= 1e-13 * np.abs(ref).max()
+    assert all(np.array_equal(a, b) for a, b in zip(Wf, W0))
+
+
+def test_video_mask_skips_noisy_chunks():
+    """LaCT page §3.3: fast weights change only after the clean-frame chunks."""
+    rng = np.random.default_rng(13)
+    d, dh, C, T = 8, 16, 4, 16
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=C, mask=[0, 1, 0, 1])
+    O, _ = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    assert np.abs(O[C:2 * C] - orc.swiglu_apply(W0, Q[C:2 * C])).max() == 0.0
+    # chunk 2 sees exactly one update, the one of chunk 1
+    W1 = orc.update(cfg, W0, orc.chunk_grad(cfg, W0, K[C:2 * C], V[C:2 * C], eta[C:2 * C]),
+                    [np.linalg.norm(w, axis=1) for w in W0])
+    assert np.abs(O[2 * C:3 * C] - orc.swiglu_apply(W1, Q[2 * C:3 * C])).max() <= 1e-13
+
+
+def test_single_chunk_is_permutation_invariant():
+    rng = np.random.default_rng(14)
+    d, dh, T = 8, 16, 40
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=T, mode="single")
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    p = rng.permutation(T)
+    O2, Wf2 = orc.ttt_head(cfg, Q[p], K[p], V[p], eta[p], W0)
+    for a, b in zip(Wf, Wf2):
+        assert np.abs(a - b).max() <= 1e-12
+    assert np.abs(O2 - O[p]).max() <= 1e-12
+
+
+@pytest.mark.parametrize("wnorm", [False, True])
+def test_resume_at_a_chunk_boundary(wnorm):
+    """Two calls split at a chunk boundary, the second starting from the first's
+    final weights, equal one call (W_final is the layer's whole state)."""
+    rng = np.random.default_rng(15)
+    d, dh, C, T = 8, 16, 5, 30
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.1, T)
+    cfg = orc.OracleCfg(chunk=C, wnorm=wnorm)
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    s = 3 * C
+    Oa, Wa = orc.ttt_head(cfg, Q[:s], K[:s], V[:s], eta[:s], W0)
+    Ob, Wb = orc.ttt_head(cfg, Q[s:], K[s:], V[s:], eta[s:], Wa)
+    tol = 1e-12 if wnorm else 0.0
+    assert np.abs(np.concatenate([Oa, Ob]) - O).max() <= tol
+    for a, b in zip(Wb, Wf):
+        assert np.abs(a - b).max() <= tol
+
+
+def test_toy_scalar_ttt_on_a_noisy_sinusoid():
+    """Tutorial page §10 project: scalar w, MSE on predicting x_t from x_{t-1},
+    SGD with lr 0.01, update then predict. With d = 1 the layer is the scalar
+    recurrence w <- w - 0.01 (w x_{t-1} - x_t) x_{t-1}."""
+    rng = np.random.default_rng(16)
+    t = np.arange(1001)
+    x = np.sin(0.05 * t) + 0.05 * rng.standard_normal(t.size)
+    K = x[:-1, None]
+    V = x[1:, None]
+    eta = np.full(1000, 0.01)
+    cfg = orc.OracleCfg(chunk=1, fast_net="linear", loss="mse", muon=False, wnorm=False)
+    O, (Wf,) = orc.ttt_head(cfg, K, K, V, eta, (np.zeros((1, 1)),))
+    w = 0.0
+    pred = []
+    for i in range(1000):
+        pred.append(w * K[i, 0])
+        w -= 0.01 * (w * K[i, 0] - V[i, 0]) * K[i, 0]
+    assert np.isfinite(O).all()
+    assert np.abs(O[:, 0] - np.array(pred)).max() <= 1e-12
+    assert abs(Wf[0, 0] - w) <= 1e-12
+    # the adapted scalar predicts better than the initial w = 0 on the last half
+    assert ((O[500:, 0] - V[500:, 0]) ** 2).mean() < (V[500:, 0] ** 2).mean()
