@@ -1,0 +1,154 @@
+/*
+ * ttt.h - C ABI of the B300 (sm_103a) chunked test-time-training layer.
+ *
+ * The layer (LaCT page, "Large Chunk Test-Time Training", §2.1): per (batch,
+ * head) a fast-weight net f_W is applied to each chunk's queries (apply phase,
+ * the page's eq. 2) and updated from the gradient of a self-supervised inner
+ * loss, summed over the chunk's tokens with per-token learning rates (update
+ * phase, eq. 4-5). The update optionally goes through Muon's Newton-Schulz
+ * orthogonalisation (§2.2.1, eq. 9-10) and an L2 row weight norm (§2.2.1,
+ * eq. 8). Shifted mode applies chunk i with the weights left by chunks
+ * 0..i-1 (§3.2, shifted block-causal mask); single mode updates on a chunk and
+ * then applies to the same chunk (§3.1: one chunk = the whole image set).
+ *
+ *   fast nets: SwiGLU   f(x) = W2 (silu(W1 x) * (W3 x)),  W1,W3: [dh, d], W2: [d, dh]
+ *              linear   f(x) = W x,                       W: [d, d]
+ *   losses:    inner product  l = -f(k).v ;  MSE  l = 1/2 ||f(k) - v||^2
+ *   update:    G = sum_t lr_t grad_W l_t ;  U = NS5(G) or G ;  W <- W - step * U ;
+ *              (weight norm) W[r,:] <- W[r,:] * n0[r] / max(||W[r,:]||, wnorm_eps),
+ *              n0 = the row norms of W0.
+ *
+ * Every call runs on the GPU. There is no CPU fallback: a build without the
+ * device code cannot be loaded.
+ */
+#ifndef TTT_B300_H
+#define TTT_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TTT_API __attribute__((visibility("default")))
+#else
+#define TTT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (0 = success, negative = error) ---------------------- */
+#define TTT_OK               0
+#define TTT_ERR_ARG         -1  /* bad shape, NULL or misaligned pointer, aliasing */
+#define TTT_ERR_UNSUPPORTED -2  /* valid request that no built kernel covers       */
+#define TTT_ERR_WORKSPACE   -3  /* workspace NULL, too small or misaligned         */
+#define TTT_ERR_CUDA        -4  /* a CUDA runtime call failed                      */
+#define TTT_ERR_TIMEOUT     -5  /* a device-side wait gave up (timeout_us)         */
+#define TTT_ERR_NONFINITE   -6  /* check_finite found a NaN/Inf in the inputs      */
+#define TTT_ERR_DEVICE      -7  /* a device-side consistency check failed          */
+
+/* ---- enumerations -------------------------------------------------------- */
+enum { TTT_NET_SWIGLU = 0, TTT_NET_LINEAR = 1 };
+enum { TTT_LOSS_IP = 0, TTT_LOSS_MSE = 1 };
+enum { TTT_MODE_SHIFTED = 0, TTT_MODE_SINGLE = 1 };
+enum { TTT_DTYPE_F32 = 0, TTT_DTYPE_BF16 = 1 };
+/* kernel family: AUTO picks the fastest one that covers the request */
+enum { TTT_IMPL_AUTO = 0, TTT_IMPL_SIMT = 1, TTT_IMPL_TC = 2, TTT_IMPL_LINEAR = 3 };
+
+/* Layer configuration. Fill it with ttt_cfg_default() and override fields. */
+typedef struct ttt_cfg {
+  int32_t B, H, T;        /* batch, heads, tokens per sequence                  */
+  int32_t d;              /* head dim (input and output width of f)             */
+  int32_t dh;             /* SwiGLU hidden width (ignored for the linear net)    */
+  int32_t chunk;          /* tokens per chunk; the last chunk may be shorter     */
+  int32_t fast_net;       /* TTT_NET_*                                            */
+  int32_t loss;           /* TTT_LOSS_*                                           */
+  int32_t mode;           /* TTT_MODE_*                                           */
+  int32_t dtype;          /* storage type of Q, K, V, O: TTT_DTYPE_*              */
+  int32_t muon;           /* 1: Newton-Schulz orthogonalisation of each G         */
+  int32_t ns_iters;       /* Newton-Schulz iterations (5)                         */
+  float   ns_a, ns_b, ns_c; /* quintic coefficients (3.4445, -4.7750, 2.0315)     */
+  float   ns_eps;         /* X0 = G / (||G||_F + ns_eps)  (1e-7)                  */
+  int32_t wnorm;          /* 1: restore the row norms of W0 after every update    */
+  float   wnorm_eps;      /* floor of the row norm in the rescale (1e-12)         */
+  float   step;           /* W <- W - step * U  (1.0)                             */
+  const uint8_t* update_mask; /* HOST array of n_chunks flags; NULL = every chunk
+                             updates. Read during the ttt_fwd call only.        */
+  int32_t w0_per_batch;   /* 0: W0 is [H, out, in] shared over B; 1: [B, H, out, in] */
+  int32_t check_finite;   /* 1: scan the inputs first; NaN/Inf -> TTT_ERR_NONFINITE */
+  uint32_t timeout_us;    /* limit of every device-side wait (default 2,000,000)  */
+  int32_t impl;           /* TTT_IMPL_*                                           */
+} ttt_cfg;
+
+/* Fills *cfg with the defaults above (B = H = T = d = dh = chunk = 0, SwiGLU,
+ * inner-product loss, shifted mode, bf16, Muon with 5 iterations, weight norm
+ * on, step 1, AUTO). */
+TTT_API void ttt_cfg_default(ttt_cfg* cfg);
+
+/* Bytes of device workspace ttt_fwd needs for *cfg (and the path AUTO picks).
+ * Returns TTT_OK, TTT_ERR_ARG or TTT_ERR_UNSUPPORTED. */
+TTT_API int ttt_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
+
+/* The layer forward (LaCT page §2.1: apply + update over all chunks).
+ *
+ * All tensor pointers are DEVICE pointers, 16-byte aligned, row-major,
+ * contiguous, owned by the caller:
+ *   Q, K, V   [B, H, T, d]     fp32 or bf16 (cfg->dtype); read only
+ *   lr        [B, H, T]        fp32 per-token learning rate; read only
+ *   W0_1..3   SwiGLU: W1 [H, dh, d], W2 [H, d, dh], W3 [H, dh, d] fp32
+ *             (each with a leading B when w0_per_batch); linear: W0_1 = W [H, d, d],
+ *             W0_2 = W0_3 = NULL; read only
+ *   O         [B, H, T, d]     cfg->dtype; written
+ *   Wf_1..3   final fast weights [B, H, out, in] fp32; written (Wf_2, Wf_3 NULL for linear)
+ *   workspace device scratch of >= ttt_workspace_bytes() bytes, 256-byte aligned;
+ *             its first 256 bytes hold the device status word
+ *   stream    a cudaStream_t (NULL = the legacy default stream)
+ * Outputs must not overlap inputs or the workspace.
+ *
+ * The work is enqueued on `stream`; the call returns without waiting. Host-
+ * detectable errors (TTT_ERR_ARG, _UNSUPPORTED, _WORKSPACE) return before any
+ * launch. Device-side errors (TTT_ERR_TIMEOUT, _NONFINITE, _DEVICE) are
+ * recorded in the workspace status word: read them with ttt_status(). */
+TTT_API int ttt_fwd(const ttt_cfg* cfg,
+            const void* Q, const void* K, const void* V, const float* lr,
+            const float* W0_1, const float* W0_2, const float* W0_3,
+            void* O, float* Wf_1, float* Wf_2, float* Wf_3,
+            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Waits for `stream`, then returns the status word of the most recent
+ * ttt_fwd on this workspace (every ttt_fwd clears it when it starts): TTT_OK,
+ * a device-side error code, or TTT_ERR_CUDA if the stream reports an error. */
+TTT_API int ttt_status(void* workspace, void* stream);
+
+/* Bytes of one DEVICE arena that ttt_fwd_host needs: room for the inputs,
+ * the outputs and the workspace, each 256-byte aligned. */
+TTT_API int ttt_host_arena_bytes(const ttt_cfg* cfg, size_t* bytes);
+
+/* The layer on HOST buffers (same shapes and types as ttt_fwd; pinned host
+ * memory gives full copy bandwidth). Copies the inputs into `arena` (device,
+ * >= ttt_host_arena_bytes(), caller-owned), runs ttt_fwd on `stream`, copies O
+ * and the final weights back, waits for the stream and returns the status
+ * (ttt_status folded in). */
+TTT_API int ttt_fwd_host(const ttt_cfg* cfg,
+                 const void* Q, const void* K, const void* V, const float* lr,
+                 const float* W0_1, const float* W0_2, const float* W0_3,
+                 void* O, float* Wf_1, float* Wf_2, float* Wf_3,
+                 void* arena, size_t arena_bytes, void* stream);
+
+/* Which kernel family AUTO (or cfg->impl) resolves to for *cfg: TTT_IMPL_*,
+ * or a negative status if none covers it. */
+TTT_API int ttt_select_impl(const ttt_cfg* cfg);
+
+/* Static description of a status code. */
+TTT_API const char* ttt_strerror(int status);
+
+/* ABI version (incremented on any incompatible change of this header). */
+TTT_API int ttt_abi_version(void);
+
+/* sizeof(ttt_cfg) as compiled into the library (lets bindings check layout). */
+TTT_API size_t ttt_cfg_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTT_B300_H */

@@ -1,0 +1,236 @@
+"""Thin ctypes binding of the C ABI in include/ttt.h (argument marshalling only).
+
+Functions keep the C names. Tensor arguments are torch tensors (device memory
+for ttt_fwd, host memory for ttt_fwd_host); only their data pointers cross the
+boundary. Every step of the layer runs in the CUDA library: if
+libttt_b300.so is missing this module fails to import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int, c_int32, c_size_t, c_uint32, c_void_p
+from typing import Optional, Sequence
+
+import numpy as np
+
+from .build_ext import LIB_PATH
+
+# status codes and enums (mirrors of include/ttt.h)
+TTT_OK = 0
+TTT_ERR_ARG = -1
+TTT_ERR_UNSUPPORTED = -2
+TTT_ERR_WORKSPACE = -3
+TTT_ERR_CUDA = -4
+TTT_ERR_TIMEOUT = -5
+TTT_ERR_NONFINITE = -6
+TTT_ERR_DEVICE = -7
+TTT_NET_SWIGLU, TTT_NET_LINEAR = 0, 1
+TTT_LOSS_IP, TTT_LOSS_MSE = 0, 1
+TTT_MODE_SHIFTED, TTT_MODE_SINGLE = 0, 1
+TTT_DTYPE_F32, TTT_DTYPE_BF16 = 0, 1
+TTT_IMPL_AUTO, TTT_IMPL_SIMT, TTT_IMPL_TC, TTT_IMPL_LINEAR = 0, 1, 2, 3
+
+EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
+            "ttt_host_arena_bytes", "ttt_fwd_host", "ttt_select_impl", "ttt_strerror",
+            "ttt_abi_version", "ttt_cfg_size")
+
+
+class ttt_cfg(ctypes.Structure):
+    _fields_ = [
+        ("B", c_int32), ("H", c_int32), ("T", c_int32), ("d", c_int32), ("dh", c_int32),
+        ("chunk", c_int32), ("fast_net", c_int32), ("loss", c_int32), ("mode", c_int32),
+        ("dtype", c_int32), ("muon", c_int32), ("ns_iters", c_int32),
+        ("ns_a", c_float), ("ns_b", c_float), ("ns_c", c_float), ("ns_eps", c_float),
+        ("wnorm", c_int32), ("wnorm_eps", c_float), ("step", c_float),
+        ("update_mask", c_void_p), ("w0_per_batch", c_int32), ("check_finite", c_int32),
+        ("timeout_us", c_uint32), ("impl", c_int32),
+    ]
+
+
+class TTTError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: {ttt_strerror(code)} ({code})" if where else ttt_strerror(code))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m long_seq_models_chunked_b300.build_ext` "
+            "(the layer has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(ttt_cfg)
+    lib.ttt_cfg_default.argtypes = [P]
+    lib.ttt_cfg_default.restype = None
+    lib.ttt_workspace_bytes.argtypes = [P, ctypes.POINTER(c_size_t)]
+    lib.ttt_host_arena_bytes.argtypes = [P, ctypes.POINTER(c_size_t)]
+    ten = [c_void_p] * 11
+    lib.ttt_fwd.argtypes = [P, *ten, c_void_p, c_size_t, c_void_p]
+    lib.ttt_fwd_host.argtypes = [P, *ten, c_void_p, c_size_t, c_void_p]
+    lib.ttt_status.argtypes = [c_void_p, c_void_p]
+    lib.ttt_select_impl.argtypes = [P]
+    lib.ttt_strerror.argtypes = [c_int]
+    lib.ttt_strerror.restype = ctypes.c_char_p
+    lib.ttt_abi_version.argtypes = []
+    lib.ttt_cfg_size.argtypes = []
+    lib.ttt_cfg_size.restype = c_size_t
+    for name in ("ttt_workspace_bytes", "ttt_host_arena_bytes", "ttt_fwd", "ttt_fwd_host",
+                 "ttt_status", "ttt_select_impl", "ttt_abi_version"):
+        getattr(lib, name).restype = c_int
+    if lib.ttt_cfg_size() != ctypes.sizeof(ttt_cfg):
+        raise ImportError("ttt_cfg layout mismatch between the binding and the library")
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+# ----------------------------------------------------------------- C names
+def ttt_cfg_default() -> ttt_cfg:
+    c = ttt_cfg()
+    _lib.ttt_cfg_default(ctypes.byref(c))
+    return c
+
+
+def ttt_strerror(code: int) -> str:
+    return _lib.ttt_strerror(int(code)).decode()
+
+
+def ttt_abi_version() -> int:
+    return _lib.ttt_abi_version()
+
+
+def ttt_select_impl(cfg: ttt_cfg) -> int:
+    return _lib.ttt_select_impl(ctypes.byref(cfg))
+
+
+def ttt_workspace_bytes(cfg: ttt_cfg) -> int:
+    n = c_size_t(0)
+    rc = _lib.ttt_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_workspace_bytes")
+    return n.value
+
+
+def ttt_host_arena_bytes(cfg: ttt_cfg) -> int:
+    n = c_size_t(0)
+    rc = _lib.ttt_host_arena_bytes(ctypes.byref(cfg), ctypes.byref(n))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_host_arena_bytes")
+    return n.value
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def ttt_fwd(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_3,
+            workspace, stream=None, check: bool = True) -> int:
+    """Enqueue the layer on `stream` (torch tensors on the GPU). Returns the status."""
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.ttt_fwd(ctypes.byref(cfg), _ptr(Q), _ptr(K), _ptr(V), _ptr(lr), _ptr(W0_1),
+                      _ptr(W0_2), _ptr(W0_3), _ptr(O), _ptr(Wf_1), _ptr(Wf_2), _ptr(Wf_3),
+                      _ptr(workspace), nbytes, _stream_handle(stream))
+    if check and rc != TTT_OK:
+        raise TTTError(rc, "ttt_fwd")
+    return rc
+
+
+def ttt_status(workspace, stream=None) -> int:
+    return _lib.ttt_status(_ptr(workspace), _stream_handle(stream))
+
+
+def ttt_fwd_host(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_3,
+                 arena, stream=None, check: bool = True) -> int:
+    """The layer on host tensors (pinned for full bandwidth); synchronous."""
+    nbytes = arena.numel() * arena.element_size()
+    rc = _lib.ttt_fwd_host(ctypes.byref(cfg), _ptr(Q), _ptr(K), _ptr(V), _ptr(lr), _ptr(W0_1),
+                           _ptr(W0_2), _ptr(W0_3), _ptr(O), _ptr(Wf_1), _ptr(Wf_2), _ptr(Wf_3),
+                           _ptr(arena), nbytes, _stream_handle(stream))
+    if check and rc != TTT_OK:
+        raise TTTError(rc, "ttt_fwd_host")
+    return rc
+
+
+# ----------------------------------------------------------------- helpers
+class CfgHolder:
+    """A ttt_cfg plus the host update-mask buffer it points to (kept alive)."""
+
+    def __init__(self, cfg: ttt_cfg, mask: Optional[np.ndarray]):
+        self.cfg = cfg
+        self.mask = mask
+
+
+def cfg_from_spec(spec, impl: int = TTT_IMPL_AUTO, check_finite: bool = False,
+                  timeout_us: int = 0, T: Optional[int] = None) -> CfgHolder:
+    """A ttt_cfg for a LayerSpec-like workload description."""
+    c = ttt_cfg_default()
+    c.B, c.H = spec.B, spec.H
+    c.T = spec.T if T is None else T
+    c.d, c.dh, c.chunk = spec.d, spec.dh, spec.chunk
+    c.fast_net = TTT_NET_SWIGLU if spec.fast_net == "swiglu" else TTT_NET_LINEAR
+    c.loss = TTT_LOSS_IP if spec.loss == "ip" else TTT_LOSS_MSE
+    c.mode = TTT_MODE_SHIFTED if spec.mode == "shifted" else TTT_MODE_SINGLE
+    c.dtype = TTT_DTYPE_F32 if spec.dtype == "fp32" else TTT_DTYPE_BF16
+    c.muon = int(spec.muon)
+    c.ns_iters = spec.ns_iters
+    c.wnorm = int(spec.wnorm)
+    c.step = spec.step
+    c.impl = impl
+    c.check_finite = int(check_finite)
+    c.timeout_us = timeout_us
+    n_chunks = (c.T + c.chunk - 1) // c.chunk
+    mask = np.ascontiguousarray(spec.replace(T=c.T).update_mask(), dtype=np.uint8)
+    assert mask.size == n_chunks
+    if mask.all():
+        mask = None
+    else:
+        c.update_mask = mask.ctypes.data
+    return CfgHolder(c, mask)
+
+
+def weight_shapes(cfg: ttt_cfg) -> Sequence[tuple]:
+    if cfg.fast_net == TTT_NET_SWIGLU:
+        return [(cfg.dh, cfg.d), (cfg.d, cfg.dh), (cfg.dh, cfg.d)]
+    return [(cfg.d, cfg.d)]
+
+
+def layer(holder: CfgHolder, Q, K, V, lr, W0: Sequence, stream=None, sync: bool = True):
+    """Allocate outputs and workspace (torch, on Q's device) and run ttt_fwd.
+
+    Returns (O, [Wf...]). With ``sync`` the status word is read back and a
+    device-side error raises TTTError.
+    """
+    import torch
+    cfg = holder.cfg
+    dev = Q.device
+    O = torch.empty_like(Q)
+    Wf = [torch.empty((cfg.B, cfg.H) + s, dtype=torch.float32, device=dev)
+          for s in weight_shapes(cfg)]
+    ws = torch.empty(ttt_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    w0 = list(W0) + [None] * (3 - len(W0))
+    wf = Wf + [None] * (3 - len(Wf))
+    ttt_fwd(cfg, Q, K, V, lr, w0[0], w0[1], w0[2], O, wf[0], wf[1], wf[2], ws, stream)
+    if sync:
+        rc = ttt_status(ws, stream)
+        if rc != TTT_OK:
+            raise TTTError(rc, "ttt_fwd (device)")
+    return O, Wf

@@ -1,0 +1,320 @@
+// C-ABI front end: argument validation, kernel-family selection, workspace
+// planning, the device status word and the host-buffer wrapper.
+#include <cmath>
+#include <cstring>
+
+#include "ttt_common.cuh"
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+int elem_bytes(int dtype) { return dtype == TTT_DTYPE_F32 ? 4 : 2; }
+
+int validate_cfg(const ttt_cfg* g) {
+  if (!g) return TTT_ERR_ARG;
+  if (g->B < 1 || g->H < 1 || g->T < 1 || g->d < 1 || g->chunk < 1) return TTT_ERR_ARG;
+  if (g->fast_net != TTT_NET_SWIGLU && g->fast_net != TTT_NET_LINEAR) return TTT_ERR_ARG;
+  if (g->fast_net == TTT_NET_SWIGLU && g->dh < 1) return TTT_ERR_ARG;
+  if (g->loss != TTT_LOSS_IP && g->loss != TTT_LOSS_MSE) return TTT_ERR_ARG;
+  if (g->mode != TTT_MODE_SHIFTED && g->mode != TTT_MODE_SINGLE) return TTT_ERR_ARG;
+  if (g->dtype != TTT_DTYPE_F32 && g->dtype != TTT_DTYPE_BF16) return TTT_ERR_ARG;
+  if ((g->muon != 0 && g->muon != 1) || (g->wnorm != 0 && g->wnorm != 1)) return TTT_ERR_ARG;
+  if (g->ns_iters < 0 || g->ns_iters > 64) return TTT_ERR_ARG;
+  if (!std::isfinite(g->ns_a) || !std::isfinite(g->ns_b) || !std::isfinite(g->ns_c)) return TTT_ERR_ARG;
+  if (!std::isfinite(g->ns_eps) || g->ns_eps < 0.f) return TTT_ERR_ARG;
+  if (!std::isfinite(g->wnorm_eps) || !(g->wnorm_eps > 0.f)) return TTT_ERR_ARG;
+  if (!std::isfinite(g->step)) return TTT_ERR_ARG;
+  if (g->w0_per_batch != 0 && g->w0_per_batch != 1) return TTT_ERR_ARG;
+  if (g->check_finite != 0 && g->check_finite != 1) return TTT_ERR_ARG;
+  if (g->impl < TTT_IMPL_AUTO || g->impl > TTT_IMPL_LINEAR) return TTT_ERR_ARG;
+  const int64_t tok = (int64_t)g->B * g->H * g->T;
+  if (tok * g->d > kMaxElems) return TTT_ERR_ARG;
+  const int64_t wd = g->fast_net == TTT_NET_SWIGLU ? (int64_t)g->d * g->dh : (int64_t)g->d * g->d;
+  if ((int64_t)g->B * g->H * wd > kMaxElems) return TTT_ERR_ARG;
+  return TTT_OK;
+}
+
+int select_impl(const ttt_cfg& g) {
+  switch (g.impl) {
+    case TTT_IMPL_SIMT: return TTT_IMPL_SIMT;
+    case TTT_IMPL_TC: return tc_supported(g) ? TTT_IMPL_TC : TTT_ERR_UNSUPPORTED;
+    case TTT_IMPL_LINEAR: return linear_supported(g) ? TTT_IMPL_LINEAR : TTT_ERR_UNSUPPORTED;
+    default: break;
+  }
+  if (g.dtype == TTT_DTYPE_BF16) {
+    if (tc_supported(g)) return TTT_IMPL_TC;
+    if (linear_supported(g)) return TTT_IMPL_LINEAR;
+  }
+  return TTT_IMPL_SIMT;
+}
+
+size_t impl_workspace(const ttt_cfg& g, int impl) {
+  switch (impl) {
+    case TTT_IMPL_TC: return tc_workspace_bytes(g);
+    case TTT_IMPL_LINEAR: return linear_workspace_bytes(g);
+    default: return simt_workspace_bytes(g);
+  }
+}
+
+struct Range {
+  const char* p;
+  size_t n;
+};
+
+bool overlap(const Range& a, const Range& b) {
+  if (!a.p || !b.p || !a.n || !b.n) return false;
+  return a.p < b.p + b.n && b.p < a.p + a.n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Sizes {
+  size_t tok_bytes, lr_bytes, w0_bytes[3], wf_bytes[3];
+  int nw;
+};
+
+Sizes tensor_sizes(const ttt_cfg& g) {
+  Sizes s{};
+  const size_t tok = (size_t)g.B * g.H * g.T;
+  s.tok_bytes = tok * g.d * elem_bytes(g.dtype);
+  s.lr_bytes = tok * sizeof(float);
+  s.nw = g.fast_net == TTT_NET_SWIGLU ? 3 : 1;
+  const size_t wsz = s.nw == 3 ? (size_t)g.d * g.dh : (size_t)g.d * g.d;
+  for (int j = 0; j < s.nw; ++j) {
+    s.w0_bytes[j] = (size_t)(g.w0_per_batch ? g.B : 1) * g.H * wsz * sizeof(float);
+    s.wf_bytes[j] = (size_t)g.B * g.H * wsz * sizeof(float);
+  }
+  return s;
+}
+
+__global__ void check_finite_kernel(const void* p, size_t n, int dtype, int* status) {
+  bool bad = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float v = ld_val(p, i, dtype);
+    bad |= !isfinite(v);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, TTT_ERR_NONFINITE);
+}
+
+}  // namespace
+
+int launch_check_finite(const Call& c) {
+  const ttt_cfg& g = c.cfg;
+  const Sizes s = tensor_sizes(g);
+  int* st = reinterpret_cast<int*>(c.ws);
+  const size_t ntok = s.tok_bytes / elem_bytes(g.dtype);
+  const void* tp[3] = {c.Q, c.K, c.V};
+  for (int i = 0; i < 3; ++i) check_finite_kernel<<<592, 256, 0, c.stream>>>(tp[i], ntok, g.dtype, st);
+  check_finite_kernel<<<592, 256, 0, c.stream>>>(c.lr, s.lr_bytes / 4, TTT_DTYPE_F32, st);
+  for (int j = 0; j < s.nw; ++j)
+    check_finite_kernel<<<592, 256, 0, c.stream>>>(c.W0[j], s.w0_bytes[j] / 4, TTT_DTYPE_F32, st);
+  return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+}  // namespace ttt
+
+using namespace ttt;
+
+extern "C" {
+
+void ttt_cfg_default(ttt_cfg* cfg) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->fast_net = TTT_NET_SWIGLU;
+  cfg->loss = TTT_LOSS_IP;
+  cfg->mode = TTT_MODE_SHIFTED;
+  cfg->dtype = TTT_DTYPE_BF16;
+  cfg->muon = 1;
+  cfg->ns_iters = 5;
+  cfg->ns_a = 3.4445f;
+  cfg->ns_b = -4.7750f;
+  cfg->ns_c = 2.0315f;
+  cfg->ns_eps = 1e-7f;
+  cfg->wnorm = 1;
+  cfg->wnorm_eps = 1e-12f;
+  cfg->step = 1.0f;
+  cfg->update_mask = nullptr;
+  cfg->w0_per_batch = 0;
+  cfg->check_finite = 0;
+  cfg->timeout_us = 2000000u;
+  cfg->impl = TTT_IMPL_AUTO;
+}
+
+int ttt_abi_version(void) { return kAbiVersion; }
+
+size_t ttt_cfg_size(void) { return sizeof(ttt_cfg); }
+
+int ttt_select_impl(const ttt_cfg* cfg) {
+  const int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  return select_impl(*cfg);
+}
+
+int ttt_workspace_bytes(const ttt_cfg* cfg, size_t* bytes) {
+  if (!bytes) return TTT_ERR_ARG;
+  const int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  const int impl = select_impl(*cfg);
+  if (impl < 0) return impl;
+  *bytes = impl_workspace(*cfg, impl);
+  return TTT_OK;
+}
+
+int ttt_fwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+            const float* W0_1, const float* W0_2, const float* W0_3, void* O, float* Wf_1,
+            float* Wf_2, float* Wf_3, void* workspace, size_t workspace_bytes, void* stream) {
+  int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  const ttt_cfg& g = *cfg;
+  const int impl = select_impl(g);
+  if (impl < 0) return impl;
+  const Sizes s = tensor_sizes(g);
+  const void* in[4] = {Q, K, V, lr};
+  for (const void* p : in)
+    if (!p || !aligned16(p)) return TTT_ERR_ARG;
+  const float* w0[3] = {W0_1, W0_2, W0_3};
+  float* wf[3] = {Wf_1, Wf_2, Wf_3};
+  for (int j = 0; j < s.nw; ++j)
+    if (!w0[j] || !wf[j] || !aligned16(w0[j]) || !aligned16(wf[j])) return TTT_ERR_ARG;
+  if (!O || !aligned16(O)) return TTT_ERR_ARG;
+  const size_t need = impl_workspace(g, impl);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return TTT_ERR_WORKSPACE;
+  // outputs may not overlap inputs, the workspace or each other
+  Range outs[4] = {{(const char*)O, s.tok_bytes}, {}, {}, {}};
+  for (int j = 0; j < s.nw; ++j) outs[1 + j] = {(const char*)wf[j], s.wf_bytes[j]};
+  Range others[8] = {{(const char*)Q, s.tok_bytes}, {(const char*)K, s.tok_bytes},
+                     {(const char*)V, s.tok_bytes}, {(const char*)lr, s.lr_bytes},
+                     {}, {}, {}, {(const char*)workspace, need}};
+  for (int j = 0; j < s.nw; ++j) others[4 + j] = {(const char*)w0[j], s.w0_bytes[j]};
+  for (int i = 0; i < 4; ++i) {
+    for (const Range& r : others)
+      if (overlap(outs[i], r)) return TTT_ERR_ARG;
+    for (int k = i + 1; k < 4; ++k)
+      if (overlap(outs[i], outs[k])) return TTT_ERR_ARG;
+  }
+  Call c{};
+  c.cfg = g;
+  if (c.cfg.timeout_us == 0) c.cfg.timeout_us = 2000000u;
+  c.n_chunks = (g.T + g.chunk - 1) / g.chunk;
+  c.nw = s.nw;
+  if (s.nw == 3) {
+    c.rows[0] = g.dh; c.cols[0] = g.d;
+    c.rows[1] = g.d;  c.cols[1] = g.dh;
+    c.rows[2] = g.dh; c.cols[2] = g.d;
+  } else {
+    c.rows[0] = g.d; c.cols[0] = g.d;
+  }
+  c.Q = Q; c.K = K; c.V = V; c.lr = lr;
+  for (int j = 0; j < 3; ++j) { c.W0[j] = j < s.nw ? w0[j] : nullptr; c.Wf[j] = j < s.nw ? wf[j] : nullptr; }
+  c.O = O;
+  c.ws = static_cast<char*>(workspace);
+  c.ws_bytes = workspace_bytes;
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.mask = g.update_mask;
+  c.mask_all = true;
+  if (g.update_mask)
+    for (int i = 0; i < c.n_chunks; ++i)
+      if (!g.update_mask[i]) { c.mask_all = false; break; }
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), c.stream) != cudaSuccess) return TTT_ERR_CUDA;
+  if (g.check_finite) {
+    v = launch_check_finite(c);
+    if (v != TTT_OK) return v;
+  }
+  switch (impl) {
+    case TTT_IMPL_TC: return tc_run(c);
+    case TTT_IMPL_LINEAR: return linear_run(c);
+    default: return simt_run(c);
+  }
+}
+
+int ttt_status(void* workspace, void* stream) {
+  if (!workspace) return TTT_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return TTT_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TTT_ERR_CUDA;
+  return word;
+}
+
+int ttt_host_arena_bytes(const ttt_cfg* cfg, size_t* bytes) {
+  if (!bytes) return TTT_ERR_ARG;
+  size_t ws = 0;
+  const int v = ttt_workspace_bytes(cfg, &ws);
+  if (v != TTT_OK) return v;
+  const Sizes s = tensor_sizes(*cfg);
+  size_t total = 4 * align_up(s.tok_bytes, 256) + align_up(s.lr_bytes, 256);
+  for (int j = 0; j < s.nw; ++j) total += align_up(s.w0_bytes[j], 256) + align_up(s.wf_bytes[j], 256);
+  *bytes = total + align_up(ws, 256);
+  return TTT_OK;
+}
+
+int ttt_fwd_host(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+                 const float* W0_1, const float* W0_2, const float* W0_3, void* O, float* Wf_1,
+                 float* Wf_2, float* Wf_3, void* arena, size_t arena_bytes, void* stream) {
+  size_t need = 0;
+  int v = ttt_host_arena_bytes(cfg, &need);
+  if (v != TTT_OK) return v;
+  if (!arena || (reinterpret_cast<uintptr_t>(arena) & 255u) || arena_bytes < need)
+    return TTT_ERR_WORKSPACE;
+  const ttt_cfg& g = *cfg;
+  const Sizes s = tensor_sizes(g);
+  const void* hin[4] = {Q, K, V, lr};
+  const size_t in_bytes[4] = {s.tok_bytes, s.tok_bytes, s.tok_bytes, s.lr_bytes};
+  const float* hw0[3] = {W0_1, W0_2, W0_3};
+  float* hwf[3] = {Wf_1, Wf_2, Wf_3};
+  for (const void* p : hin)
+    if (!p) return TTT_ERR_ARG;
+  if (!O) return TTT_ERR_ARG;
+  for (int j = 0; j < s.nw; ++j)
+    if (!hw0[j] || !hwf[j]) return TTT_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* p = static_cast<char*>(arena);
+  void* din[4];
+  for (int i = 0; i < 4; ++i) { din[i] = p; p += align_up(in_bytes[i], 256); }
+  float* dw0[3] = {nullptr, nullptr, nullptr};
+  float* dwf[3] = {nullptr, nullptr, nullptr};
+  for (int j = 0; j < s.nw; ++j) { dw0[j] = reinterpret_cast<float*>(p); p += align_up(s.w0_bytes[j], 256); }
+  void* dO = p;
+  p += align_up(s.tok_bytes, 256);
+  for (int j = 0; j < s.nw; ++j) { dwf[j] = reinterpret_cast<float*>(p); p += align_up(s.wf_bytes[j], 256); }
+  void* dws = p;
+  size_t ws_bytes = 0;
+  ttt_workspace_bytes(cfg, &ws_bytes);
+  for (int i = 0; i < 4; ++i)
+    if (cudaMemcpyAsync(din[i], hin[i], in_bytes[i], cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return TTT_ERR_CUDA;
+  for (int j = 0; j < s.nw; ++j)
+    if (cudaMemcpyAsync(dw0[j], hw0[j], s.w0_bytes[j], cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return TTT_ERR_CUDA;
+  v = ttt_fwd(cfg, din[0], din[1], din[2], static_cast<const float*>(din[3]), dw0[0], dw0[1], dw0[2],
+              dO, dwf[0], dwf[1], dwf[2], dws, ws_bytes, stream);
+  if (v != TTT_OK) return v;
+  if (cudaMemcpyAsync(O, dO, s.tok_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return TTT_ERR_CUDA;
+  for (int j = 0; j < s.nw; ++j)
+    if (cudaMemcpyAsync(hwf[j], dwf[j], s.wf_bytes[j], cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return TTT_ERR_CUDA;
+  return ttt_status(dws, stream);
+}
+
+const char* ttt_strerror(int status) {
+  switch (status) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_ARG: return "invalid argument (shape, NULL or misaligned pointer, or overlapping buffers)";
+    case TTT_ERR_UNSUPPORTED: return "configuration not covered by the selected kernel family";
+    case TTT_ERR_WORKSPACE: return "workspace NULL, misaligned or smaller than ttt_workspace_bytes()";
+    case TTT_ERR_CUDA: return "a CUDA runtime call failed";
+    case TTT_ERR_TIMEOUT: return "a device-side wait exceeded timeout_us";
+    case TTT_ERR_NONFINITE: return "an input holds NaN or Inf";
+    case TTT_ERR_DEVICE: return "a device-side consistency check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI front end and the kernel families.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ttt.h"
+
+namespace ttt {
+
+// A validated ttt_fwd request (host side).
+struct Call {
+  ttt_cfg cfg;
+  int n_chunks;
+  int nw;                       // fast-weight matrices: 3 (SwiGLU) or 1 (linear)
+  int rows[3], cols[3];         // out x in of each matrix
+  const void *Q, *K, *V;
+  const float* lr;
+  const float* W0[3];
+  void* O;
+  float* Wf[3];
+  char* ws;                     // workspace base (status word at offset 0)
+  size_t ws_bytes;
+  cudaStream_t stream;
+  bool mask_all;                // every chunk updates
+  const uint8_t* mask;          // host flags (may be NULL when mask_all)
+};
+
+inline bool call_updates(const Call& c, int chunk) {
+  return c.mask_all || c.mask[chunk] != 0;
+}
+
+// ---- SIMT fp32 family (any shape, one CTA per head) -----------------------
+size_t simt_workspace_bytes(const ttt_cfg& cfg);
+int simt_run(const Call& c);
+
+// ---- tensor-core bf16 family (tcgen05 / TMEM / TMA) ------------------------
+bool tc_supported(const ttt_cfg& cfg);
+size_t tc_workspace_bytes(const ttt_cfg& cfg);
+int tc_run(const Call& c);
+
+// ---- linear small-chunk family (persistent, W resident on chip) ------------
+bool linear_supported(const ttt_cfg& cfg);
+size_t linear_workspace_bytes(const ttt_cfg& cfg);
+int linear_run(const Call& c);
+
+// ---- misc ------------------------------------------------------------------
+int launch_check_finite(const Call& c);
+
+}  // namespace ttt

@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad requests before launching anything. No GPU needed:
+every ttt_fwd call here fails validation, so no pointer is ever dereferenced."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from long_seq_models_chunked_b300 import abi, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"TTT_API\s+[\w\s\*]+?\b(\w+)\s*\(", txt)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert "ttt_fwd" in names and len(names) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(abi.lib(), n)
+    assert set(abi.EXPORTED) <= set(names)
+
+
+def test_cfg_layout_and_defaults():
+    assert abi.lib().ttt_cfg_size() == ctypes.sizeof(abi.ttt_cfg)
+    c = abi.ttt_cfg_default()
+    assert (c.fast_net, c.loss, c.mode, c.dtype, c.muon, c.ns_iters, c.wnorm) == (0, 0, 0, 1, 1, 5, 1)
+    assert abs(c.ns_a - 3.4445) < 1e-6 and abs(c.ns_b + 4.775) < 1e-6 and abs(c.ns_c - 2.0315) < 1e-6
+    assert c.step == 1.0 and c.timeout_us == 2000000 and abi.ttt_abi_version() >= 1
+
+
+def test_workspace_query_and_selection():
+    for name, spec in synth.WORKLOADS.items():
+        h = abi.cfg_from_spec(spec)
+        assert abi.ttt_select_impl(h.cfg) >= 1, name
+        assert abi.ttt_workspace_bytes(h.cfg) >= 256, name
+        assert abi.ttt_host_arena_bytes(h.cfg) > abi.ttt_workspace_bytes(h.cfg)
+    tiny = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"]).cfg
+    assert abi.ttt_select_impl(tiny) == abi.TTT_IMPL_SIMT
+
+
+@pytest.mark.parametrize("field,value", [("B", 0), ("T", -1), ("d", 0), ("chunk", 0),
+                                         ("fast_net", 2), ("loss", 5), ("mode", 3),
+                                         ("dtype", 7), ("ns_iters", -1), ("wnorm_eps", 0.0),
+                                         ("impl", 9), ("muon", 2)])
+def test_bad_cfg_is_rejected(field, value):
+    c = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"]).cfg
+    setattr(c, field, value)
+    assert abi.ttt_select_impl(c) == abi.TTT_ERR_ARG
+    with pytest.raises(abi.TTTError):
+        abi.ttt_workspace_bytes(c)
+
+
+def _fake(n):  # distinct, 256-aligned, never dereferenced
+    return 0x10000000 + n * 0x1000000
+
+
+def _call(c, **over):
+    p = dict(Q=_fake(1), K=_fake(2), V=_fake(3), lr=_fake(4), W1=_fake(5), W2=_fake(6),
+             W3=_fake(7), O=_fake(8), F1=_fake(9), F2=_fake(10), F3=_fake(11), ws=_fake(12),
+             ws_bytes=abi.ttt_workspace_bytes(c))
+    p.update(over)
+    return abi.lib().ttt_fwd(ctypes.byref(c), p["Q"], p["K"], p["V"], p["lr"], p["W1"],
+                             p["W2"], p["W3"], p["O"], p["F1"], p["F2"], p["F3"], p["ws"],
+                             p["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Q=0), abi.TTT_ERR_ARG),
+    (dict(lr=_fake(4) + 4), abi.TTT_ERR_ARG),          # misaligned
+    (dict(W2=0), abi.TTT_ERR_ARG),
+    (dict(O=_fake(1)), abi.TTT_ERR_ARG),               # O aliases Q
+    (dict(F2=_fake(9)), abi.TTT_ERR_ARG),              # two outputs alias
+    (dict(O=_fake(12) + 256), abi.TTT_ERR_ARG),        # output inside the workspace
+    (dict(ws=0), abi.TTT_ERR_WORKSPACE),
+    (dict(ws=_fake(12) + 16), abi.TTT_ERR_WORKSPACE),  # not 256-aligned
+    (dict(ws_bytes=255), abi.TTT_ERR_WORKSPACE),
+])
+def test_fwd_rejects_before_launch(over, code):
+    c = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"]).cfg
+    assert _call(c, **over) == code
+
+
+def test_strerror_covers_every_code():
+    for code in range(0, -8, -1):
+        assert abi.ttt_strerror(code) != "unknown status"
+    assert abi.ttt_strerror(12345) == "unknown status"
