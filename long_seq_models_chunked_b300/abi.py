@@ -33,7 +33,7 @@ TTT_IMPL_AUTO, TTT_IMPL_SIMT, TTT_IMPL_TC, TTT_IMPL_LINEAR = 0, 1, 2, 3
 
 EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_host_arena_bytes", "ttt_fwd_host", "ttt_select_impl", "ttt_strerror",
-            "ttt_abi_version", "ttt_cfg_size")
+            "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16")
 
 
 class ttt_cfg(ctypes.Structure):
@@ -78,6 +78,9 @@ def _load():
     for name in ("ttt_workspace_bytes", "ttt_host_arena_bytes", "ttt_fwd", "ttt_fwd_host",
                  "ttt_status", "ttt_select_impl", "ttt_abi_version"):
         getattr(lib, name).restype = c_int
+    lib.ttt_dbg_gemm_bf16.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
+                                      c_int, c_void_p]
+    lib.ttt_dbg_gemm_bf16.restype = c_int
     if lib.ttt_cfg_size() != ctypes.sizeof(ttt_cfg):
         raise ImportError("ttt_cfg layout mismatch between the binding and the library")
     return lib
@@ -168,6 +171,13 @@ def ttt_fwd_host(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_
     if check and rc != TTT_OK:
         raise TTTError(rc, "ttt_fwd_host")
     return rc
+
+
+def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: int, N: int, K: int,
+                      stream=None) -> int:
+    """Test hook: D[z] = A[z] B[z]^T on the tcgen05 tile kernel (include/ttt_debug.h)."""
+    return _lib.ttt_dbg_gemm_bf16(_ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N,
+                                  K, _stream_handle(stream))
 
 
 # ----------------------------------------------------------------- helpers
