@@ -54,6 +54,16 @@ enum { TTT_MODE_SHIFTED = 0, TTT_MODE_SINGLE = 1 };
 enum { TTT_DTYPE_F32 = 0, TTT_DTYPE_BF16 = 1 };
 /* kernel family: AUTO picks the fastest one that covers the request */
 enum { TTT_IMPL_AUTO = 0, TTT_IMPL_SIMT = 1, TTT_IMPL_TC = 2, TTT_IMPL_LINEAR = 3 };
+/* operand precision of the tensor-core family on the weight-update path
+ * (the forward of the keys, the gradient, Newton-Schulz):
+ *   SPLIT  every operand computed inside the layer is carried as a bf16 pair
+ *          (hi + lo) and every product takes the two or three bf16 MMAs that
+ *          keep ~16 significant bits; the fast weights, whose updates feed back
+ *          chunk after chunk, stay within the bf16 tier's tolerance of an exact
+ *          computation over long sequences of updates (default);
+ *   SINGLE one bf16 (fp16 inside Newton-Schulz) operand per product: fewer MMAs,
+ *          but the rounding is amplified from chunk to chunk. */
+enum { TTT_PREC_SPLIT = 0, TTT_PREC_SINGLE = 1 };
 
 /* Layer configuration. Fill it with ttt_cfg_default() and override fields. */
 typedef struct ttt_cfg {
@@ -78,11 +88,12 @@ typedef struct ttt_cfg {
   int32_t check_finite;   /* 1: scan the inputs first; NaN/Inf -> TTT_ERR_NONFINITE */
   uint32_t timeout_us;    /* limit of every device-side wait (default 2,000,000)  */
   int32_t impl;           /* TTT_IMPL_*                                           */
+  int32_t precision;      /* TTT_PREC_* (tensor-core family only)                 */
 } ttt_cfg;
 
 /* Fills *cfg with the defaults above (B = H = T = d = dh = chunk = 0, SwiGLU,
  * inner-product loss, shifted mode, bf16, Muon with 5 iterations, weight norm
- * on, step 1, AUTO). */
+ * on, step 1, AUTO, SPLIT precision). */
 TTT_API void ttt_cfg_default(ttt_cfg* cfg);
 
 /* Bytes of device workspace ttt_fwd needs for *cfg (and the path AUTO picks).

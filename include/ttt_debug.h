@@ -24,6 +24,35 @@ extern "C" {
 TTT_API int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, float* D,
                               int Z, int M, int N, int K, void* stream);
 
+/* ---- launch accounting and per-kernel timing ------------------------------
+ * Every kernel launch of the library is counted by class. With timing on, each
+ * launch is bracketed by CUDA events recorded on its own stream (a few
+ * microseconds of overhead per launch); the times resolve when read. */
+enum {
+  TTT_KERNEL_FWD = 0,     /* fused [A|B] = X[W1;W3]^T, Dm = V W2, SwiGLU (backward) epilogue */
+  TTT_KERNEL_APPLY = 1,   /* O = H_q W2^T                                                   */
+  TTT_KERNEL_GRAD = 2,    /* chunk gradients G1^T, G2, G3^T (+ split-K reduction)            */
+  TTT_KERNEL_GRAM = 3,    /* Newton-Schulz S = X X^T                                         */
+  TTT_KERNEL_POLY = 4,    /* Newton-Schulz P = bS + cS^2                                     */
+  TTT_KERNEL_XUPD = 5,    /* Newton-Schulz X <- aX + P X                                     */
+  TTT_KERNEL_UPDATE = 6,  /* W <- W - step U, row weight norm, shadows                        */
+  TTT_KERNEL_AUX = 7,     /* import/export of the weights, normalisation, finiteness scan     */
+  TTT_KERNEL_LINEAR = 8,  /* linear small-chunk persistent kernel                            */
+  TTT_KERNEL_SIMT = 9,    /* fp32 SIMT layer kernel                                          */
+  TTT_KERNEL_COUNT = 10
+};
+
+TTT_API void ttt_prof_enable(int on);
+/* Drops recorded timings and zeroes the launch counters. */
+TTT_API void ttt_prof_reset(void);
+/* Totals of one kernel class since the last reset: summed event time (ms), how
+ * many launches were timed, how many were launched. Waits for the recorded
+ * events. Returns TTT_OK or TTT_ERR_ARG. */
+TTT_API int ttt_prof_read(int kind, double* total_ms, long long* timed_launches, long long* launches);
+/* Kernel launches of every class since the last reset. */
+TTT_API long long ttt_launch_count(void);
+TTT_API const char* ttt_kernel_name(int kind);
+
 #ifdef __cplusplus
 }
 #endif

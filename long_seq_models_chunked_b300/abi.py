@@ -30,10 +30,15 @@ TTT_LOSS_IP, TTT_LOSS_MSE = 0, 1
 TTT_MODE_SHIFTED, TTT_MODE_SINGLE = 0, 1
 TTT_DTYPE_F32, TTT_DTYPE_BF16 = 0, 1
 TTT_IMPL_AUTO, TTT_IMPL_SIMT, TTT_IMPL_TC, TTT_IMPL_LINEAR = 0, 1, 2, 3
+TTT_PREC_SPLIT, TTT_PREC_SINGLE = 0, 1
 
 EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_host_arena_bytes", "ttt_fwd_host", "ttt_select_impl", "ttt_strerror",
-            "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16")
+            "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16", "ttt_prof_enable",
+            "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name")
+TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
+TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
+TTT_KERNEL_COUNT = 10
 
 
 class ttt_cfg(ctypes.Structure):
@@ -44,7 +49,7 @@ class ttt_cfg(ctypes.Structure):
         ("ns_a", c_float), ("ns_b", c_float), ("ns_c", c_float), ("ns_eps", c_float),
         ("wnorm", c_int32), ("wnorm_eps", c_float), ("step", c_float),
         ("update_mask", c_void_p), ("w0_per_batch", c_int32), ("check_finite", c_int32),
-        ("timeout_us", c_uint32), ("impl", c_int32),
+        ("timeout_us", c_uint32), ("impl", c_int32), ("precision", c_int32),
     ]
 
 
@@ -81,6 +86,17 @@ def _load():
     lib.ttt_dbg_gemm_bf16.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                       c_int, c_void_p]
     lib.ttt_dbg_gemm_bf16.restype = c_int
+    lib.ttt_prof_enable.argtypes = [c_int]
+    lib.ttt_prof_enable.restype = None
+    lib.ttt_prof_reset.argtypes = []
+    lib.ttt_prof_reset.restype = None
+    lib.ttt_prof_read.argtypes = [c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong),
+                                  ctypes.POINTER(ctypes.c_longlong)]
+    lib.ttt_prof_read.restype = c_int
+    lib.ttt_launch_count.argtypes = []
+    lib.ttt_launch_count.restype = ctypes.c_longlong
+    lib.ttt_kernel_name.argtypes = [c_int]
+    lib.ttt_kernel_name.restype = ctypes.c_char_p
     if lib.ttt_cfg_size() != ctypes.sizeof(ttt_cfg):
         raise ImportError("ttt_cfg layout mismatch between the binding and the library")
     return lib
@@ -180,6 +196,31 @@ def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: in
                                   K, _stream_handle(stream))
 
 
+def ttt_prof_enable(on: bool) -> None:
+    _lib.ttt_prof_enable(int(on))
+
+
+def ttt_prof_reset() -> None:
+    _lib.ttt_prof_reset()
+
+
+def ttt_prof_read(kind: int):
+    """(total event ms, timed launches, launches) of one kernel class since the last reset."""
+    ms, timed, n = ctypes.c_double(0), ctypes.c_longlong(0), ctypes.c_longlong(0)
+    rc = _lib.ttt_prof_read(kind, ctypes.byref(ms), ctypes.byref(timed), ctypes.byref(n))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_prof_read")
+    return ms.value, timed.value, n.value
+
+
+def ttt_launch_count() -> int:
+    return _lib.ttt_launch_count()
+
+
+def ttt_kernel_name(kind: int) -> str:
+    return _lib.ttt_kernel_name(kind).decode()
+
+
 # ----------------------------------------------------------------- helpers
 class CfgHolder:
     """A ttt_cfg plus the host update-mask buffer it points to (kept alive)."""
@@ -190,7 +231,8 @@ class CfgHolder:
 
 
 def cfg_from_spec(spec, impl: int = TTT_IMPL_AUTO, check_finite: bool = False,
-                  timeout_us: int = 0, T: Optional[int] = None) -> CfgHolder:
+                  timeout_us: int = 0, T: Optional[int] = None,
+                  precision: int = TTT_PREC_SPLIT) -> CfgHolder:
     """A ttt_cfg for a LayerSpec-like workload description."""
     c = ttt_cfg_default()
     c.B, c.H = spec.B, spec.H
@@ -205,6 +247,7 @@ def cfg_from_spec(spec, impl: int = TTT_IMPL_AUTO, check_finite: bool = False,
     c.wnorm = int(spec.wnorm)
     c.step = spec.step
     c.impl = impl
+    c.precision = precision
     c.check_finite = int(check_finite)
     c.timeout_us = timeout_us
     n_chunks = (c.T + c.chunk - 1) // c.chunk

@@ -31,6 +31,7 @@ int validate_cfg(const ttt_cfg* g) {
   if (g->w0_per_batch != 0 && g->w0_per_batch != 1) return TTT_ERR_ARG;
   if (g->check_finite != 0 && g->check_finite != 1) return TTT_ERR_ARG;
   if (g->impl < TTT_IMPL_AUTO || g->impl > TTT_IMPL_LINEAR) return TTT_ERR_ARG;
+  if (g->precision != TTT_PREC_SPLIT && g->precision != TTT_PREC_SINGLE) return TTT_ERR_ARG;
   const int64_t tok = (int64_t)g->B * g->H * g->T;
   if (tok * g->d > kMaxElems) return TTT_ERR_ARG;
   const int64_t wd = g->fast_net == TTT_NET_SWIGLU ? (int64_t)g->d * g->dh : (int64_t)g->d * g->d;
@@ -109,10 +110,12 @@ int launch_check_finite(const Call& c) {
   int* st = reinterpret_cast<int*>(c.ws);
   const size_t ntok = s.tok_bytes / elem_bytes(g.dtype);
   const void* tp[3] = {c.Q, c.K, c.V};
+  prof_before(TTT_KERNEL_AUX, c.stream);
   for (int i = 0; i < 3; ++i) check_finite_kernel<<<592, 256, 0, c.stream>>>(tp[i], ntok, g.dtype, st);
   check_finite_kernel<<<592, 256, 0, c.stream>>>(c.lr, s.lr_bytes / 4, TTT_DTYPE_F32, st);
   for (int j = 0; j < s.nw; ++j)
     check_finite_kernel<<<592, 256, 0, c.stream>>>(c.W0[j], s.w0_bytes[j] / 4, TTT_DTYPE_F32, st);
+  prof_after(TTT_KERNEL_AUX, c.stream);
   return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
@@ -143,6 +146,7 @@ void ttt_cfg_default(ttt_cfg* cfg) {
   cfg->check_finite = 0;
   cfg->timeout_us = 2000000u;
   cfg->impl = TTT_IMPL_AUTO;
+  cfg->precision = TTT_PREC_SPLIT;
 }
 
 int ttt_abi_version(void) { return kAbiVersion; }

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/ttt.h"
+#include "../../include/ttt_debug.h"
 
 namespace ttt {
 
@@ -47,5 +48,9 @@ int linear_run(const Call& c);
 
 // ---- misc ------------------------------------------------------------------
 int launch_check_finite(const Call& c);
+
+// Launch accounting (and optional event timing) around every kernel launch.
+void prof_before(int kind, cudaStream_t st);
+void prof_after(int kind, cudaStream_t st);
 
 }  // namespace ttt

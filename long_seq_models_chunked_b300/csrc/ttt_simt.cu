@@ -386,7 +386,9 @@ int simt_run(const Call& c) {
     for (int i = 0; i < c.n_chunks; ++i)
       if (c.mask[i]) a.mask.w[i >> 5] |= 1u << (i & 31);
   const unsigned heads = (unsigned)g.B * (unsigned)g.H;
+  prof_before(TTT_KERNEL_SIMT, c.stream);
   simt_layer_kernel<<<heads, kThreads, 0, c.stream>>>(a);
+  prof_after(TTT_KERNEL_SIMT, c.stream);
   return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 

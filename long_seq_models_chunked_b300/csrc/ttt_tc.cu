@@ -73,6 +73,29 @@ __device__ __forceinline__ void st_f16x32(f16* dst, const float* v) {
   }
 }
 
+// Stores 32 values as one fp16 operand (SINGLE) or as a bf16 hi/lo pair (SPLIT):
+// hi = bf16(v), lo = bf16(v - hi), so hi + lo carries ~16 significant bits.
+template <bool SPLIT>
+__device__ __forceinline__ void st_op32(void* hi, void* lo, size_t o, const float* v) {
+  if (SPLIT) {
+    float l[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
+    st_bf16x32(static_cast<bf16*>(hi) + o, v);
+    st_bf16x32(static_cast<bf16*>(lo) + o, l);
+  } else {
+    st_f16x32(static_cast<f16*>(hi) + o, v);
+  }
+}
+
+__device__ __forceinline__ void st_bf16pair32(bf16* hi, bf16* lo, const float* v) {
+  float l[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
+  st_bf16x32(hi, v);
+  st_bf16x32(lo, l);
+}
+
 __device__ __forceinline__ void st_f32x32(float* dst, const float* v) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -100,10 +123,12 @@ struct FwdOp {
   struct Params {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
     CUtensorMap mW;          // bf16 shadows [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
+    CUtensorMap mWl;         // low halves of the shadows (split precision)
     const float* lr;
     bf16* Hq;                // [BH][Cp][dh]
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
-    int d, dh, T, Cp, chunk_start, valid, q_tiles, k_tiles, n_tiles;
+    bf16* El;                // low halves of E (split precision)
+    int d, dh, T, Cp, chunk_start, valid, q_tiles, k_tiles, n_tiles, split;
     TcCommon cm;
   };
   struct Tile {
@@ -123,35 +148,47 @@ struct FwdOp {
     t.bh = blockIdx.y;
     return true;
   }
-  static __device__ int num_kblocks(const Params& p, const Tile& t) { return (t.is_k ? 2 : 1) * (p.d / BK); }
-  static __device__ uint32_t stage_tx(const Params& p, const Tile&, int kb) {
-    return kb < p.d / BK ? kABytes + 4 * kBox : kABytes + 2 * kBox;
+  // k-blocks: segment 0 ([A|B], the weights' hi then, when split, lo halves),
+  // then for key tiles segment 1 (Dm, same order). The keys/values are exact bf16,
+  // so W = hi + lo needs two products, not three.
+  static __device__ int seg0_blocks(const Params& p, const Tile& t) {
+    return (t.is_k && p.split ? 2 : 1) * (p.d / BK);
+  }
+  static __device__ int num_kblocks(const Params& p, const Tile& t) {
+    return t.is_k ? 2 * seg0_blocks(p, t) : seg0_blocks(p, t);
+  }
+  static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int kb) {
+    return kb < seg0_blocks(p, t) ? kABytes + 4 * kBox : kABytes + 2 * kBox;
   }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
     const int nk = p.d / BK;
+    const int n0 = seg0_blocks(p, t);
     const int z = t.bh * 3;
-    if (kb < nk) {
-      ptx::tma_load_3d(st, t.is_k ? &p.mK : &p.mQ, bar, kb * BK, p.chunk_start + t.row0, t.bh);
+    if (kb < n0) {
+      const int k = kb % nk;
+      const CUtensorMap* w = kb >= nk ? &p.mWl : &p.mW;
+      ptx::tma_load_3d(st, t.is_k ? &p.mK : &p.mQ, bar, k * BK, p.chunk_start + t.row0, t.bh);
       for (int g = 0; g < 2; ++g) {
-        ptx::tma_load_3d(st + kABytes + g * kBox, &p.mW, bar, t.j0 + g * 64, kb * BK, z + 0);
-        ptx::tma_load_3d(st + kABytes + (2 + g) * kBox, &p.mW, bar, t.j0 + g * 64, kb * BK, z + 2);
+        ptx::tma_load_3d(st + kABytes + g * kBox, w, bar, t.j0 + g * 64, k * BK, z + 0);
+        ptx::tma_load_3d(st + kABytes + (2 + g) * kBox, w, bar, t.j0 + g * 64, k * BK, z + 2);
       }
     } else {
-      const int k2 = kb - nk;
-      ptx::tma_load_3d(st, &p.mV, bar, k2 * BK, p.chunk_start + t.row0, t.bh);
+      const int k2 = kb - n0, k = k2 % nk;
+      const CUtensorMap* w = k2 >= nk ? &p.mWl : &p.mW;
+      ptx::tma_load_3d(st, &p.mV, bar, k * BK, p.chunk_start + t.row0, t.bh);
       for (int g = 0; g < 2; ++g)
-        ptx::tma_load_3d(st + kABytes + g * kBox, &p.mW, bar, t.j0 + g * 64, k2 * BK, z + 1);
+        ptx::tma_load_3d(st + kABytes + g * kBox, w, bar, t.j0 + g * 64, k * BK, z + 1);
     }
   }
-  static __device__ void consume(const Params& p, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    const int nk = p.d / BK;
+  static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
+    const int n0 = seg0_blocks(p, t);
     const uint32_t a = st, b = st + kABytes;
-    if (kb < nk) {
+    if (kb < n0) {
       constexpr uint32_t id = ptx::idesc_bf16(128, 256, false, true);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
     } else {
-      const int k2 = kb - nk;
+      const int k2 = kb - n0;
       constexpr uint32_t id = ptx::idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem + 256, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
@@ -174,7 +211,8 @@ struct FwdOp {
     } else {
       const float eta = valid ? p.lr[(size_t)t.bh * p.T + p.chunk_start + tl] : 0.f;
       const size_t plane = (size_t)p.Cp * p.dh;
-      bf16* dA = p.E + ((size_t)t.bh * 3 * p.Cp + tl) * p.dh + t.j0;
+      const size_t oA = ((size_t)t.bh * 3 * p.Cp + tl) * p.dh + t.j0;
+      bf16* dA = p.E + oA;
       bf16* dH = dA + plane;
       bf16* dB = dA + 2 * plane;
       float vd[32];
@@ -193,9 +231,15 @@ struct FwdOp {
           va[i] = g * b * sg * (1.f + a * (1.f - sg));
           vb[i] = g * s;
         }
-        st_bf16x32(dA + c, va);
-        st_bf16x32(dH + c, oh);
-        st_bf16x32(dB + c, vb);
+        if (p.split) {
+          st_bf16pair32(dA + c, p.El + oA + c, va);
+          st_bf16pair32(dH + c, p.El + oA + plane + c, oh);
+          st_bf16pair32(dB + c, p.El + oA + 2 * plane + c, vb);
+        } else {
+          st_bf16x32(dA + c, va);
+          st_bf16x32(dH + c, oh);
+          st_bf16x32(dB + c, vb);
+        }
       }
     }
   }
@@ -258,10 +302,12 @@ struct GOp {
     CUtensorMap mK4, mV4;  // 4D {d, C, n_full, BH}, box {64, 64, 1, 1}  (full chunks)
     CUtensorMap mK3, mV3;  // 3D {d, T, BH}, box {64, 64, 1}            (ragged last chunk)
     CUtensorMap mE;        // 3D {dh, Cp, 3BH}, box {64, 64, 1}
+    CUtensorMap mEl;       // low halves of E (split precision)
     float* G;              // [Z][d][dh] fp32   (splits == 1)
     float* part;           // [Z][part_stride] sums of squares per tile (splits == 1)
     float* split_out;      // [splits][Z][d][dh] fp32 (splits > 1)
     int d, dh, Z, chunk_idx, chunk_start, valid, use4d, m_tiles, n_tiles, splits, kb_per_split, part_stride;
+    int prec_split;        // E carried as hi + lo: two k passes over the tokens
     TcCommon cm;
   };
   struct Tile {
@@ -286,10 +332,11 @@ struct GOp {
     t.nkb = min(total, t.kb0 + p.kb_per_split) - t.kb0;
     return t.nkb > 0;
   }
-  static __device__ int num_kblocks(const Params&, const Tile& t) { return t.nkb; }
+  static __device__ int num_kblocks(const Params& p, const Tile& t) { return t.nkb * (p.prec_split ? 2 : 1); }
   static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    const int tok = (t.kb0 + kb) * BK;
+    const CUtensorMap* e = kb >= t.nkb ? &p.mEl : &p.mE;
+    const int tok = (t.kb0 + kb % t.nkb) * BK;
     for (int g = 0; g < 2; ++g) {
       if (p.use4d)
         ptx::tma_load_4d(st + g * kBox, t.j == 1 ? &p.mV4 : &p.mK4, bar, t.m0 + g * 64, tok, p.chunk_idx, t.bh);
@@ -297,7 +344,7 @@ struct GOp {
         ptx::tma_load_3d(st + g * kBox, t.j == 1 ? &p.mV3 : &p.mK3, bar, t.m0 + g * 64, p.chunk_start + tok, t.bh);
     }
 #pragma unroll
-    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, &p.mE, bar, t.n0 + g * 64, tok, t.z);
+    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, e, bar, t.n0 + g * 64, tok, t.z);
   }
   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
     constexpr uint32_t id = ptx::idesc_bf16(128, BN, true, true);
@@ -335,18 +382,26 @@ struct GOp {
 };
 
 // ============================================================ Newton-Schulz GEMMs
-// The iteration's operands are fp16 (11-bit significand, same tensor rate as
-// bf16): X is normalised first (|X|_F = 1), S = X X^T and P = bS + cS^2 stay
-// within a few units, so fp16's range holds them. fp32 is kept for X itself
-// (the aX term) and for S (the bS term).
+// Operands of the iteration: SINGLE precision uses one fp16 operand per matrix
+// (11-bit significand at the bf16 tensor rate; X is normalised first, so X, S
+// and P stay within fp16's range); SPLIT precision carries every operand as a
+// bf16 pair (hi, lo) and forms each product from three MMAs
+// (hi*hi + hi*lo + lo*hi, the lo*lo term is below the pair's resolution).
+// X itself (the aX term) and S (the bS term) are also kept in fp32.
+//
+// k-block order of a SPLIT product: [hi*hi | hi*lo | lo*hi], each over the full K.
+template <bool SPLIT>
+__device__ __forceinline__ int ns_part(int kb, int nk) { return SPLIT ? kb / nk : 0; }
+
 // Gram: S = X X^T (d x d, K = dh)
-template <int BN>
+template <int BN, bool SPLIT>
 struct GramOp {
   struct Params {
-    CUtensorMap mXa;  // X fp16 3D {dh, d, Z}, box {64, 128, 1}
-    CUtensorMap mXn;  // same buffer, box {64, BN, 1}
+    CUtensorMap mXa, mXal;  // X hi / lo 3D {dh, d, Z}, box {64, 128, 1}
+    CUtensorMap mXn, mXnl;  // same buffers, box {64, BN, 1}
     float* S;
-    f16* Sh;
+    void* Sh;
+    void* Sl;
     int d, dh, m_tiles, n_tiles;
     TcCommon cm;
   };
@@ -364,14 +419,15 @@ struct GramOp {
     t.z = blockIdx.y;
     return true;
   }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return p.dh / BK; }
+  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.dh / BK); }
   static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    ptx::tma_load_3d(st, &p.mXa, bar, kb * BK, t.m0, t.z);
-    ptx::tma_load_3d(st + kABytes, &p.mXn, bar, kb * BK, t.n0, t.z);
+    const int nk = p.dh / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
+    ptx::tma_load_3d(st, part == 2 ? &p.mXal : &p.mXa, bar, k * BK, t.m0, t.z);
+    ptx::tma_load_3d(st + kABytes, part == 1 ? &p.mXnl : &p.mXn, bar, k * BK, t.n0, t.z);
   }
   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, true);
+    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, !SPLIT);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), kdesc(st + kABytes, kk), id, (kb | kk) != 0);
   }
@@ -384,19 +440,20 @@ struct GramOp {
       if (m >= p.d || t.n0 + c >= p.d) continue;
       const size_t o = ((size_t)t.z * p.d + m) * p.d + t.n0 + c;
       st_f32x32(p.S + o, v);
-      st_f16x32(p.Sh + o, v);
+      st_op32<SPLIT>(p.Sh, p.Sl, o, v);
     }
   }
 };
 
-// Poly: P = b S + c S S  (d x d, K = d)
-template <int BN>
+// Poly: P = b S + c S S  (d x d, K = d; S is symmetric, so S^T serves as the B operand)
+template <int BN, bool SPLIT>
 struct PolyOp {
   struct Params {
-    CUtensorMap mSa;  // S fp16 3D {d, d, Z}, box {64, 128, 1}
-    CUtensorMap mSn;  // box {64, BN, 1}
+    CUtensorMap mSa, mSal;  // S hi / lo 3D {d, d, Z}, box {64, 128, 1}
+    CUtensorMap mSn, mSnl;  // box {64, BN, 1}
     const float* S;
-    f16* Ph;
+    void* Ph;
+    void* Pl;
     float b, c;
     int d, m_tiles, n_tiles;
     TcCommon cm;
@@ -415,14 +472,15 @@ struct PolyOp {
     t.z = blockIdx.y;
     return true;
   }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return p.d / BK; }
+  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.d / BK); }
   static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    ptx::tma_load_3d(st, &p.mSa, bar, kb * BK, t.m0, t.z);
-    ptx::tma_load_3d(st + kABytes, &p.mSn, bar, kb * BK, t.n0, t.z);
+    const int nk = p.d / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
+    ptx::tma_load_3d(st, part == 2 ? &p.mSal : &p.mSa, bar, k * BK, t.m0, t.z);
+    ptx::tma_load_3d(st + kABytes, part == 1 ? &p.mSnl : &p.mSn, bar, k * BK, t.n0, t.z);
   }
   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, true);
+    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, !SPLIT);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), kdesc(st + kABytes, kk), id, (kb | kk) != 0);
   }
@@ -437,19 +495,20 @@ struct PolyOp {
       ld_f32x32(p.S + o, s);
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = p.b * s[i] + p.c * v[i];
-      st_f16x32(p.Ph + o, v);
+      st_op32<SPLIT>(p.Ph, p.Pl, o, v);
     }
   }
 };
 
 // Xupd: X <- a X + P X  (d x dh, K = d); P K-major, X as the MN-major B operand.
-template <int BN>
+template <int BN, bool SPLIT>
 struct XupdOp {
   struct Params {
-    CUtensorMap mPa;  // P fp16 3D {d, d, Z}, box {64, 128, 1}
-    CUtensorMap mXm;  // current X fp16 3D {dh, d, Z}, box {64, 64, 1}
-    float* X;         // fp32 [Z][d][dh], updated in place
-    f16* Xh_next;     // fp16 copy of the new X
+    CUtensorMap mPa, mPal;  // P hi / lo 3D {d, d, Z}, box {64, 128, 1}
+    CUtensorMap mXm, mXml;  // current X hi / lo 3D {dh, d, Z}, box {64, 64, 1}
+    float* X;               // fp32 [Z][d][dh], updated in place
+    void* Xh_next;          // operand copy of the new X (hi)
+    void* Xl_next;          // (lo, SPLIT only)
     float a;
     int d, dh, m_tiles, n_tiles;
     TcCommon cm;
@@ -468,15 +527,17 @@ struct XupdOp {
     t.z = blockIdx.y;
     return true;
   }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return p.d / BK; }
+  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.d / BK); }
   static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    ptx::tma_load_3d(st, &p.mPa, bar, kb * BK, t.m0, t.z);
+    const int nk = p.d / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
+    ptx::tma_load_3d(st, part == 2 ? &p.mPal : &p.mPa, bar, k * BK, t.m0, t.z);
+    const CUtensorMap* xb = part == 1 ? &p.mXml : &p.mXm;
 #pragma unroll
-    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, &p.mXm, bar, t.n0 + g * 64, kb * BK, t.z);
+    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, xb, bar, t.n0 + g * 64, k * BK, t.z);
   }
   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, true, true);
+    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, true, !SPLIT);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), mdesc(st + kABytes, kk), id, (kb | kk) != 0);
   }
@@ -492,7 +553,7 @@ struct XupdOp {
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = p.a * x[i] + v[i];
       st_f32x32(p.X + o, x);
-      st_f16x32(p.Xh_next + o, x);
+      st_op32<SPLIT>(p.Xh_next, p.Xl_next, o, x);
     }
   }
 };
@@ -557,15 +618,23 @@ struct PlainOp {
 };
 
 // ============================================================ SIMT helper kernels
-// W0 (out x in, per head) -> M = [W1^T, W2, W3^T] fp32 + bf16 shadow, per (b, h).
-__global__ void import_kernel(const float* W1, const float* W2, const float* W3, float* M, bf16* Ms, int H,
-                              int d, int dh, int w0_per_batch) {
+__device__ __forceinline__ void st_shadow(bf16* hi, bf16* lo, size_t o, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  hi[o] = h;
+  if (lo) lo[o] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// W0 (out x in, per head) -> M = [W1^T, W2, W3^T] fp32 + bf16 shadow (hi, and lo
+// when the weights are carried split), per (b, h).
+__global__ void import_kernel(const float* W1, const float* W2, const float* W3, float* M, bf16* Ms, bf16* Msl,
+                              int H, int d, int dh, int w0_per_batch) {
   __shared__ float tile[32][33];
   const int z = blockIdx.z, bh = z / 3, j = z % 3;
   const int src_head = w0_per_batch ? bh : bh % H;
   const size_t n = (size_t)d * dh;
   float* dst = M + (size_t)z * n;
-  bf16* dsts = Ms + (size_t)z * n;
+  bf16* dh_ = Ms + (size_t)z * n;
+  bf16* dl_ = Msl ? Msl + (size_t)z * n : nullptr;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   if (j == 1) {
     const float* src = W2 + (size_t)src_head * n;  // [d][dh]
@@ -575,7 +644,7 @@ __global__ void import_kernel(const float* W1, const float* W2, const float* W3,
       if (r < d && c < dh) {
         const float v = src[(size_t)r * dh + c];
         dst[(size_t)r * dh + c] = v;
-        dsts[(size_t)r * dh + c] = __float2bfloat16_rn(v);
+        st_shadow(dh_, dl_, (size_t)r * dh + c, v);
       }
     }
     return;
@@ -593,7 +662,7 @@ __global__ void import_kernel(const float* W1, const float* W2, const float* W3,
     if (i < d && jj < dh) {
       const float v = tile[tx][rr];
       dst[(size_t)i * dh + jj] = v;
-      dsts[(size_t)i * dh + jj] = __float2bfloat16_rn(v);
+      st_shadow(dh_, dl_, (size_t)i * dh + jj, v);
     }
   }
 }
@@ -628,7 +697,6 @@ __global__ void export_kernel(const float* M, float* Wf1, float* Wf2, float* Wf3
 
 // Row norms of W0 in the internal layout: columns of M1/M3 (over d), rows of M2 (over dh).
 // One block of 256 threads per (z, 32-column slab) for j = 0, 2 and per (z, 8 rows) for j = 1.
-
 __global__ void norms_kernel(const float* M, float* n0, int d, int dh) {
   __shared__ float red[8][33];
   const int z = blockIdx.y, j = z % 3;
@@ -658,14 +726,16 @@ __global__ void norms_kernel(const float* M, float* n0, int d, int dh) {
   }
 }
 
-// M <- M - step*U; optional weight norm back to n0; refresh the bf16 shadow.
-__global__ void update_kernel(float* M, bf16* Ms, const float* U, const float* n0, float step, int wnorm,
-                              float floor_, int d, int dh) {
+// M <- M - step*U; optional weight norm back to n0 (LaCT page §2.2.1, eq. 8; the
+// rows of W1/W3 are the columns of M1/M3); refresh the bf16 shadow(s).
+__global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, const float* n0, float step,
+                              int wnorm, float floor_, int d, int dh) {
   __shared__ float red[8][33];
   const int z = blockIdx.y, j = z % 3;
   const size_t base = (size_t)z * d * dh;
   float* m = M + base;
   bf16* ms = Ms + base;
+  bf16* ml = Msl ? Msl + base : nullptr;
   const float* u = U + base;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (j == 1) {
@@ -682,7 +752,7 @@ __global__ void update_kernel(float* M, bf16* Ms, const float* U, const float* n
     for (int c = lane; c < dh; c += 32) {
       const float x = (m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c]) * sc;
       m[(size_t)r * dh + c] = x;
-      ms[(size_t)r * dh + c] = __float2bfloat16_rn(x);
+      st_shadow(ms, ml, (size_t)r * dh + c, x);
     }
   } else {
     if (blockIdx.x * 32 >= dh) return;
@@ -702,7 +772,7 @@ __global__ void update_kernel(float* M, bf16* Ms, const float* U, const float* n
       for (int r = w; r < d; r += 8) {
         const float x = (m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c]) * sc;
         m[(size_t)r * dh + c] = x;
-        ms[(size_t)r * dh + c] = __float2bfloat16_rn(x);
+        st_shadow(ms, ml, (size_t)r * dh + c, x);
       }
   }
 }
@@ -728,26 +798,39 @@ __global__ void gsplit_reduce_kernel(const float* parts, float* G, float* part, 
   if (threadIdx.x == 0) part[(size_t)z * part_stride + blockIdx.x] = red[0];
 }
 
-// X0 = G / (||G||_F + eps) in place (fp32) plus its fp16 operand copy. Every
-// block sums the per-tile squares of its matrix in the same order, so all of
-// them use the same norm.
-__global__ void ns_normalize_kernel(float* G, f16* Xh, const float* part, int n_part, int part_stride,
-                                    float eps, size_t per_z) {
+// X0 = G / (||G||_F + eps) in place (fp32) plus its operand copy (fp16, or a
+// bf16 hi/lo pair). Every block sums the per-tile squares of its matrix in the
+// same order, so all of them use the same norm.
+template <bool SPLIT>
+__global__ void ns_normalize_kernel(float* G, void* Xh, void* Xl, const float* part, int n_part,
+                                    int part_stride, float eps, size_t per_z) {
   const int z = blockIdx.y;
   float s = 0.f;
   for (int i = 0; i < n_part; ++i) s += part[(size_t)z * part_stride + i];
   const float inv = 1.f / (sqrtf(s) + eps);
   float* g = G + (size_t)z * per_z;
-  f16* xh = Xh + (size_t)z * per_z;
   for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < per_z;
        e += (size_t)gridDim.x * blockDim.x * 4) {
     float4 v = *reinterpret_cast<float4*>(g + e);
     v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
     *reinterpret_cast<float4*>(g + e) = v;
-    uint2 h;
-    h.x = pack_f16(v.x, v.y);
-    h.y = pack_f16(v.z, v.w);
-    *reinterpret_cast<uint2*>(xh + e) = h;
+    const size_t o = (size_t)z * per_z + e;
+    if (SPLIT) {
+      uint2 h, l;
+      h.x = pack_bf16(v.x, v.y);
+      h.y = pack_bf16(v.z, v.w);
+      const __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&h.x);
+      const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162*>(&h.y);
+      l.x = pack_bf16(v.x - __low2float(h0), v.y - __high2float(h0));
+      l.y = pack_bf16(v.z - __low2float(h1), v.w - __high2float(h1));
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(Xh) + o) = h;
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(Xl) + o) = l;
+    } else {
+      uint2 h;
+      h.x = pack_f16(v.x, v.y);
+      h.y = pack_f16(v.z, v.w);
+      *reinterpret_cast<uint2*>(static_cast<f16*>(Xh) + o) = h;
+    }
   }
 }
 
@@ -765,11 +848,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map over a row-major array with dims (innermost first) and box.
+// 16-bit tensor map over a row-major array with dims (innermost first) and box.
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || !base) return false;
   cuuint64_t gd[5], gs[4];
   cuuint32_t bx[5], es[5];
   uint64_t stride = 2;
@@ -793,25 +876,32 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
   return make_map(m, base, 3, dims, box, dt);
 }
 
-bool map3h(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
-  return map3(m, base, d0, d1, d2, b0, b1, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-}
-
 template <class Op>
-int launch_op(const typename Op::Params& p, dim3 grid, cudaStream_t st) {
+int launch_op(int kind, const typename Op::Params& p, dim3 grid, cudaStream_t st) {
   const size_t smem = tc_smem_bytes<Op>();
   if (cudaFuncSetAttribute(tc_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return TTT_ERR_CUDA;
+  prof_before(kind, st);
   tc_kernel<Op><<<grid, kTcThreads, smem, st>>>(p);
+  prof_after(kind, st);
   return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+// Plain kernel launch with accounting.
+#define TTT_LAUNCH(kind, st, ...)      \
+  do {                                 \
+    prof_before(kind, st);             \
+    __VA_ARGS__;                       \
+    prof_after(kind, st);              \
+    if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA; \
+  } while (0)
+
 struct Plan {
-  int BH, Z, d, dh, C, Cp, T;
+  int BH, Z, d, dh, C, Cp, T, split;
   int bn_o, bn_dd;        // N tile of the apply GEMM (over d) and of the d x d NS GEMMs
   int g_mt, g_nt, splits, kb_per_split, part_stride, reduce_blocks;
-  size_t off_M, off_Ms, off_n0, off_Hq, off_E, off_G, off_Xh0, off_Xh1, off_S, off_Sh, off_Ph, off_part,
-      off_split, total;
+  size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_S, off_Sh,
+      off_Sl, off_Ph, off_Pl, off_part, off_split, total;
 };
 
 int pick_bn_d(int d) {
@@ -827,6 +917,7 @@ Plan make_plan(const ttt_cfg& g) {
   P.d = g.d;
   P.dh = g.dh;
   P.T = g.T;
+  P.split = g.precision == TTT_PREC_SPLIT ? 1 : 0;
   P.C = std::min(g.chunk, g.T);
   P.Cp = (P.C + BM - 1) / BM * BM;
   P.bn_o = pick_bn_d(g.d);
@@ -843,6 +934,8 @@ Plan make_plan(const ttt_cfg& g) {
   P.reduce_blocks = 32;
   P.part_stride = std::max(P.g_mt * P.g_nt, P.reduce_blocks);
   const size_t wz = (size_t)P.Z * g.d * g.dh;
+  const size_t dd = (size_t)P.Z * g.d * g.d;
+  const size_t lo = P.split ? 1 : 0;  // the low halves exist only in split precision
   size_t off = kStatusBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -851,19 +944,74 @@ Plan make_plan(const ttt_cfg& g) {
   };
   P.off_M = take(wz * 4);
   P.off_Ms = take(wz * 2);
+  P.off_Msl = take(lo * wz * 2);
   P.off_n0 = take((size_t)P.Z * g.dh * 4);
   P.off_Hq = take((size_t)P.BH * P.Cp * g.dh * 2);
   P.off_E = take((size_t)P.BH * 3 * P.Cp * g.dh * 2);
+  P.off_El = take(lo * P.BH * 3 * P.Cp * g.dh * 2);
   P.off_G = take(wz * 4);
-  P.off_Xh0 = take(wz * 2);
-  P.off_Xh1 = take(wz * 2);
-  P.off_S = take((size_t)P.Z * g.d * g.d * 4);
-  P.off_Sh = take((size_t)P.Z * g.d * g.d * 2);
-  P.off_Ph = take((size_t)P.Z * g.d * g.d * 2);
+  for (int i = 0; i < 2; ++i) {
+    P.off_Xh[i] = take(wz * 2);
+    P.off_Xl[i] = take(lo * wz * 2);
+  }
+  P.off_S = take(dd * 4);
+  P.off_Sh = take(dd * 2);
+  P.off_Sl = take(lo * dd * 2);
+  P.off_Ph = take(dd * 2);
+  P.off_Pl = take(lo * dd * 2);
   P.off_part = take((size_t)P.Z * P.part_stride * 4);
   P.off_split = take(P.splits > 1 ? (size_t)P.splits * wz * 4 : 0);
   P.total = off;
   return P;
+}
+
+// Launches one Newton-Schulz iteration's three GEMMs for a fixed N tile choice.
+template <int BND, int BNX, bool SPLIT>
+int ns_iteration(const CUtensorMap* mXa, const CUtensorMap* mXn, const CUtensorMap* mXm, const CUtensorMap* mSa,
+                 const CUtensorMap* mSn, const CUtensorMap* mPa, float* X, void* xh_next, void* xl_next, float* S,
+                 void* Sh, void* Sl, void* Ph, void* Pl, const ttt_cfg& g, int Z, const TcCommon& cm,
+                 cudaStream_t st) {
+  const int d = g.d, dh = g.dh;
+  const int mt = (d + BM - 1) / BM, ntd = (d + BND - 1) / BND, ntx = dh / BNX;
+  {
+    typename GramOp<BND, SPLIT>::Params p{};
+    p.mXa = mXa[0]; p.mXal = mXa[1]; p.mXn = mXn[0]; p.mXnl = mXn[1];
+    p.S = S; p.Sh = Sh; p.Sl = Sl; p.d = d; p.dh = dh; p.m_tiles = mt; p.n_tiles = ntd; p.cm = cm;
+    const int r = launch_op<GramOp<BND, SPLIT>>(TTT_KERNEL_GRAM, p, dim3(mt * ntd, Z), st);
+    if (r != TTT_OK) return r;
+  }
+  {
+    typename PolyOp<BND, SPLIT>::Params p{};
+    p.mSa = mSa[0]; p.mSal = mSa[1]; p.mSn = mSn[0]; p.mSnl = mSn[1];
+    p.S = S; p.Ph = Ph; p.Pl = Pl; p.b = g.ns_b; p.c = g.ns_c; p.d = d; p.m_tiles = mt; p.n_tiles = ntd;
+    p.cm = cm;
+    const int r = launch_op<PolyOp<BND, SPLIT>>(TTT_KERNEL_POLY, p, dim3(mt * ntd, Z), st);
+    if (r != TTT_OK) return r;
+  }
+  typename XupdOp<BNX, SPLIT>::Params p{};
+  p.mPa = mPa[0]; p.mPal = mPa[1]; p.mXm = mXm[0]; p.mXml = mXm[1];
+  p.X = X; p.Xh_next = xh_next; p.Xl_next = xl_next; p.a = g.ns_a; p.d = d; p.dh = dh; p.m_tiles = mt;
+  p.n_tiles = ntx; p.cm = cm;
+  return launch_op<XupdOp<BNX, SPLIT>>(TTT_KERNEL_XUPD, p, dim3(mt * ntx, Z), st);
+}
+
+template <bool SPLIT>
+int ns_iteration_any(int bnd, int bnx, const CUtensorMap* mXa, const CUtensorMap* mXn, const CUtensorMap* mXm,
+                     const CUtensorMap* mSa, const CUtensorMap* mSn, const CUtensorMap* mPa, float* X,
+                     void* xh_next, void* xl_next, float* S, void* Sh, void* Sl, void* Ph, void* Pl,
+                     const ttt_cfg& g, int Z, const TcCommon& cm, cudaStream_t st) {
+#define TTT_NS_CASE(BD, BX)                                                                                  \
+  if (bnd == BD && bnx == BX)                                                                                 \
+    return ns_iteration<BD, BX, SPLIT>(mXa, mXn, mXm, mSa, mSn, mPa, X, xh_next, xl_next, S, Sh, Sl, Ph, Pl, \
+                                       g, Z, cm, st);
+  TTT_NS_CASE(256, 256)
+  TTT_NS_CASE(256, 128)
+  TTT_NS_CASE(192, 256)
+  TTT_NS_CASE(192, 128)
+  TTT_NS_CASE(128, 256)
+  TTT_NS_CASE(128, 128)
+#undef TTT_NS_CASE
+  return TTT_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -878,28 +1026,36 @@ size_t tc_workspace_bytes(const ttt_cfg& g) { return make_plan(g).total; }
 int tc_run(const Call& c) {
   const ttt_cfg& g = c.cfg;
   const Plan P = make_plan(g);
+  const bool split = P.split != 0;
   const cudaStream_t st = c.stream;
   char* ws = c.ws;
+  auto at = [&](size_t off, size_t n) -> void* { return n ? static_cast<void*>(ws + off) : nullptr; };
   float* M = reinterpret_cast<float*>(ws + P.off_M);
   bf16* Ms = reinterpret_cast<bf16*>(ws + P.off_Ms);
+  bf16* Msl = split ? reinterpret_cast<bf16*>(ws + P.off_Msl) : nullptr;
   float* n0 = reinterpret_cast<float*>(ws + P.off_n0);
   bf16* Hq = reinterpret_cast<bf16*>(ws + P.off_Hq);
   bf16* E = reinterpret_cast<bf16*>(ws + P.off_E);
+  bf16* El = split ? reinterpret_cast<bf16*>(ws + P.off_El) : nullptr;
   float* G = reinterpret_cast<float*>(ws + P.off_G);
-  f16* Xh[2] = {reinterpret_cast<f16*>(ws + P.off_Xh0), reinterpret_cast<f16*>(ws + P.off_Xh1)};
+  void* Xh[2] = {ws + P.off_Xh[0], ws + P.off_Xh[1]};
+  void* Xl[2] = {at(P.off_Xl[0], split), at(P.off_Xl[1], split)};
   float* S = reinterpret_cast<float*>(ws + P.off_S);
-  f16* Sh = reinterpret_cast<f16*>(ws + P.off_Sh);
-  f16* Ph = reinterpret_cast<f16*>(ws + P.off_Ph);
+  void* Sh = ws + P.off_Sh;
+  void* Sl = at(P.off_Sl, split);
+  void* Ph = ws + P.off_Ph;
+  void* Pl = at(P.off_Pl, split);
   float* part = reinterpret_cast<float*>(ws + P.off_part);
   float* splitbuf = reinterpret_cast<float*>(ws + P.off_split);
   int* status = reinterpret_cast<int*>(ws);
   const TcCommon cm{status, (unsigned long long)c.cfg.timeout_us * 1000ull};
   const int d = g.d, dh = g.dh, BH = P.BH, Z = P.Z, T = g.T;
   const int n_full = T / P.C;
+  const CUtensorMapDataType ns_dt = split ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
-  // ---- tensor maps
-  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW, mHq, mW2o, mE;
-  CUtensorMap mXa[2], mXn[2], mXm[2], mSa, mSn, mPa;
+  // ---- tensor maps ([0] = hi or single operand, [1] = lo; lo maps alias hi in SINGLE precision)
+  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mHq, mW2o, mE[2];
+  CUtensorMap mXa[2][2], mXn[2][2], mXm[2][2], mSa[2], mSn[2], mPa[2];
   bool ok = true;
   ok &= map3(&mQ, c.Q, d, T, BH, 64, 128);
   ok &= map3(&mK, c.K, d, T, BH, 64, 128);
@@ -908,16 +1064,14 @@ int tc_run(const Call& c) {
   ok &= map3(&mV3, c.V, d, T, BH, 64, 64);
   if (n_full > 0) {
     // 4D view {d, C, n_full, BH}: a chunk's token range ends at the chunk boundary
-    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)P.C, (uint64_t)n_full, (uint64_t)BH};
-    const uint32_t box[4] = {64, 64, 1, 1};
+    auto fn = encode_fn();
+    if (!fn) return TTT_ERR_CUDA;
     CUtensorMap* outs[2] = {&mK4, &mV4};
     const void* bases[2] = {c.K, c.V};
     for (int i = 0; i < 2; ++i) {
-      auto fn = encode_fn();
-      if (!fn) return TTT_ERR_CUDA;
-      cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+      cuuint64_t gd[4] = {(cuuint64_t)d, (cuuint64_t)P.C, (cuuint64_t)n_full, (cuuint64_t)BH};
       cuuint64_t gs[3] = {(cuuint64_t)d * 2, (cuuint64_t)P.C * d * 2, (cuuint64_t)T * d * 2};
-      cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+      cuuint32_t bx[4] = {64, 64, 1, 1};
       cuuint32_t es[4] = {1, 1, 1, 1};
       ok &= fn(outs[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]), gd, gs, bx, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -927,41 +1081,51 @@ int tc_run(const Call& c) {
     mK4 = mK3;
     mV4 = mV3;
   }
-  ok &= map3(&mW, Ms, dh, d, Z, 64, 64);
+  ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
+  ok &= map3(&mW[1], split ? Msl : Ms, dh, d, Z, 64, 64);
   ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
   ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
-  ok &= map3(&mE, E, dh, P.Cp, Z, 64, 64);
-  for (int i = 0; i < 2; ++i) {
-    ok &= map3h(&mXa[i], Xh[i], dh, d, Z, 64, 128);
-    ok &= map3h(&mXn[i], Xh[i], dh, d, Z, 64, P.bn_dd);
-    ok &= map3h(&mXm[i], Xh[i], dh, d, Z, 64, 64);
+  ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 64);
+  ok &= map3(&mE[1], split ? El : E, dh, P.Cp, Z, 64, 64);
+  for (int i = 0; i < 2; ++i)      // ping-pong buffer
+    for (int h = 0; h < 2; ++h) {  // hi / lo
+      const void* b = (h && split) ? Xl[i] : Xh[i];
+      ok &= map3(&mXa[i][h], b, dh, d, Z, 64, 128, ns_dt);
+      ok &= map3(&mXn[i][h], b, dh, d, Z, 64, P.bn_dd, ns_dt);
+      ok &= map3(&mXm[i][h], b, dh, d, Z, 64, 64, ns_dt);
+    }
+  for (int h = 0; h < 2; ++h) {
+    const void* sb = (h && split) ? Sl : Sh;
+    const void* pb = (h && split) ? Pl : Ph;
+    ok &= map3(&mSa[h], sb, d, d, Z, 64, 128, ns_dt);
+    ok &= map3(&mSn[h], sb, d, d, Z, 64, P.bn_dd, ns_dt);
+    ok &= map3(&mPa[h], pb, d, d, Z, 64, 128, ns_dt);
   }
-  ok &= map3h(&mSa, Sh, d, d, Z, 64, 128);
-  ok &= map3h(&mSn, Sh, d, d, Z, 64, P.bn_dd);
-  ok &= map3h(&mPa, Ph, d, d, Z, 64, 128);
   if (!ok) return TTT_ERR_CUDA;
 
   int rc;
   // ---- import W0, reference row norms
   {
-    dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
-    import_kernel<<<grid, 256, 0, st>>>(c.W0[0], c.W0[1], c.W0[2], M, Ms, g.H, d, dh, g.w0_per_batch);
-    dim3 gn(std::max((dh + 31) / 32, (d + 7) / 8), Z);
-    norms_kernel<<<gn, 256, 0, st>>>(M, n0, d, dh);
-    if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+    const dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
+    TTT_LAUNCH(TTT_KERNEL_AUX, st,
+               import_kernel<<<grid, 256, 0, st>>>(c.W0[0], c.W0[1], c.W0[2], M, Ms, Msl, g.H, d, dh,
+                                                   g.w0_per_batch));
+    const dim3 gn(std::max((dh + 31) / 32, (d + 7) / 8), Z);
+    TTT_LAUNCH(TTT_KERNEL_AUX, st, norms_kernel<<<gn, 256, 0, st>>>(M, n0, d, dh));
   }
 
   auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
     FwdOp::Params p{};
-    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW;
-    p.lr = c.lr; p.Hq = Hq; p.E = E;
+    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
+    p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     const int tiles = (valid + BM - 1) / BM;
     p.q_tiles = q ? tiles : 0;
     p.k_tiles = k ? tiles : 0;
     p.n_tiles = dh / 128;
+    p.split = split ? 1 : 0;
     p.cm = cm;
-    return launch_op<FwdOp>(p, dim3((p.q_tiles + p.k_tiles) * p.n_tiles, BH), st);
+    return launch_op<FwdOp>(TTT_KERNEL_FWD, p, dim3((p.q_tiles + p.k_tiles) * p.n_tiles, BH), st);
   };
   auto run_o = [&](int s, int valid) -> int {
     const int mt = (valid + BM - 1) / BM, nt = (d + P.bn_o - 1) / P.bn_o;
@@ -970,79 +1134,58 @@ int tc_run(const Call& c) {
       p.d = d; p.dh = dh; p.T = T; p.chunk_start = s; p.valid = valid; p.m_tiles = mt; p.n_tiles = nt; p.cm = cm;
     };
     const dim3 grid(mt * nt, BH);
-    if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(p, grid, st); }
-    if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(p, grid, st); }
-    typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(p, grid, st);
+    if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(TTT_KERNEL_APPLY, p, grid, st); }
+    if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, st); }
+    typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(TTT_KERNEL_APPLY, p, grid, st);
   };
   auto run_grad = [&](int ci, int s, int valid, int& n_part) -> int {
     const bool full = (s + P.C <= T) && ci < n_full;
-    auto fill = [&](auto& p) {
-      p.mK4 = mK4; p.mV4 = mV4; p.mK3 = mK3; p.mV3 = mV3; p.mE = mE;
-      p.G = G; p.part = part; p.split_out = splitbuf;
-      p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
-      p.m_tiles = P.g_mt; p.n_tiles = P.g_nt; p.splits = P.splits; p.kb_per_split = P.kb_per_split;
-      p.part_stride = P.part_stride; p.cm = cm;
-    };
     const int kbs = (valid + BK - 1) / BK;
     const int splits = (kbs + P.kb_per_split - 1) / P.kb_per_split;
+    auto fill = [&](auto& p) {
+      p.mK4 = mK4; p.mV4 = mV4; p.mK3 = mK3; p.mV3 = mV3; p.mE = mE[0]; p.mEl = mE[1];
+      p.G = G; p.part = part; p.split_out = splitbuf;
+      p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
+      p.m_tiles = P.g_mt; p.n_tiles = P.g_nt; p.splits = splits; p.kb_per_split = P.kb_per_split;
+      p.part_stride = P.part_stride; p.prec_split = split ? 1 : 0; p.cm = cm;
+    };
     const dim3 grid(P.g_mt * P.g_nt, Z, splits);
     int r;
-    if (dh % 256 == 0) { typename GOp<256>::Params p{}; fill(p); p.splits = splits; r = launch_op<GOp<256>>(p, grid, st); }
-    else { typename GOp<128>::Params p{}; fill(p); p.splits = splits; r = launch_op<GOp<128>>(p, grid, st); }
+    if (dh % 256 == 0) { typename GOp<256>::Params p{}; fill(p); r = launch_op<GOp<256>>(TTT_KERNEL_GRAD, p, grid, st); }
+    else { typename GOp<128>::Params p{}; fill(p); r = launch_op<GOp<128>>(TTT_KERNEL_GRAD, p, grid, st); }
     if (r != TTT_OK) return r;
-    if (splits > 1) {
-      gsplit_reduce_kernel<<<dim3(P.reduce_blocks, Z), 256, 0, st>>>(splitbuf, G, part, splits, Z,
-                                                                      (size_t)d * dh, P.part_stride);
-      if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
-    }
+    if (splits > 1)
+      TTT_LAUNCH(TTT_KERNEL_GRAD, st,
+                 gsplit_reduce_kernel<<<dim3(P.reduce_blocks, Z), 256, 0, st>>>(splitbuf, G, part, splits, Z,
+                                                                                 (size_t)d * dh, P.part_stride));
     n_part = splits > 1 ? P.reduce_blocks : P.g_mt * P.g_nt;
     return TTT_OK;
   };
   auto run_ns = [&](int n_part) -> int {
-    ns_normalize_kernel<<<dim3(16, Z), 256, 0, st>>>(G, Xh[0], part, n_part, P.part_stride, g.ns_eps,
-                                                    (size_t)d * dh);
-    if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
-    const int mt = (d + BM - 1) / BM, ntd = (d + P.bn_dd - 1) / P.bn_dd;
-    const int xbn = (dh % 256 == 0) ? 256 : 128;
-    const int ntx = dh / xbn;
+    if (split)
+      TTT_LAUNCH(TTT_KERNEL_AUX, st,
+                 ns_normalize_kernel<true><<<dim3(16, Z), 256, 0, st>>>(G, Xh[0], Xl[0], part, n_part,
+                                                                        P.part_stride, g.ns_eps, (size_t)d * dh));
+    else
+      TTT_LAUNCH(TTT_KERNEL_AUX, st,
+                 ns_normalize_kernel<false><<<dim3(16, Z), 256, 0, st>>>(G, Xh[0], Xl[0], part, n_part,
+                                                                         P.part_stride, g.ns_eps, (size_t)d * dh));
+    const int bnx = (dh % 256 == 0) ? 256 : 128;
     for (int it = 0; it < g.ns_iters; ++it) {
       const int cur = it & 1, nxt = cur ^ 1;
-      int r;
-      auto gram = [&](auto& p) {
-        p.mXa = mXa[cur]; p.mXn = mXn[cur]; p.S = S; p.Sh = Sh;
-        p.d = d; p.dh = dh; p.m_tiles = mt; p.n_tiles = ntd; p.cm = cm;
-      };
-      auto poly = [&](auto& p) {
-        p.mSa = mSa; p.mSn = mSn; p.S = S; p.Ph = Ph; p.b = g.ns_b; p.c = g.ns_c;
-        p.d = d; p.m_tiles = mt; p.n_tiles = ntd; p.cm = cm;
-      };
-      const dim3 gdd(mt * ntd, Z);
-      if (P.bn_dd == 256) {
-        typename GramOp<256>::Params a{}; gram(a); r = launch_op<GramOp<256>>(a, gdd, st);
-        if (r == TTT_OK) { typename PolyOp<256>::Params b{}; poly(b); r = launch_op<PolyOp<256>>(b, gdd, st); }
-      } else if (P.bn_dd == 192) {
-        typename GramOp<192>::Params a{}; gram(a); r = launch_op<GramOp<192>>(a, gdd, st);
-        if (r == TTT_OK) { typename PolyOp<192>::Params b{}; poly(b); r = launch_op<PolyOp<192>>(b, gdd, st); }
-      } else {
-        typename GramOp<128>::Params a{}; gram(a); r = launch_op<GramOp<128>>(a, gdd, st);
-        if (r == TTT_OK) { typename PolyOp<128>::Params b{}; poly(b); r = launch_op<PolyOp<128>>(b, gdd, st); }
-      }
-      if (r != TTT_OK) return r;
-      auto xup = [&](auto& p) {
-        p.mPa = mPa; p.mXm = mXm[cur]; p.X = G; p.Xh_next = Xh[nxt]; p.a = g.ns_a;
-        p.d = d; p.dh = dh; p.m_tiles = mt; p.n_tiles = ntx; p.cm = cm;
-      };
-      const dim3 gx(mt * ntx, Z);
-      if (xbn == 256) { typename XupdOp<256>::Params p{}; xup(p); r = launch_op<XupdOp<256>>(p, gx, st); }
-      else { typename XupdOp<128>::Params p{}; xup(p); r = launch_op<XupdOp<128>>(p, gx, st); }
+      const int r = split ? ns_iteration_any<true>(P.bn_dd, bnx, mXa[cur], mXn[cur], mXm[cur], mSa, mSn, mPa, G,
+                                                   Xh[nxt], Xl[nxt], S, Sh, Sl, Ph, Pl, g, Z, cm, st)
+                          : ns_iteration_any<false>(P.bn_dd, bnx, mXa[cur], mXn[cur], mXm[cur], mSa, mSn, mPa,
+                                                    G, Xh[nxt], Xl[nxt], S, Sh, Sl, Ph, Pl, g, Z, cm, st);
       if (r != TTT_OK) return r;
     }
     return TTT_OK;
   };
   auto run_update = [&]() -> int {
     const dim3 grid(std::max((dh + 31) / 32, (d + 7) / 8), Z);
-    update_kernel<<<grid, 256, 0, st>>>(M, Ms, G, n0, g.step, g.wnorm, g.wnorm_eps, d, dh);
-    return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+    TTT_LAUNCH(TTT_KERNEL_UPDATE, st,
+               update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, G, n0, g.step, g.wnorm, g.wnorm_eps, d, dh));
+    return TTT_OK;
   };
   auto do_update = [&](int ci, int s, int valid) -> int {
     int n_part = 0;
@@ -1075,9 +1218,8 @@ int tc_run(const Call& c) {
     if (rc != TTT_OK) return rc;
   }
   {
-    dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
-    export_kernel<<<grid, 256, 0, st>>>(M, c.Wf[0], c.Wf[1], c.Wf[2], d, dh);
-    if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+    const dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
+    TTT_LAUNCH(TTT_KERNEL_AUX, st, export_kernel<<<grid, 256, 0, st>>>(M, c.Wf[0], c.Wf[1], c.Wf[2], d, dh));
   }
   return TTT_OK;
 }
@@ -1103,7 +1245,7 @@ extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, i
     using Op = decltype(op);
     typename Op::Params p{};
     p.mA = mA; p.mB = mB; p.D = D; p.M = M; p.N = N; p.K = K; p.m_tiles = mt; p.n_tiles = nt; p.cm = cm;
-    return launch_op<Op>(p, grid, st);
+    return launch_op<Op>(TTT_KERNEL_AUX, p, grid, st);
   };
   if (a_mn_major && b_mn_major) return go(PlainOp<true, true>{});
   if (a_mn_major) return go(PlainOp<true, false>{});

@@ -59,3 +59,20 @@ def compare(spec, gpu, ref, tol: float):
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{spec.name}: {errs} (tol {tol})"
     return errs
+
+
+def full_workload_check(spec, heads, tol: float, block: int = 0, **gpu_kw):
+    """Run a full-size workload on the GPU and compare the sampled (b, h) heads
+    with the oracle, head by head (the oracle regenerates only those heads' exact
+    inputs). Returns {(b, h): errs}."""
+    x = synth.layer_inputs(spec, exact=False)
+    O, Wf = run_gpu(spec, x, **gpu_kw)
+    cfg = OracleCfg.from_spec(spec)
+    from oracle import ttt_head
+    out = {}
+    for (b, h) in heads:
+        ht = synth.head_tokens(spec, b, h)
+        w0 = [w[h].astype(np.float64) for w in x["W0"]]
+        Or, Wr = ttt_head(cfg, ht["Q64"], ht["K64"], ht["V64"], ht["lr"], w0, block=block)
+        out[(b, h)] = compare(spec, (O[b, h], [w[b, h] for w in Wf]), (Or, Wr), tol)
+    return out
