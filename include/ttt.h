@@ -46,6 +46,7 @@ extern "C" {
 #define TTT_ERR_TIMEOUT     -5  /* a device-side wait gave up (timeout_us)         */
 #define TTT_ERR_NONFINITE   -6  /* check_finite found a NaN/Inf in the inputs      */
 #define TTT_ERR_DEVICE      -7  /* a device-side consistency check failed          */
+#define TTT_ERR_SCRATCH_LIMIT -8 /* request needs more than the static scratch array */
 
 /* ---- enumerations -------------------------------------------------------- */
 enum { TTT_NET_SWIGLU = 0, TTT_NET_LINEAR = 1 };
@@ -145,6 +146,40 @@ TTT_API int ttt_fwd_host(const ttt_cfg* cfg,
                  const float* W0_1, const float* W0_2, const float* W0_3,
                  void* O, float* Wf_1, float* Wf_2, float* Wf_3,
                  void* arena, size_t arena_bytes, void* stream);
+
+/* ---- allocation-free variant ----------------------------------------------
+ * The pages define no such call; it serves callers that are given their input
+ * and output buffers but may not allocate device memory: a plugin running
+ * inside a host application that keeps all device memory in its own pool, or a
+ * latency-bound loop in which cudaMalloc/cudaFree (which can synchronise the
+ * whole device) are not allowed. Such callers cannot provide the workspace
+ * that ttt_fwd takes.
+ *
+ * ttt_fwd_static_scratch runs the fp32 SIMT kernel family (every
+ * configuration; cfg->impl must be TTT_IMPL_AUTO or TTT_IMPL_SIMT) with its
+ * scratch in one array of TTT_STATIC_SCRATCH_BYTES that the library holds in
+ * device memory, on every GPU that loads the library, until the process exits.
+ * Arguments are those of ttt_fwd without the workspace; `status` is an
+ * optional DEVICE int (NULL = not wanted) that receives the device-side status
+ * word (TTT_OK, TTT_ERR_NONFINITE, ...) once the layer has run on `stream`.
+ *
+ * - The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *   routine. It runs on the calling thread's current device.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture.
+ * - A request whose scratch (ttt_workspace_bytes with impl = SIMT) exceeds
+ *   TTT_STATIC_SCRATCH_BYTES returns TTT_ERR_SCRATCH_LIMIT before any launch.
+ * - Every call uses the same array, which keeps the previous call's contents
+ *   (the call clears what has to start at zero). Calls that overlap on the GPU
+ *   (other streams, other host threads) race on it: serialise them.
+ * Returns TTT_OK or a host-detected error, as ttt_fwd does. */
+#define TTT_STATIC_SCRATCH_BYTES (16u << 20)
+TTT_API int ttt_fwd_static_scratch(const ttt_cfg* cfg,
+            const void* Q, const void* K, const void* V, const float* lr,
+            const float* W0_1, const float* W0_2, const float* W0_3,
+            void* O, float* Wf_1, float* Wf_2, float* Wf_3,
+            int* status, void* stream);
 
 /* Which kernel family AUTO (or cfg->impl) resolves to for *cfg: TTT_IMPL_*,
  * or a negative status if none covers it. */

@@ -25,6 +25,8 @@ TTT_ERR_CUDA = -4
 TTT_ERR_TIMEOUT = -5
 TTT_ERR_NONFINITE = -6
 TTT_ERR_DEVICE = -7
+TTT_ERR_SCRATCH_LIMIT = -8
+TTT_STATIC_SCRATCH_BYTES = 16 << 20
 TTT_NET_SWIGLU, TTT_NET_LINEAR = 0, 1
 TTT_LOSS_IP, TTT_LOSS_MSE = 0, 1
 TTT_MODE_SHIFTED, TTT_MODE_SINGLE = 0, 1
@@ -35,7 +37,8 @@ TTT_PREC_SPLIT, TTT_PREC_SINGLE = 0, 1
 EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_host_arena_bytes", "ttt_fwd_host", "ttt_select_impl", "ttt_strerror",
             "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16", "ttt_prof_enable",
-            "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name")
+            "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name",
+            "ttt_fwd_static_scratch")
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
 TTT_KERNEL_COUNT = 10
@@ -74,6 +77,8 @@ def _load():
     lib.ttt_fwd.argtypes = [P, *ten, c_void_p, c_size_t, c_void_p]
     lib.ttt_fwd_host.argtypes = [P, *ten, c_void_p, c_size_t, c_void_p]
     lib.ttt_status.argtypes = [c_void_p, c_void_p]
+    lib.ttt_fwd_static_scratch.argtypes = [P, *ten, c_void_p, c_void_p]
+    lib.ttt_fwd_static_scratch.restype = c_int
     lib.ttt_select_impl.argtypes = [P]
     lib.ttt_strerror.argtypes = [c_int]
     lib.ttt_strerror.restype = ctypes.c_char_p
@@ -186,6 +191,19 @@ def ttt_fwd_host(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_
                            _ptr(arena), nbytes, _stream_handle(stream))
     if check and rc != TTT_OK:
         raise TTTError(rc, "ttt_fwd_host")
+    return rc
+
+
+def ttt_fwd_static_scratch(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_3,
+                           status=None, stream=None, check: bool = True) -> int:
+    """The allocation-free variant (fp32 SIMT family, library-held scratch):
+    same tensors as ttt_fwd minus the workspace; `status` is an optional device
+    int32 tensor that receives the device-side status word."""
+    rc = _lib.ttt_fwd_static_scratch(ctypes.byref(cfg), _ptr(Q), _ptr(K), _ptr(V), _ptr(lr), _ptr(W0_1),
+                                     _ptr(W0_2), _ptr(W0_3), _ptr(O), _ptr(Wf_1), _ptr(Wf_2), _ptr(Wf_3),
+                                     _ptr(status), _stream_handle(stream))
+    if check and rc != TTT_OK:
+        raise TTTError(rc, "ttt_fwd_static_scratch")
     return rc
 
 

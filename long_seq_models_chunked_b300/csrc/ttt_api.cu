@@ -317,6 +317,7 @@ const char* ttt_strerror(int status) {
     case TTT_ERR_TIMEOUT: return "a device-side wait exceeded timeout_us";
     case TTT_ERR_NONFINITE: return "an input holds NaN or Inf";
     case TTT_ERR_DEVICE: return "a device-side consistency check failed";
+    case TTT_ERR_SCRATCH_LIMIT: return "request needs more scratch than TTT_STATIC_SCRATCH_BYTES";
     default: return "unknown status";
   }
 }
