@@ -69,10 +69,13 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.02)   # the first sample marks the sampler as running
         except OSError:
             self.proc = None
         return self
@@ -172,6 +175,7 @@ def kernel_flops_per_launch(spec, kind: int, launches: int) -> float:
       apply  O = H W2^T: 2 d dh C
       grad   G1, G2, G3: 6 d dh C (updated chunks)
       gram / xupd  2 m^2 n per matrix and iteration; poly  2 m^3
+      ns (fused)   3 matrices x iters x (4 m^2 n + 2 m^3) per update
     """
     from long_seq_models_chunked_b300 import abi
     heads = spec.B * spec.H
@@ -188,6 +192,7 @@ def kernel_flops_per_launch(spec, kind: int, launches: int) -> float:
         abi.TTT_KERNEL_GRAM: heads * n_upd * 3 * spec.ns_iters * 2.0 * m * m * n if spec.muon else 0.0,
         abi.TTT_KERNEL_POLY: heads * n_upd * 3 * spec.ns_iters * 2.0 * m ** 3 if spec.muon else 0.0,
         abi.TTT_KERNEL_XUPD: heads * n_upd * 3 * spec.ns_iters * 2.0 * m * m * n if spec.muon else 0.0,
+        abi.TTT_KERNEL_NS: heads * n_upd * 3 * spec.ns_iters * (4.0 * m * m * n + 2.0 * m ** 3) if spec.muon else 0.0,
     }
     if spec.fast_net == "linear":
         tot = {abi.TTT_KERNEL_LINEAR: heads * (2.0 * d * d * T + 4.0 * d * d * upd_tok),
@@ -222,6 +227,14 @@ def read_traffic(kernel: str, workload: str):
 
 
 # ------------------------------------------------------------------ the GPU arm
+def workload_spec(args):
+    from long_seq_models_chunked_b300 import synth
+    spec = synth.WORKLOADS[args.workload]
+    if args.seq_len:
+        spec = spec.replace(T=args.seq_len, chunk=min(spec.chunk, args.seq_len))
+    return spec
+
+
 def run_ours(args, rank, local, world, pg):
     import numpy as np
     import torch
@@ -230,7 +243,7 @@ def run_ours(args, rank, local, world, pg):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = synth.WORKLOADS[args.workload]
+    spec = workload_spec(args)
     x = synth.layer_inputs(spec.replace(seed=spec.seed + 1000 * rank) if rank else spec, exact=False)
     holder = abi.cfg_from_spec(spec)
     cfg = holder.cfg
@@ -257,11 +270,13 @@ def run_ours(args, rank, local, world, pg):
     def step():
         abi.ttt_fwd(cfg, Q, K, V, lr, w0[0], w0[1], w0[2], O, wf[0], wf[1], wf[2], ws, stream)
 
+    clk = ClockSampler(local).__enter__()   # samples warm-up and timed steps (both under load)
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     rc = abi.ttt_status(ws, stream)
     if rc != abi.TTT_OK:
+        clk.__exit__(None, None, None)
         raise abi.TTTError(rc, "warm-up")
 
     # ---- timed region: device time per step, L2 flushed before each step
@@ -272,13 +287,13 @@ def run_ours(args, rank, local, world, pg):
     launches0 = abi.ttt_launch_count()
     barrier(pg, dev if world > 1 else None)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk.__exit__(None, None, None)
     barrier(pg, dev if world > 1 else None)
     launches = abi.ttt_launch_count() - launches0
     abi.ttt_prof_enable(False)
@@ -460,17 +475,18 @@ def run_reference(args, spec):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="lm_chunk2k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override T (small cases for profiling; not a bench configuration)")
     args = ap.parse_args()
 
-    from long_seq_models_chunked_b300 import synth
-    spec = synth.WORKLOADS[args.workload]
-    config = {"workload": spec.name, "B": spec.B, "H": spec.H, "T": spec.T, "d": spec.d, "dh": spec.dh,
+    spec = workload_spec(args)
+    config = {"workload": spec.name + (f" (T overridden to {spec.T})" if args.seq_len else ""), "B": spec.B, "H": spec.H, "T": spec.T, "d": spec.d, "dh": spec.dh,
               "chunk": spec.chunk, "fast_net": spec.fast_net, "loss": spec.loss, "mode": spec.mode,
               "muon": spec.muon, "ns_iters": spec.ns_iters, "wnorm": spec.wnorm, "update": spec.update,
               "storage": spec.dtype, "state": "fp32", "global_batch": spec.B, "seq_len": spec.T,

@@ -24,6 +24,29 @@ extern "C" {
 TTT_API int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, float* D,
                               int Z, int M, int N, int K, void* stream);
 
+/* CTAs of the fused Muon kernel's cooperative grid for *cfg on the current
+ * device; *resident (may be NULL) receives how many of its CTAs fit at once.
+ * Returns TTT_OK, TTT_ERR_ARG (cfg not on the tensor-core path) or TTT_ERR_CUDA. */
+TTT_API int ttt_dbg_ns_plan(const ttt_cfg* cfg, int* grid, int* resident);
+
+/* In TTT_PREC_SPLIT precision, which stages of the weight-update path carry
+ * split (bf16 hi + lo) operands: bit 0 the keys' forward (W = hi + lo), bit 1
+ * the gradient (E = hi + lo), bit 2 Newton-Schulz; a cleared bit gives that
+ * stage single operands. Default 7 (all). Process-global, for precision
+ * studies and tests. Returns TTT_OK or TTT_ERR_ARG. */
+TTT_API int ttt_dbg_split_mask(int mask);
+
+/* Caps the fused Muon kernel's grid at `ctas` CTAs (0 = one per SM, the
+ * default) for every later launch in this process. For tuning sweeps and tests.
+ * Returns TTT_OK or TTT_ERR_ARG. */
+TTT_API int ttt_dbg_ns_force_grid(int ctas);
+
+/* Failure-detection test: the next launch of the linear small-chunk kernel
+ * issues none of its loads, so its first wait (bounded by cfg->timeout_us)
+ * runs out; the kernel records TTT_ERR_TIMEOUT in the status word and returns
+ * with nothing in flight. Later launches are unaffected. */
+TTT_API void ttt_dbg_stall_next_linear(void);
+
 /* ---- launch accounting and per-kernel timing ------------------------------
  * Every kernel launch of the library is counted by class. With timing on, each
  * launch is bracketed by CUDA events recorded on its own stream (a few
@@ -39,7 +62,9 @@ enum {
   TTT_KERNEL_AUX = 7,     /* import/export of the weights, normalisation, finiteness scan     */
   TTT_KERNEL_LINEAR = 8,  /* linear small-chunk persistent kernel                            */
   TTT_KERNEL_SIMT = 9,    /* fp32 SIMT layer kernel                                          */
-  TTT_KERNEL_COUNT = 10
+  TTT_KERNEL_NS = 10,     /* fused Muon step: normalise, 5 Newton-Schulz iterations, update,
+                             row weight norm (one cooperative grid over every matrix)       */
+  TTT_KERNEL_COUNT = 11
 };
 
 TTT_API void ttt_prof_enable(int on);

@@ -38,10 +38,12 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_host_arena_bytes", "ttt_fwd_host", "ttt_select_impl", "ttt_strerror",
             "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16", "ttt_prof_enable",
             "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name",
-            "ttt_fwd_static_scratch")
+            "ttt_fwd_static_scratch", "ttt_dbg_ns_plan", "ttt_dbg_ns_force_grid",
+            "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear")
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
-TTT_KERNEL_COUNT = 10
+TTT_KERNEL_NS = 10
+TTT_KERNEL_COUNT = 11
 
 
 class ttt_cfg(ctypes.Structure):
@@ -91,6 +93,14 @@ def _load():
     lib.ttt_dbg_gemm_bf16.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                       c_int, c_void_p]
     lib.ttt_dbg_gemm_bf16.restype = c_int
+    lib.ttt_dbg_ns_plan.argtypes = [P, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
+    lib.ttt_dbg_ns_plan.restype = c_int
+    lib.ttt_dbg_ns_force_grid.argtypes = [c_int]
+    lib.ttt_dbg_ns_force_grid.restype = c_int
+    lib.ttt_dbg_split_mask.argtypes = [c_int]
+    lib.ttt_dbg_split_mask.restype = c_int
+    lib.ttt_dbg_stall_next_linear.argtypes = []
+    lib.ttt_dbg_stall_next_linear.restype = None
     lib.ttt_prof_enable.argtypes = [c_int]
     lib.ttt_prof_enable.restype = None
     lib.ttt_prof_reset.argtypes = []
@@ -212,6 +222,35 @@ def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: in
     """Test hook: D[z] = A[z] B[z]^T on the tcgen05 tile kernel (include/ttt_debug.h)."""
     return _lib.ttt_dbg_gemm_bf16(_ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N,
                                   K, _stream_handle(stream))
+
+
+def ttt_dbg_ns_plan(cfg: ttt_cfg):
+    """Test hook: (grid CTAs, CTAs resident at once) of the fused Muon kernel."""
+    grid, res = c_int(0), c_int(0)
+    rc = _lib.ttt_dbg_ns_plan(ctypes.byref(cfg), ctypes.byref(grid), ctypes.byref(res))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_ns_plan")
+    return grid.value, res.value
+
+
+def ttt_dbg_ns_force_grid(ctas: int) -> None:
+    """Test hook: cap the fused Muon kernel's grid (0 = one CTA per SM)."""
+    rc = _lib.ttt_dbg_ns_force_grid(int(ctas))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_ns_force_grid")
+
+
+def ttt_dbg_split_mask(mask: int) -> None:
+    """Test hook: stages with split operands in SPLIT precision (bit 0 keys'
+    forward, bit 1 gradient, bit 2 Newton-Schulz; default 7)."""
+    rc = _lib.ttt_dbg_split_mask(int(mask))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_split_mask")
+
+
+def ttt_dbg_stall_next_linear() -> None:
+    """Test hook: the next linear-kernel launch withholds its loads and times out."""
+    _lib.ttt_dbg_stall_next_linear()
 
 
 def ttt_prof_enable(on: bool) -> None:

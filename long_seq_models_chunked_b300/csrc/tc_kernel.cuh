@@ -62,6 +62,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const Tc
   }
 }
 
+// Waits, bounded by the timeout alone, for the copy tracked by `bar` to land.
+// Used after an abort: a CTA must not exit while a TMA copy into its shared
+// memory is still in flight, whatever the abort flag says.
+__device__ __forceinline__ void tc_drain(uint64_t* bar, uint32_t parity, const TcCommon& cm) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && globaltimer_ns() - t0 <= cm.timeout_ns) {
+  }
+}
+
 template <class Op>
 __host__ __device__ constexpr size_t tc_smem_bytes() {
   return (size_t)Op::kStages * Op::kStageBytes + 1024 + 512;
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
       if (*abort_flag) {
         // drain the copies this thread started before the CTA returns
         for (int kb = issued - Op::kStages > 0 ? issued - Op::kStages : 0; kb < issued; ++kb)
-          tc_wait(&full[kb % Op::kStages], (uint32_t)(kb / Op::kStages) & 1u, p.cm, abort_flag);
+          tc_drain(&full[kb % Op::kStages], (uint32_t)(kb / Op::kStages) & 1u, p.cm);
       }
     }
   } else if (warp == 1) {
@@ -131,6 +140,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         ptx::mma_commit(&empty[s]);
       }
       ptx::mma_commit(accb);
+      // after an abort nobody waits for the accumulator: the MMAs already issued
+      // must finish before TMEM is freed
+      if (*abort_flag) tc_drain(accb, 0, p.cm);
     }
   } else {
     const int g = warp & 3;  // TMEM lane group this warp may access

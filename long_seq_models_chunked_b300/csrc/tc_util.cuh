@@ -1,0 +1,153 @@
+// Helpers shared by the tensor-core kernels: operand packing and stores,
+// shared-memory descriptors of the 128-byte-swizzled tiles, and the host-side
+// TMA tensor-map construction.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tc_ptx.cuh"
+
+namespace ttt {
+namespace tcu {
+
+using bf16 = __nv_bfloat16;
+using f16 = __half;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr uint32_t kABytes = BM * BK * 2;   // K-major A tile, or two MN-major boxes
+constexpr uint32_t kBox = 64 * BK * 2;      // one 64 x 64 bf16 box (MN-major)
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_bf16x32(bf16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = w;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_f16x32(f16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_f16(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_f16(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_f16(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_f16(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = w;
+  }
+}
+
+// Stores 32 values as one fp16 operand (SINGLE) or as a bf16 hi/lo pair (SPLIT):
+// hi = bf16(v), lo = bf16(v - hi), so hi + lo carries ~16 significant bits.
+template <bool SPLIT>
+__device__ __forceinline__ void st_op32(void* hi, void* lo, size_t o, const float* v) {
+  if (SPLIT) {
+    float l[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
+    st_bf16x32(static_cast<bf16*>(hi) + o, v);
+    st_bf16x32(static_cast<bf16*>(lo) + o, l);
+  } else {
+    st_f16x32(static_cast<f16*>(hi) + o, v);
+  }
+}
+
+__device__ __forceinline__ void st_bf16pair32(bf16* hi, bf16* lo, const float* v) {
+  float l[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
+  st_bf16x32(hi, v);
+  st_bf16x32(lo, l);
+}
+
+__device__ __forceinline__ void st_f32x32(float* dst, const float* v) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+__device__ __forceinline__ void ld_f32x32(const float* src, float* v) {
+  const float4* s = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 x = s[q];
+    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+  }
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// K-major operand descriptor for K step kk of a 64-deep stage.
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) { return ptx::sdesc(base + kk * 32, 16, 1024); }
+// MN-major operand descriptor (64-wide groups kBox apart) for K step kk.
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, int kk) { return ptx::sdesc(base + kk * 2048, kBox, 1024); }
+
+__device__ __forceinline__ void st_shadow(bf16* hi, bf16* lo, size_t o, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  hi[o] = h;
+  if (lo) lo[o] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 16-bit tensor map over a row-major array with dims (innermost first) and box.
+inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  auto fn = encode_fn();
+  if (!fn || !base) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  uint64_t stride = 2;
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i > 0) gs[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = fn(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+          CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint32_t box[3] = {b0, b1, 1};
+  return make_map(m, base, 3, dims, box, dt);
+}
+
+}  // namespace tcu
+}  // namespace ttt

@@ -1,0 +1,37 @@
+// Fused Muon step (Newton-Schulz + update + weight norm) of the tensor-core path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/ttt.h"
+#include "tc_kernel.cuh"
+
+namespace ttt {
+
+struct NsFusedArgs {
+  const ttt_cfg* cfg;
+  int Z;                 // matrices: 3 per (batch, head)
+  bool split;            // SPLIT (bf16 hi/lo operands) or SINGLE (fp16) precision
+  float* X;              // [Z][d][dh] fp32: the chunk gradient on entry; U on exit
+  void* Xh[2];           // operand ping-pong buffers (hi)
+  void* Xl[2];           //                          (lo; SPLIT only)
+  void* Rh; void* Rl;    // R = X X^T + beta I operand (hi, lo), [Z][d][d] each
+  void* Ph; void* Pl;    // P operand (hi, lo)
+  float* M;              // [Z][d][dh] fp32 master weights, updated in place
+  void* Ms; void* Msl;   // bf16 shadows (hi, lo or nullptr)
+  const float* n0;       // [Z][dh] reference row norms
+  float* scratch;        // >= ns_fused_scratch_floats() floats (partial sums, barrier)
+  TcCommon cm;
+};
+
+bool ns_fused_supported(const ttt_cfg& g);
+size_t ns_fused_scratch_floats(const ttt_cfg& g, int Z);
+// CTAs of the fused kernel's cooperative grid (<= 0: it cannot be launched);
+// *resident (optional) receives how many CTAs fit on the device at once.
+int ns_fused_plan(const ttt_cfg& g, int* resident);
+// Test hook: cap the grid at `ctas` CTAs (0 = every SM).
+void ns_force_grid(int ctas);
+int ns_fused_run(const NsFusedArgs& a, cudaStream_t st);
+
+}  // namespace ttt

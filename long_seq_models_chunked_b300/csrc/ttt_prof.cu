@@ -111,7 +111,7 @@ long long ttt_launch_count(void) {
 const char* ttt_kernel_name(int kind) {
   static const char* names[TTT_KERNEL_COUNT] = {
       "fwd_swiglu",  "apply_out", "grad_outer", "ns_gram",      "ns_poly", "ns_xupd",
-      "update_norm", "aux",       "linear_chunk", "simt_layer"};
+      "update_norm", "aux",       "linear_chunk", "simt_layer", "ns_fused"};
   return (kind >= 0 && kind < TTT_KERNEL_COUNT) ? names[kind] : "unknown";
 }
 

@@ -24,99 +24,18 @@
 
 #include "../../include/ttt_debug.h"
 #include "tc_kernel.cuh"
+#include "tc_mc.cuh"
+#include "tc_util.cuh"
 #include "ttt_internal.h"
+#include "ttt_ns.h"
 
 namespace ttt {
 namespace {
 
-using bf16 = __nv_bfloat16;
-using f16 = __half;
+using namespace tcu;
 
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr uint32_t kABytes = BM * BK * 2;   // K-major A tile, or two MN-major boxes
-constexpr uint32_t kBox = 64 * BK * 2;      // one 64 x 64 bf16 box (MN-major)
+int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void st_bf16x32(bf16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    d[q] = w;
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void st_f16x32(f16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_f16(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_f16(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_f16(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_f16(v[8 * q + 6], v[8 * q + 7]);
-    d[q] = w;
-  }
-}
-
-// Stores 32 values as one fp16 operand (SINGLE) or as a bf16 hi/lo pair (SPLIT):
-// hi = bf16(v), lo = bf16(v - hi), so hi + lo carries ~16 significant bits.
-template <bool SPLIT>
-__device__ __forceinline__ void st_op32(void* hi, void* lo, size_t o, const float* v) {
-  if (SPLIT) {
-    float l[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
-    st_bf16x32(static_cast<bf16*>(hi) + o, v);
-    st_bf16x32(static_cast<bf16*>(lo) + o, l);
-  } else {
-    st_f16x32(static_cast<f16*>(hi) + o, v);
-  }
-}
-
-__device__ __forceinline__ void st_bf16pair32(bf16* hi, bf16* lo, const float* v) {
-  float l[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
-  st_bf16x32(hi, v);
-  st_bf16x32(lo, l);
-}
-
-__device__ __forceinline__ void st_f32x32(float* dst, const float* v) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
-__device__ __forceinline__ void ld_f32x32(const float* src, float* v) {
-  const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 x = s[q];
-    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-  }
-}
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// K-major operand descriptor for K step kk of a 64-deep stage.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) { return ptx::sdesc(base + kk * 32, 16, 1024); }
-// MN-major operand descriptor (64-wide groups kBox apart) for K step kk.
-__device__ __forceinline__ uint64_t mdesc(uint32_t base, int kk) { return ptx::sdesc(base + kk * 2048, kBox, 1024); }
 
 // ============================================================ fwd (apply-1 + update forward)
 struct FwdOp {
@@ -128,7 +47,9 @@ struct FwdOp {
     bf16* Hq;                // [BH][Cp][dh]
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
     bf16* El;                // low halves of E (split precision)
-    int d, dh, T, Cp, chunk_start, valid, q_tiles, k_tiles, n_tiles, split;
+    int d, dh, T, Cp, chunk_start, valid, q_tiles, k_tiles, n_tiles;
+    int w_split;             // keys: W = hi + lo (two products)
+    int e_split;             // E stored as hi + lo
     TcCommon cm;
   };
   struct Tile {
@@ -152,7 +73,7 @@ struct FwdOp {
   // then for key tiles segment 1 (Dm, same order). The keys/values are exact bf16,
   // so W = hi + lo needs two products, not three.
   static __device__ int seg0_blocks(const Params& p, const Tile& t) {
-    return (t.is_k && p.split ? 2 : 1) * (p.d / BK);
+    return (t.is_k && p.w_split ? 2 : 1) * (p.d / BK);
   }
   static __device__ int num_kblocks(const Params& p, const Tile& t) {
     return t.is_k ? 2 * seg0_blocks(p, t) : seg0_blocks(p, t);
@@ -231,7 +152,7 @@ struct FwdOp {
           va[i] = g * b * sg * (1.f + a * (1.f - sg));
           vb[i] = g * s;
         }
-        if (p.split) {
+        if (p.e_split) {
           st_bf16pair32(dA + c, p.El + oA + c, va);
           st_bf16pair32(dH + c, p.El + oA + plane + c, oh);
           st_bf16pair32(dB + c, p.El + oA + 2 * plane + c, vb);
@@ -294,266 +215,89 @@ struct OOp {
   }
 };
 
-// ============================================================ chunk gradients
-// z = bh*3 + j:  j=0  G1^T = K^T DA;  j=1  G2 = V^T He;  j=2  G3^T = K^T DB  (all [d, dh])
+// ============================================================ chunk gradients, multicast
+// Cluster of cs = ceil(d/128) CTAs per work item (z, n-block, token split):
+// CTA `rank` computes rows [128 rank, +128) of G_z^T (d x dh) over the item's
+// tokens; the E operand (the item's dh columns) is the same for every rank and
+// is multicast, each CTA loading a share of its 64-column boxes.
+//   z = bh*3 + j:  j=0  G1^T = K^T DA;  j=1  G2 = V^T He;  j=2  G3^T = K^T DB
+// With split E (hi + lo) both halves sit in one stage and every A tile feeds
+// two MMAs.
 template <int BN>
-struct GOp {
+struct GradMcOp {
   struct Params {
-    CUtensorMap mK4, mV4;  // 4D {d, C, n_full, BH}, box {64, 64, 1, 1}  (full chunks)
-    CUtensorMap mK3, mV3;  // 3D {d, T, BH}, box {64, 64, 1}            (ragged last chunk)
-    CUtensorMap mE;        // 3D {dh, Cp, 3BH}, box {64, 64, 1}
-    CUtensorMap mEl;       // low halves of E (split precision)
-    float* G;              // [Z][d][dh] fp32   (splits == 1)
-    float* part;           // [Z][part_stride] sums of squares per tile (splits == 1)
+    CUtensorMap mK4, mV4;  // 4D {d, C, n_full, BH}, box {64, 32, 1, 1}  (full chunks)
+    CUtensorMap mK3, mV3;  // 3D {d, T, BH}, box {64, 32, 1}            (ragged last chunk)
+    CUtensorMap mE, mEl;   // 3D {dh, Cp, 3BH}, box {64, 32, 1}
+    float* G;              // [Z][d][dh] fp32 (splits == 1)
     float* split_out;      // [splits][Z][d][dh] fp32 (splits > 1)
-    int d, dh, Z, chunk_idx, chunk_start, valid, use4d, m_tiles, n_tiles, splits, kb_per_split, part_stride;
-    int prec_split;        // E carried as hi + lo: two k passes over the tokens
+    int d, dh, Z, chunk_idx, chunk_start, valid, use4d, nt, splits, kb_per_split, e_split;
     TcCommon cm;
   };
   struct Tile {
-    int z, bh, j, m0, n0, kb0, nkb, split, tile_id;
+    int z, bh, j, m0, n0, kb0, nkb, split;
   };
-  static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kABytes + BN * BK * 2;
-  static constexpr int kTmemCols = BN <= 128 ? 128 : 256;
+  // 32 tokens per stage: five stages (200 KB) keep four in flight
+  static constexpr int kTok = 32;
+  static constexpr uint32_t kBoxG = 64 * kTok * 2;       // one 64 x 32 box
+  static constexpr uint32_t kAB = 2 * kBoxG;              // A: 128 rows of d
+  static constexpr uint32_t kEB = (BN / 64) * kBoxG;      // one half of E
+  static constexpr int kStages = 5;
+  static constexpr int kStageBytes = kAB + 2 * kEB;
+  static constexpr int kAccCols = BN;
 
-  static __device__ bool tile_of(const Params& p, Tile& t) {
-    const int nt = blockIdx.x % p.n_tiles, mt = blockIdx.x / p.n_tiles;
-    if (mt >= p.m_tiles) return false;
-    t.tile_id = blockIdx.x;
-    t.m0 = mt * BM;
-    t.n0 = nt * BN;
-    t.z = blockIdx.y;
+  static __device__ int num_work(const Params& p) { return p.Z * p.nt * p.splits; }
+  static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
+    t.split = w / (p.Z * p.nt);
+    const int r = w % (p.Z * p.nt);
+    t.z = r / p.nt;
+    t.n0 = (r % p.nt) * BN;
     t.bh = t.z / 3;
     t.j = t.z % 3;
-    t.split = blockIdx.z;
-    const int total = (p.valid + BK - 1) / BK;
+    t.m0 = rank * BM;
+    const int total = (p.valid + kTok - 1) / kTok;
     t.kb0 = t.split * p.kb_per_split;
-    t.nkb = min(total, t.kb0 + p.kb_per_split) - t.kb0;
-    return t.nkb > 0;
+    t.nkb = max(0, min(total, t.kb0 + p.kb_per_split) - t.kb0);
   }
-  static __device__ int num_kblocks(const Params& p, const Tile& t) { return t.nkb * (p.prec_split ? 2 : 1); }
-  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    const CUtensorMap* e = kb >= t.nkb ? &p.mEl : &p.mE;
-    const int tok = (t.kb0 + kb % t.nkb) * BK;
+  static __device__ int num_kblocks(const Params&, const Tile& t) { return t.nkb; }
+  static __device__ uint32_t stage_tx(const Params& p, const Tile&) {
+    return kAB + (p.e_split ? 2u : 1u) * kEB;
+  }
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar, int rank,
+                                 int cs, uint16_t mask) {
+    const int tok = (t.kb0 + kb) * kTok;
     for (int g = 0; g < 2; ++g) {
       if (p.use4d)
-        ptx::tma_load_4d(st + g * kBox, t.j == 1 ? &p.mV4 : &p.mK4, bar, t.m0 + g * 64, tok, p.chunk_idx, t.bh);
+        ptx::tma_load_4d(st + g * kBoxG, t.j == 1 ? &p.mV4 : &p.mK4, bar, t.m0 + g * 64, tok, p.chunk_idx, t.bh);
       else
-        ptx::tma_load_3d(st + g * kBox, t.j == 1 ? &p.mV3 : &p.mK3, bar, t.m0 + g * 64, p.chunk_start + tok, t.bh);
+        ptx::tma_load_3d(st + g * kBoxG, t.j == 1 ? &p.mV3 : &p.mK3, bar, t.m0 + g * 64, p.chunk_start + tok, t.bh);
     }
-#pragma unroll
-    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, e, bar, t.n0 + g * 64, tok, t.z);
+    constexpr int nb = BN / 64;
+    const int boxes = nb * (p.e_split ? 2 : 1);
+    for (int b = rank; b < boxes; b += cs) {
+      const int half = b / nb, g = b % nb;
+      ptx::tma_load_3d_mc(st + kAB + half * kEB + g * kBoxG, half ? &p.mEl : &p.mE, bar, t.n0 + g * 64, tok,
+                          t.z, mask);
+    }
   }
-  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
+  static __device__ void consume(const Params& p, const Tile&, int kb, uint32_t st, uint32_t tmem) {
     constexpr uint32_t id = ptx::idesc_bf16(128, BN, true, true);
+    const uint32_t eh = st + kAB, el = eh + kEB;
+    // MN-major operands of 64-wide groups kBoxG apart, 16 tokens per MMA
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, mdesc(st, kk), mdesc(st + kABytes, kk), id, (kb | kk) != 0);
-  }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float* red, bool ok) {
-    const int m = t.m0 + r;
-    const bool valid = ok && m < p.d;
-    float ss = 0.f;
-    float v[32];
-    if (ok) {
-      for (int c = 0; c < BN; c += 32) {
-        ptx::tmem_ld32(tm + c, v);
-        if (!valid || t.n0 + c >= p.dh) continue;
-        if (p.splits == 1) {
-          const size_t o = ((size_t)t.z * p.d + m) * p.dh + t.n0 + c;
-          st_f32x32(p.G + o, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
-        } else {
-          st_f32x32(p.split_out + (((size_t)t.split * p.Z + t.z) * p.d + m) * p.dh + t.n0 + c, v);
-        }
-      }
-    }
-    if (p.splits == 1) {
-      // deterministic per-tile sum of squares: warp butterfly, then 4 warps in lane-group order
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if ((r & 31) == 0) red[r >> 5] = ss;
-      epi_bar();
-      if (r == 0) p.part[(size_t)t.z * p.part_stride + t.tile_id] = ((red[0] + red[1]) + red[2]) + red[3];
-      epi_bar();
+    for (int kk = 0; kk < kTok / 16; ++kk) {
+      const uint64_t a = ptx::sdesc(st + kk * 2048, kBoxG, 1024);
+      ptx::mma_bf16(tmem, a, ptx::sdesc(eh + kk * 2048, kBoxG, 1024), id, (kb | kk) != 0);
+      if (p.e_split) ptx::mma_bf16(tmem, a, ptx::sdesc(el + kk * 2048, kBoxG, 1024), id, 1u);
     }
   }
-};
-
-// ============================================================ Newton-Schulz GEMMs
-// Operands of the iteration: SINGLE precision uses one fp16 operand per matrix
-// (11-bit significand at the bf16 tensor rate; X is normalised first, so X, S
-// and P stay within fp16's range); SPLIT precision carries every operand as a
-// bf16 pair (hi, lo) and forms each product from three MMAs
-// (hi*hi + hi*lo + lo*hi, the lo*lo term is below the pair's resolution).
-// X itself (the aX term) and S (the bS term) are also kept in fp32.
-//
-// k-block order of a SPLIT product: [hi*hi | hi*lo | lo*hi], each over the full K.
-template <bool SPLIT>
-__device__ __forceinline__ int ns_part(int kb, int nk) { return SPLIT ? kb / nk : 0; }
-
-// Gram: S = X X^T (d x d, K = dh)
-template <int BN, bool SPLIT>
-struct GramOp {
-  struct Params {
-    CUtensorMap mXa, mXal;  // X hi / lo 3D {dh, d, Z}, box {64, 128, 1}
-    CUtensorMap mXn, mXnl;  // same buffers, box {64, BN, 1}
-    float* S;
-    void* Sh;
-    void* Sl;
-    int d, dh, m_tiles, n_tiles;
-    TcCommon cm;
-  };
-  struct Tile {
-    int z, m0, n0;
-  };
-  static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kABytes + BN * BK * 2;
-  static constexpr int kTmemCols = BN <= 128 ? 128 : 256;
-  static __device__ bool tile_of(const Params& p, Tile& t) {
-    const int nt = blockIdx.x % p.n_tiles, mt = blockIdx.x / p.n_tiles;
-    if (mt >= p.m_tiles) return false;
-    t.m0 = mt * BM;
-    t.n0 = nt * BN;
-    t.z = blockIdx.y;
-    return true;
-  }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.dh / BK); }
-  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    const int nk = p.dh / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
-    ptx::tma_load_3d(st, part == 2 ? &p.mXal : &p.mXa, bar, k * BK, t.m0, t.z);
-    ptx::tma_load_3d(st + kABytes, part == 1 ? &p.mXnl : &p.mXn, bar, k * BK, t.n0, t.z);
-  }
-  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, !SPLIT);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), kdesc(st + kABytes, kk), id, (kb | kk) != 0);
-  }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float*, bool ok) {
-    if (!ok) return;
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
     const int m = t.m0 + r;
     float v[32];
+    float* dst = p.splits > 1 ? p.split_out + (size_t)t.split * p.Z * p.d * p.dh : p.G;
     for (int c = 0; c < BN; c += 32) {
       ptx::tmem_ld32(tm + c, v);
-      if (m >= p.d || t.n0 + c >= p.d) continue;
-      const size_t o = ((size_t)t.z * p.d + m) * p.d + t.n0 + c;
-      st_f32x32(p.S + o, v);
-      st_op32<SPLIT>(p.Sh, p.Sl, o, v);
-    }
-  }
-};
-
-// Poly: P = b S + c S S  (d x d, K = d; S is symmetric, so S^T serves as the B operand)
-template <int BN, bool SPLIT>
-struct PolyOp {
-  struct Params {
-    CUtensorMap mSa, mSal;  // S hi / lo 3D {d, d, Z}, box {64, 128, 1}
-    CUtensorMap mSn, mSnl;  // box {64, BN, 1}
-    const float* S;
-    void* Ph;
-    void* Pl;
-    float b, c;
-    int d, m_tiles, n_tiles;
-    TcCommon cm;
-  };
-  struct Tile {
-    int z, m0, n0;
-  };
-  static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kABytes + BN * BK * 2;
-  static constexpr int kTmemCols = BN <= 128 ? 128 : 256;
-  static __device__ bool tile_of(const Params& p, Tile& t) {
-    const int nt = blockIdx.x % p.n_tiles, mt = blockIdx.x / p.n_tiles;
-    if (mt >= p.m_tiles) return false;
-    t.m0 = mt * BM;
-    t.n0 = nt * BN;
-    t.z = blockIdx.y;
-    return true;
-  }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.d / BK); }
-  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    const int nk = p.d / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
-    ptx::tma_load_3d(st, part == 2 ? &p.mSal : &p.mSa, bar, k * BK, t.m0, t.z);
-    ptx::tma_load_3d(st + kABytes, part == 1 ? &p.mSnl : &p.mSn, bar, k * BK, t.n0, t.z);
-  }
-  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false, !SPLIT);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), kdesc(st + kABytes, kk), id, (kb | kk) != 0);
-  }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float*, bool ok) {
-    if (!ok) return;
-    const int m = t.m0 + r;
-    float v[32], s[32];
-    for (int c = 0; c < BN; c += 32) {
-      ptx::tmem_ld32(tm + c, v);
-      if (m >= p.d || t.n0 + c >= p.d) continue;
-      const size_t o = ((size_t)t.z * p.d + m) * p.d + t.n0 + c;
-      ld_f32x32(p.S + o, s);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = p.b * s[i] + p.c * v[i];
-      st_op32<SPLIT>(p.Ph, p.Pl, o, v);
-    }
-  }
-};
-
-// Xupd: X <- a X + P X  (d x dh, K = d); P K-major, X as the MN-major B operand.
-template <int BN, bool SPLIT>
-struct XupdOp {
-  struct Params {
-    CUtensorMap mPa, mPal;  // P hi / lo 3D {d, d, Z}, box {64, 128, 1}
-    CUtensorMap mXm, mXml;  // current X hi / lo 3D {dh, d, Z}, box {64, 64, 1}
-    float* X;               // fp32 [Z][d][dh], updated in place
-    void* Xh_next;          // operand copy of the new X (hi)
-    void* Xl_next;          // (lo, SPLIT only)
-    float a;
-    int d, dh, m_tiles, n_tiles;
-    TcCommon cm;
-  };
-  struct Tile {
-    int z, m0, n0;
-  };
-  static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kABytes + BN * BK * 2;
-  static constexpr int kTmemCols = BN <= 128 ? 128 : 256;
-  static __device__ bool tile_of(const Params& p, Tile& t) {
-    const int nt = blockIdx.x % p.n_tiles, mt = blockIdx.x / p.n_tiles;
-    if (mt >= p.m_tiles) return false;
-    t.m0 = mt * BM;
-    t.n0 = nt * BN;
-    t.z = blockIdx.y;
-    return true;
-  }
-  static __device__ int num_kblocks(const Params& p, const Tile&) { return (SPLIT ? 3 : 1) * (p.d / BK); }
-  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
-    const int nk = p.d / BK, part = ns_part<SPLIT>(kb, nk), k = kb % nk;
-    ptx::tma_load_3d(st, part == 2 ? &p.mPal : &p.mPa, bar, k * BK, t.m0, t.z);
-    const CUtensorMap* xb = part == 1 ? &p.mXml : &p.mXm;
-#pragma unroll
-    for (int g = 0; g < BN / 64; ++g) ptx::tma_load_3d(st + kABytes + g * kBox, xb, bar, t.n0 + g * 64, k * BK, t.z);
-  }
-  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
-    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, true, !SPLIT);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(st, kk), mdesc(st + kABytes, kk), id, (kb | kk) != 0);
-  }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float*, bool ok) {
-    if (!ok) return;
-    const int m = t.m0 + r;
-    float v[32], x[32];
-    for (int c = 0; c < BN; c += 32) {
-      ptx::tmem_ld32(tm + c, v);
-      if (m >= p.d || t.n0 + c >= p.dh) continue;
-      const size_t o = ((size_t)t.z * p.d + m) * p.dh + t.n0 + c;
-      ld_f32x32(p.X + o, x);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = p.a * x[i] + v[i];
-      st_f32x32(p.X + o, x);
-      st_op32<SPLIT>(p.Xh_next, p.Xl_next, o, x);
+      if (m < p.d) st_f32x32(dst + ((size_t)t.z * p.d + m) * p.dh + t.n0 + c, v);
     }
   }
 };
@@ -618,11 +362,6 @@ struct PlainOp {
 };
 
 // ============================================================ SIMT helper kernels
-__device__ __forceinline__ void st_shadow(bf16* hi, bf16* lo, size_t o, float v) {
-  const bf16 h = __float2bfloat16_rn(v);
-  hi[o] = h;
-  if (lo) lo[o] = __float2bfloat16_rn(v - __bfloat162float(h));
-}
 
 // W0 (out x in, per head) -> M = [W1^T, W2, W3^T] fp32 + bf16 shadow (hi, and lo
 // when the weights are carried split), per (b, h).
@@ -777,104 +516,20 @@ __global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, con
   }
 }
 
-// Split-K reduction of the gradient: fixed split order; sums of squares per block.
-__global__ void gsplit_reduce_kernel(const float* parts, float* G, float* part, int splits, int Z,
-                                     size_t per_z, int part_stride) {
-  __shared__ float red[256];
-  const int z = blockIdx.y;
-  float ss = 0.f;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < per_z; e += (size_t)gridDim.x * blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s) acc += parts[((size_t)s * Z + z) * per_z + e];
-    G[(size_t)z * per_z + e] = acc;
-    ss = fmaf(acc, acc, ss);
-  }
-  red[threadIdx.x] = ss;
-  __syncthreads();
-  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) part[(size_t)z * part_stride + blockIdx.x] = red[0];
-}
-
-// X0 = G / (||G||_F + eps) in place (fp32) plus its operand copy (fp16, or a
-// bf16 hi/lo pair). Every block sums the per-tile squares of its matrix in the
-// same order, so all of them use the same norm.
-template <bool SPLIT>
-__global__ void ns_normalize_kernel(float* G, void* Xh, void* Xl, const float* part, int n_part,
-                                    int part_stride, float eps, size_t per_z) {
-  const int z = blockIdx.y;
-  float s = 0.f;
-  for (int i = 0; i < n_part; ++i) s += part[(size_t)z * part_stride + i];
-  const float inv = 1.f / (sqrtf(s) + eps);
-  float* g = G + (size_t)z * per_z;
-  for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < per_z;
-       e += (size_t)gridDim.x * blockDim.x * 4) {
-    float4 v = *reinterpret_cast<float4*>(g + e);
-    v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
-    *reinterpret_cast<float4*>(g + e) = v;
-    const size_t o = (size_t)z * per_z + e;
-    if (SPLIT) {
-      uint2 h, l;
-      h.x = pack_bf16(v.x, v.y);
-      h.y = pack_bf16(v.z, v.w);
-      const __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&h.x);
-      const __nv_bfloat162 h1 = *reinterpret_cast<__nv_bfloat162*>(&h.y);
-      l.x = pack_bf16(v.x - __low2float(h0), v.y - __high2float(h0));
-      l.y = pack_bf16(v.z - __low2float(h1), v.w - __high2float(h1));
-      *reinterpret_cast<uint2*>(static_cast<bf16*>(Xh) + o) = h;
-      *reinterpret_cast<uint2*>(static_cast<bf16*>(Xl) + o) = l;
-    } else {
-      uint2 h;
-      h.x = pack_f16(v.x, v.y);
-      h.y = pack_f16(v.z, v.w);
-      *reinterpret_cast<uint2*>(static_cast<f16*>(Xh) + o) = h;
+// Token-split reduction of the gradient partials in a fixed split order (the
+// result does not depend on scheduling), 4 values per thread.
+__global__ void gsplit_reduce_kernel(const float* parts, float* G, int splits, size_t n) {
+  for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < n; e += (size_t)gridDim.x * blockDim.x * 4) {
+    float4 acc = *reinterpret_cast<const float4*>(parts + e);
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(parts + (size_t)s * n + e);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
+    *reinterpret_cast<float4*>(G + e) = acc;
   }
 }
 
 // ============================================================ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 16-bit tensor map over a row-major array with dims (innermost first) and box.
-bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
-              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  auto fn = encode_fn();
-  if (!fn || !base) return false;
-  cuuint64_t gd[5], gs[4];
-  cuuint32_t bx[5], es[5];
-  uint64_t stride = 2;
-  for (int i = 0; i < rank; ++i) {
-    gd[i] = dims[i];
-    bx[i] = box[i];
-    es[i] = 1;
-    if (i > 0) gs[i - 1] = stride;
-    stride *= dims[i];
-  }
-  const CUresult r = fn(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
-          CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  const uint64_t dims[3] = {d0, d1, d2};
-  const uint32_t box[3] = {b0, b1, 1};
-  return make_map(m, base, 3, dims, box, dt);
-}
 
 template <class Op>
 int launch_op(int kind, const typename Op::Params& p, dim3 grid, cudaStream_t st) {
@@ -896,12 +551,80 @@ int launch_op(int kind, const typename Op::Params& p, dim3 grid, cudaStream_t st
     if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA; \
   } while (0)
 
+// SM count the workspace plan assumes when it sizes the token-split buffers
+// (B300: 148); the launches query the device itself.
+constexpr int kNumSmsHint = 148;
+
+// Clusters of `cs` CTAs of the multicast engine that fit on the device at once
+// (cached per operation and cluster size).
+template <class Op>
+int mc_max_clusters(int cs) {
+  static int cached[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  static int cached_dev[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (cs < 1 || cs > 8) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cached_dev[cs] == dev) return cached[cs];
+  auto kern = tc_mc_kernel<Op>;
+  const size_t smem = tc_mc_smem_bytes<Op>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cached[cs] = n;
+  cached_dev[cs] = dev;
+  return n;
+}
+
+// Persistent cluster launch: one cluster per work item up to the device's
+// capacity, each cluster looping over items.
+template <class Op>
+int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaStream_t st) {
+  auto kern = tc_mc_kernel<Op>;
+  const size_t smem = tc_mc_smem_bytes<Op>();
+  const int max_cl = mc_max_clusters<Op>(cs);
+  if (max_cl <= 0) return TTT_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return TTT_ERR_CUDA;
+  const int n_cl = std::max(1, std::min(n_work, max_cl));
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(n_cl * cs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  prof_before(kind, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  prof_after(kind, st);
+  return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 struct Plan {
   int BH, Z, d, dh, C, Cp, T, split;
-  int bn_o, bn_dd;        // N tile of the apply GEMM (over d) and of the d x d NS GEMMs
-  int g_mt, g_nt, splits, kb_per_split, part_stride, reduce_blocks;
-  size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_S, off_Sh,
-      off_Sl, off_Ph, off_Pl, off_part, off_split, total;
+  int bn_o;               // N tile of the apply GEMM (over d)
+  int g_cs, g_bn, g_nt;   // gradient: cluster size (d / 128 row tiles), N tile over dh, N tiles
+  int g_splits_max;       // token splits the workspace has room for
+  size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_Sh,
+      off_Sl, off_Ph, off_Pl, off_split, off_nsq, total;
 };
 
 int pick_bn_d(int d) {
@@ -921,18 +644,12 @@ Plan make_plan(const ttt_cfg& g) {
   P.C = std::min(g.chunk, g.T);
   P.Cp = (P.C + BM - 1) / BM * BM;
   P.bn_o = pick_bn_d(g.d);
-  P.bn_dd = pick_bn_d(g.d);
-  const int gbn = (g.dh % 256 == 0) ? 256 : 128;
-  P.g_mt = (g.d + BM - 1) / BM;
-  P.g_nt = g.dh / gbn;
-  const int tiles = P.g_mt * P.g_nt * P.Z;
+  P.g_cs = (g.d + BM - 1) / BM;
+  P.g_bn = (g.dh % 256 == 0) ? 256 : 128;
+  P.g_nt = g.dh / P.g_bn;
+  // token splits when the (z, n-block) items alone leave SMs idle (up to 8)
   const int kbs = (P.C + BK - 1) / BK;
-  int splits = 1;
-  if (tiles < 2 * 148) splits = std::min(std::max(1, kbs / 16), (2 * 148 + tiles - 1) / tiles);
-  P.kb_per_split = (kbs + splits - 1) / splits;
-  P.splits = (kbs + P.kb_per_split - 1) / P.kb_per_split;
-  P.reduce_blocks = 32;
-  P.part_stride = std::max(P.g_mt * P.g_nt, P.reduce_blocks);
+  P.g_splits_max = std::max(1, std::min({8, kbs / 8, (kNumSmsHint / P.g_cs) / (P.Z * P.g_nt)}));
   const size_t wz = (size_t)P.Z * g.d * g.dh;
   const size_t dd = (size_t)P.Z * g.d * g.d;
   const size_t lo = P.split ? 1 : 0;  // the low halves exist only in split precision
@@ -954,71 +671,23 @@ Plan make_plan(const ttt_cfg& g) {
     P.off_Xh[i] = take(wz * 2);
     P.off_Xl[i] = take(lo * wz * 2);
   }
-  P.off_S = take(dd * 4);
   P.off_Sh = take(dd * 2);
   P.off_Sl = take(lo * dd * 2);
   P.off_Ph = take(dd * 2);
   P.off_Pl = take(lo * dd * 2);
-  P.off_part = take((size_t)P.Z * P.part_stride * 4);
-  P.off_split = take(P.splits > 1 ? (size_t)P.splits * wz * 4 : 0);
+  P.off_split = take(P.g_splits_max > 1 ? (size_t)P.g_splits_max * wz * 4 : 0);
+  P.off_nsq = take(ns_fused_scratch_floats(g, P.Z) * 4);
   P.total = off;
   return P;
-}
-
-// Launches one Newton-Schulz iteration's three GEMMs for a fixed N tile choice.
-template <int BND, int BNX, bool SPLIT>
-int ns_iteration(const CUtensorMap* mXa, const CUtensorMap* mXn, const CUtensorMap* mXm, const CUtensorMap* mSa,
-                 const CUtensorMap* mSn, const CUtensorMap* mPa, float* X, void* xh_next, void* xl_next, float* S,
-                 void* Sh, void* Sl, void* Ph, void* Pl, const ttt_cfg& g, int Z, const TcCommon& cm,
-                 cudaStream_t st) {
-  const int d = g.d, dh = g.dh;
-  const int mt = (d + BM - 1) / BM, ntd = (d + BND - 1) / BND, ntx = dh / BNX;
-  {
-    typename GramOp<BND, SPLIT>::Params p{};
-    p.mXa = mXa[0]; p.mXal = mXa[1]; p.mXn = mXn[0]; p.mXnl = mXn[1];
-    p.S = S; p.Sh = Sh; p.Sl = Sl; p.d = d; p.dh = dh; p.m_tiles = mt; p.n_tiles = ntd; p.cm = cm;
-    const int r = launch_op<GramOp<BND, SPLIT>>(TTT_KERNEL_GRAM, p, dim3(mt * ntd, Z), st);
-    if (r != TTT_OK) return r;
-  }
-  {
-    typename PolyOp<BND, SPLIT>::Params p{};
-    p.mSa = mSa[0]; p.mSal = mSa[1]; p.mSn = mSn[0]; p.mSnl = mSn[1];
-    p.S = S; p.Ph = Ph; p.Pl = Pl; p.b = g.ns_b; p.c = g.ns_c; p.d = d; p.m_tiles = mt; p.n_tiles = ntd;
-    p.cm = cm;
-    const int r = launch_op<PolyOp<BND, SPLIT>>(TTT_KERNEL_POLY, p, dim3(mt * ntd, Z), st);
-    if (r != TTT_OK) return r;
-  }
-  typename XupdOp<BNX, SPLIT>::Params p{};
-  p.mPa = mPa[0]; p.mPal = mPa[1]; p.mXm = mXm[0]; p.mXml = mXm[1];
-  p.X = X; p.Xh_next = xh_next; p.Xl_next = xl_next; p.a = g.ns_a; p.d = d; p.dh = dh; p.m_tiles = mt;
-  p.n_tiles = ntx; p.cm = cm;
-  return launch_op<XupdOp<BNX, SPLIT>>(TTT_KERNEL_XUPD, p, dim3(mt * ntx, Z), st);
-}
-
-template <bool SPLIT>
-int ns_iteration_any(int bnd, int bnx, const CUtensorMap* mXa, const CUtensorMap* mXn, const CUtensorMap* mXm,
-                     const CUtensorMap* mSa, const CUtensorMap* mSn, const CUtensorMap* mPa, float* X,
-                     void* xh_next, void* xl_next, float* S, void* Sh, void* Sl, void* Ph, void* Pl,
-                     const ttt_cfg& g, int Z, const TcCommon& cm, cudaStream_t st) {
-#define TTT_NS_CASE(BD, BX)                                                                                  \
-  if (bnd == BD && bnx == BX)                                                                                 \
-    return ns_iteration<BD, BX, SPLIT>(mXa, mXn, mXm, mSa, mSn, mPa, X, xh_next, xl_next, S, Sh, Sl, Ph, Pl, \
-                                       g, Z, cm, st);
-  TTT_NS_CASE(256, 256)
-  TTT_NS_CASE(256, 128)
-  TTT_NS_CASE(192, 256)
-  TTT_NS_CASE(192, 128)
-  TTT_NS_CASE(128, 256)
-  TTT_NS_CASE(128, 128)
-#undef TTT_NS_CASE
-  return TTT_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
 bool tc_supported(const ttt_cfg& g) {
+  // d <= 1024: the gradient's clusters hold d / 128 <= 8 CTAs
+  // (the fused Muon step completes the square of its quintic, so it needs c != 0)
   return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU && g.loss == TTT_LOSS_IP && g.d % 64 == 0 &&
-         g.dh % 128 == 0 && g.d <= g.dh && g.d <= 4096 && g.dh <= 16384;
+         g.dh % 128 == 0 && g.d <= g.dh && g.d <= 1024 && g.dh <= 16384 && (!g.muon || g.ns_c != 0.f);
 }
 
 size_t tc_workspace_bytes(const ttt_cfg& g) { return make_plan(g).total; }
@@ -1027,6 +696,10 @@ int tc_run(const Call& c) {
   const ttt_cfg& g = c.cfg;
   const Plan P = make_plan(g);
   const bool split = P.split != 0;
+  // which stages carry split operands (all of them unless a test hook narrowed it)
+  const bool split_fwd = split && (g_split_mask & 1);
+  const bool split_grad = split && (g_split_mask & 2);
+  const bool split_ns = split && (g_split_mask & 4);
   const cudaStream_t st = c.stream;
   char* ws = c.ws;
   auto at = [&](size_t off, size_t n) -> void* { return n ? static_cast<void*>(ws + off) : nullptr; };
@@ -1040,28 +713,24 @@ int tc_run(const Call& c) {
   float* G = reinterpret_cast<float*>(ws + P.off_G);
   void* Xh[2] = {ws + P.off_Xh[0], ws + P.off_Xh[1]};
   void* Xl[2] = {at(P.off_Xl[0], split), at(P.off_Xl[1], split)};
-  float* S = reinterpret_cast<float*>(ws + P.off_S);
   void* Sh = ws + P.off_Sh;
   void* Sl = at(P.off_Sl, split);
   void* Ph = ws + P.off_Ph;
   void* Pl = at(P.off_Pl, split);
-  float* part = reinterpret_cast<float*>(ws + P.off_part);
   float* splitbuf = reinterpret_cast<float*>(ws + P.off_split);
   int* status = reinterpret_cast<int*>(ws);
   const TcCommon cm{status, (unsigned long long)c.cfg.timeout_us * 1000ull};
   const int d = g.d, dh = g.dh, BH = P.BH, Z = P.Z, T = g.T;
   const int n_full = T / P.C;
-  const CUtensorMapDataType ns_dt = split ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
   // ---- tensor maps ([0] = hi or single operand, [1] = lo; lo maps alias hi in SINGLE precision)
   CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mHq, mW2o, mE[2];
-  CUtensorMap mXa[2][2], mXn[2][2], mXm[2][2], mSa[2], mSn[2], mPa[2];
   bool ok = true;
   ok &= map3(&mQ, c.Q, d, T, BH, 64, 128);
   ok &= map3(&mK, c.K, d, T, BH, 64, 128);
   ok &= map3(&mV, c.V, d, T, BH, 64, 128);
-  ok &= map3(&mK3, c.K, d, T, BH, 64, 64);
-  ok &= map3(&mV3, c.V, d, T, BH, 64, 64);
+  ok &= map3(&mK3, c.K, d, T, BH, 64, 32);  // gradient: 32-token boxes
+  ok &= map3(&mV3, c.V, d, T, BH, 64, 32);
   if (n_full > 0) {
     // 4D view {d, C, n_full, BH}: a chunk's token range ends at the chunk boundary
     auto fn = encode_fn();
@@ -1071,7 +740,7 @@ int tc_run(const Call& c) {
     for (int i = 0; i < 2; ++i) {
       cuuint64_t gd[4] = {(cuuint64_t)d, (cuuint64_t)P.C, (cuuint64_t)n_full, (cuuint64_t)BH};
       cuuint64_t gs[3] = {(cuuint64_t)d * 2, (cuuint64_t)P.C * d * 2, (cuuint64_t)T * d * 2};
-      cuuint32_t bx[4] = {64, 64, 1, 1};
+      cuuint32_t bx[4] = {64, 32, 1, 1};
       cuuint32_t es[4] = {1, 1, 1, 1};
       ok &= fn(outs[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]), gd, gs, bx, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1082,25 +751,11 @@ int tc_run(const Call& c) {
     mV4 = mV3;
   }
   ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
-  ok &= map3(&mW[1], split ? Msl : Ms, dh, d, Z, 64, 64);
+  ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
   ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
   ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
-  ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 64);
-  ok &= map3(&mE[1], split ? El : E, dh, P.Cp, Z, 64, 64);
-  for (int i = 0; i < 2; ++i)      // ping-pong buffer
-    for (int h = 0; h < 2; ++h) {  // hi / lo
-      const void* b = (h && split) ? Xl[i] : Xh[i];
-      ok &= map3(&mXa[i][h], b, dh, d, Z, 64, 128, ns_dt);
-      ok &= map3(&mXn[i][h], b, dh, d, Z, 64, P.bn_dd, ns_dt);
-      ok &= map3(&mXm[i][h], b, dh, d, Z, 64, 64, ns_dt);
-    }
-  for (int h = 0; h < 2; ++h) {
-    const void* sb = (h && split) ? Sl : Sh;
-    const void* pb = (h && split) ? Pl : Ph;
-    ok &= map3(&mSa[h], sb, d, d, Z, 64, 128, ns_dt);
-    ok &= map3(&mSn[h], sb, d, d, Z, 64, P.bn_dd, ns_dt);
-    ok &= map3(&mPa[h], pb, d, d, Z, 64, 128, ns_dt);
-  }
+  ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
+  ok &= map3(&mE[1], split_grad ? El : E, dh, P.Cp, Z, 64, 32);
   if (!ok) return TTT_ERR_CUDA;
 
   int rc;
@@ -1123,7 +778,8 @@ int tc_run(const Call& c) {
     p.q_tiles = q ? tiles : 0;
     p.k_tiles = k ? tiles : 0;
     p.n_tiles = dh / 128;
-    p.split = split ? 1 : 0;
+    p.w_split = split_fwd ? 1 : 0;
+    p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
     return launch_op<FwdOp>(TTT_KERNEL_FWD, p, dim3((p.q_tiles + p.k_tiles) * p.n_tiles, BH), st);
   };
@@ -1138,48 +794,29 @@ int tc_run(const Call& c) {
     if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, st); }
     typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(TTT_KERNEL_APPLY, p, grid, st);
   };
-  auto run_grad = [&](int ci, int s, int valid, int& n_part) -> int {
+  auto run_grad = [&](int ci, int s, int valid) -> int {
     const bool full = (s + P.C <= T) && ci < n_full;
-    const int kbs = (valid + BK - 1) / BK;
-    const int splits = (kbs + P.kb_per_split - 1) / P.kb_per_split;
-    auto fill = [&](auto& p) {
+    const int kbs = (valid + 31) / 32;  // 32-token k-blocks
+    const int items = Z * P.g_nt;
+    auto launch = [&](auto op) -> int {
+      using Op = decltype(op);
+      const int max_cl = mc_max_clusters<Op>(P.g_cs);
+      if (max_cl <= 0) return TTT_ERR_CUDA;
+      int splits = std::max(1, std::min({P.g_splits_max, kbs / 16, max_cl / items}));
+      const int kb_per_split = (kbs + splits - 1) / splits;
+      splits = (kbs + kb_per_split - 1) / kb_per_split;
+      typename Op::Params p{};
       p.mK4 = mK4; p.mV4 = mV4; p.mK3 = mK3; p.mV3 = mV3; p.mE = mE[0]; p.mEl = mE[1];
-      p.G = G; p.part = part; p.split_out = splitbuf;
+      p.G = G; p.split_out = splitbuf;
       p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
-      p.m_tiles = P.g_mt; p.n_tiles = P.g_nt; p.splits = splits; p.kb_per_split = P.kb_per_split;
-      p.part_stride = P.part_stride; p.prec_split = split ? 1 : 0; p.cm = cm;
+      p.nt = P.g_nt; p.splits = splits; p.kb_per_split = kb_per_split; p.e_split = split_grad ? 1 : 0; p.cm = cm;
+      const int r = launch_mc<Op>(TTT_KERNEL_GRAD, p, P.g_cs, items * splits, st);
+      if (r != TTT_OK || splits == 1) return r;
+      const size_t n = (size_t)Z * d * dh;
+      TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, G, splits, n));
+      return TTT_OK;
     };
-    const dim3 grid(P.g_mt * P.g_nt, Z, splits);
-    int r;
-    if (dh % 256 == 0) { typename GOp<256>::Params p{}; fill(p); r = launch_op<GOp<256>>(TTT_KERNEL_GRAD, p, grid, st); }
-    else { typename GOp<128>::Params p{}; fill(p); r = launch_op<GOp<128>>(TTT_KERNEL_GRAD, p, grid, st); }
-    if (r != TTT_OK) return r;
-    if (splits > 1)
-      TTT_LAUNCH(TTT_KERNEL_GRAD, st,
-                 gsplit_reduce_kernel<<<dim3(P.reduce_blocks, Z), 256, 0, st>>>(splitbuf, G, part, splits, Z,
-                                                                                 (size_t)d * dh, P.part_stride));
-    n_part = splits > 1 ? P.reduce_blocks : P.g_mt * P.g_nt;
-    return TTT_OK;
-  };
-  auto run_ns = [&](int n_part) -> int {
-    if (split)
-      TTT_LAUNCH(TTT_KERNEL_AUX, st,
-                 ns_normalize_kernel<true><<<dim3(16, Z), 256, 0, st>>>(G, Xh[0], Xl[0], part, n_part,
-                                                                        P.part_stride, g.ns_eps, (size_t)d * dh));
-    else
-      TTT_LAUNCH(TTT_KERNEL_AUX, st,
-                 ns_normalize_kernel<false><<<dim3(16, Z), 256, 0, st>>>(G, Xh[0], Xl[0], part, n_part,
-                                                                         P.part_stride, g.ns_eps, (size_t)d * dh));
-    const int bnx = (dh % 256 == 0) ? 256 : 128;
-    for (int it = 0; it < g.ns_iters; ++it) {
-      const int cur = it & 1, nxt = cur ^ 1;
-      const int r = split ? ns_iteration_any<true>(P.bn_dd, bnx, mXa[cur], mXn[cur], mXm[cur], mSa, mSn, mPa, G,
-                                                   Xh[nxt], Xl[nxt], S, Sh, Sl, Ph, Pl, g, Z, cm, st)
-                          : ns_iteration_any<false>(P.bn_dd, bnx, mXa[cur], mXn[cur], mXm[cur], mSa, mSn, mPa,
-                                                    G, Xh[nxt], Xl[nxt], S, Sh, Sl, Ph, Pl, g, Z, cm, st);
-      if (r != TTT_OK) return r;
-    }
-    return TTT_OK;
+    return P.g_bn == 256 ? launch(GradMcOp<256>{}) : launch(GradMcOp<128>{});
   };
   auto run_update = [&]() -> int {
     const dim3 grid(std::max((dh + 31) / 32, (d + 7) / 8), Z);
@@ -1187,15 +824,19 @@ int tc_run(const Call& c) {
                update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, G, n0, g.step, g.wnorm, g.wnorm_eps, d, dh));
     return TTT_OK;
   };
+  NsFusedArgs nsa{};
+  nsa.cfg = &c.cfg; nsa.Z = Z; nsa.split = split_ns; nsa.X = G;
+  for (int i = 0; i < 2; ++i) { nsa.Xh[i] = Xh[i]; nsa.Xl[i] = Xl[i]; }
+  nsa.Rh = Sh; nsa.Rl = Sl; nsa.Ph = Ph; nsa.Pl = Pl;
+  nsa.M = M; nsa.Ms = Ms; nsa.Msl = Msl; nsa.n0 = n0;
+  nsa.scratch = reinterpret_cast<float*>(ws + P.off_nsq);
+  nsa.cm = cm;
+  // update: gradient, then Muon + update + weight norm in one launch (or, without
+  // Muon, the plain update + weight norm)
   auto do_update = [&](int ci, int s, int valid) -> int {
-    int n_part = 0;
-    int r = run_grad(ci, s, valid, n_part);
+    const int r = run_grad(ci, s, valid);
     if (r != TTT_OK) return r;
-    if (g.muon) {
-      r = run_ns(n_part);
-      if (r != TTT_OK) return r;
-    }
-    return run_update();
+    return g.muon ? ns_fused_run(nsa, st) : run_update();
   };
 
   for (int ci = 0; ci < c.n_chunks; ++ci) {
@@ -1226,7 +867,28 @@ int tc_run(const Call& c) {
 
 }  // namespace ttt
 
-// ============================================================ test hook
+// ============================================================ test hooks
+extern "C" int ttt_dbg_ns_plan(const ttt_cfg* cfg, int* grid, int* resident) {
+  using namespace ttt;
+  if (!cfg || !grid || ttt_select_impl(cfg) != TTT_IMPL_TC || !ns_fused_supported(*cfg)) return TTT_ERR_ARG;
+  const int G = ns_fused_plan(*cfg, resident);
+  if (G <= 0) return TTT_ERR_CUDA;
+  *grid = G;
+  return TTT_OK;
+}
+
+extern "C" int ttt_dbg_split_mask(int mask) {
+  if (mask < 0 || mask > 7) return TTT_ERR_ARG;
+  ttt::g_split_mask = mask;
+  return TTT_OK;
+}
+
+extern "C" int ttt_dbg_ns_force_grid(int ctas) {
+  if (ctas < 0) return TTT_ERR_ARG;
+  ttt::ns_force_grid(ctas);
+  return TTT_OK;
+}
+
 extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, float* D, int Z,
                                  int M, int N, int K, void* stream) {
   using namespace ttt;
