@@ -25,7 +25,7 @@
 //   static __device__ int  num_work(const Params&);
 //   static __device__ void tile_of(const Params&, int item, int rank, Tile&);
 //   static __device__ int  num_kblocks(const Params&, const Tile&)   (same for every rank of an item)
-//   static __device__ uint32_t stage_tx(const Params&, const Tile&)  bytes landing in THIS CTA per stage
+//   static __device__ uint32_t stage_tx(const Params&, const Tile&, int kb)  bytes landing in THIS CTA
 //   static __device__ void produce(const Params&, const Tile&, int kb, uint8_t* stage, uint64_t* bar,
 //                                  int rank, int cs, uint16_t mask)
 //        issues this CTA's own loads and its multicast slice (mask = every CTA)
@@ -95,12 +95,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
         typename Op::Tile t;
         Op::tile_of(p, w, rank, t);
         const int nkb = Op::num_kblocks(p, t);
-        const uint32_t tx = Op::stage_tx(p, t);
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = pc % Op::kStages;
           if (!tc_wait(&empty[s], ((pc / Op::kStages) & 1u) ^ 1u, p.cm, abort_flag)) break;
           uint8_t* st = smem + (size_t)s * Op::kStageBytes;
-          ptx::mbar_expect_tx(&full[s], tx);
+          ptx::mbar_expect_tx(&full[s], Op::stage_tx(p, t, kb));
           Op::produce(p, t, kb, st, &full[s], rank, cs, mask);
           ++pc;
         }

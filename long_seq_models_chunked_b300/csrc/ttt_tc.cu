@@ -37,110 +37,124 @@ using namespace tcu;
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
 
 
-// ============================================================ fwd (apply-1 + update forward)
-struct FwdOp {
+// ============================================================ forward, multicast
+// Forward of the fast net on 128-token x 64-hidden tiles (LaCT page §2.1): the
+// clusters' CTAs take consecutive token tiles of one (b, h, hidden slice) and
+// share that slice's weights by TMA multicast (each CTA loads a share of the
+// weight boxes); the token rows are each CTA's own.
+//   query tile: [A|B] = Q [W1;W3]^T -> H_q = silu(A) * B                 (apply-1)
+//   key tile:   [A|B] = K [W1;W3]^T, Dm = V W2 -> DA, He, DB (SwiGLU backward,
+//               scaled by -lr per token), the gradient kernel's E operand
+// TMEM: [A|B] in columns 0-127, Dm in 128-191 of one 256-column accumulator.
+struct FwdMcOp {
   struct Params {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
-    CUtensorMap mW;          // bf16 shadows [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
-    CUtensorMap mWl;         // low halves of the shadows (split precision)
+    CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
     const float* lr;
     bf16* Hq;                // [BH][Cp][dh]
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
     bf16* El;                // low halves of E (split precision)
-    int d, dh, T, Cp, chunk_start, valid, q_tiles, k_tiles, n_tiles;
-    int w_split;             // keys: W = hi + lo (two products)
-    int e_split;             // E stored as hi + lo
+    int d, dh, T, Cp, chunk_start, valid;
+    int n_tok, groups, n_js, BH, cs;
+    int q, k;                // which kinds of tiles this launch computes
+    int w_split, e_split;
     TcCommon cm;
   };
   struct Tile {
-    int bh, row0, j0;
-    bool is_k;
+    int bh, js, tok;
+    bool is_k, real;
   };
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = kABytes + 4 * kBox;
-  static constexpr int kTmemCols = 512;
+  static constexpr int kAccCols = 256;
 
-  static __device__ bool tile_of(const Params& p, Tile& t) {
-    const int nt = blockIdx.x % p.n_tiles, rt = blockIdx.x / p.n_tiles;
-    if (rt >= p.q_tiles + p.k_tiles) return false;
-    t.is_k = rt >= p.q_tiles;
-    t.row0 = (t.is_k ? rt - p.q_tiles : rt) * BM;
-    t.j0 = nt * 128;
-    t.bh = blockIdx.y;
-    return true;
+  static __device__ int num_work(const Params& p) { return p.BH * p.n_js * p.groups * (p.q + p.k); }
+  static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
+    const int kinds = p.q + p.k;
+    const int kind = w % kinds;
+    w /= kinds;
+    t.is_k = p.q ? kind == 1 : true;
+    const int g = w % p.groups;
+    w /= p.groups;
+    t.js = w % p.n_js;
+    t.bh = w / p.n_js;
+    t.tok = g * p.cs + rank;
+    t.real = t.tok < p.n_tok;
   }
-  // k-blocks: segment 0 ([A|B], the weights' hi then, when split, lo halves),
-  // then for key tiles segment 1 (Dm, same order). The keys/values are exact bf16,
-  // so W = hi + lo needs two products, not three.
-  static __device__ int seg0_blocks(const Params& p, const Tile& t) {
-    return (t.is_k && p.w_split ? 2 : 1) * (p.d / BK);
-  }
-  static __device__ int num_kblocks(const Params& p, const Tile& t) {
-    return t.is_k ? 2 * seg0_blocks(p, t) : seg0_blocks(p, t);
+  static __device__ int num_kblocks(const Params& p, const Tile& t) { return (t.is_k ? 2 : 1) * (p.d / BK); }
+  // weight boxes of k-block kb: queries [W1, W3] (hi); keys segment 0
+  // [W1 hi, W3 hi, W1 lo, W3 lo], segment 1 [W2 hi, W2 lo]
+  static __device__ int n_boxes(const Params& p, const Tile& t, int kb) {
+    if (!t.is_k) return 2;
+    return (kb < p.d / BK ? 2 : 1) * (p.w_split ? 2 : 1);
   }
   static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int kb) {
-    return kb < seg0_blocks(p, t) ? kABytes + 4 * kBox : kABytes + 2 * kBox;
+    return kABytes + (uint32_t)n_boxes(p, t, kb) * kBox;
   }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar, int rank,
+                                 int cs, uint16_t mask) {
     const int nk = p.d / BK;
-    const int n0 = seg0_blocks(p, t);
+    const bool seg1 = t.is_k && kb >= nk;
+    const int k = (seg1 ? kb - nk : kb) * BK;
+    const CUtensorMap* x = seg1 ? &p.mV : (t.is_k ? &p.mK : &p.mQ);
+    ptx::tma_load_3d(st, x, bar, k, p.chunk_start + t.tok * BM, t.bh);
     const int z = t.bh * 3;
-    if (kb < n0) {
-      const int k = kb % nk;
-      const CUtensorMap* w = kb >= nk ? &p.mWl : &p.mW;
-      ptx::tma_load_3d(st, t.is_k ? &p.mK : &p.mQ, bar, k * BK, p.chunk_start + t.row0, t.bh);
-      for (int g = 0; g < 2; ++g) {
-        ptx::tma_load_3d(st + kABytes + g * kBox, w, bar, t.j0 + g * 64, k * BK, z + 0);
-        ptx::tma_load_3d(st + kABytes + (2 + g) * kBox, w, bar, t.j0 + g * 64, k * BK, z + 2);
-      }
-    } else {
-      const int k2 = kb - n0, k = k2 % nk;
-      const CUtensorMap* w = k2 >= nk ? &p.mWl : &p.mW;
-      ptx::tma_load_3d(st, &p.mV, bar, k * BK, p.chunk_start + t.row0, t.bh);
-      for (int g = 0; g < 2; ++g)
-        ptx::tma_load_3d(st + kABytes + g * kBox, w, bar, t.j0 + g * 64, k * BK, z + 1);
+    const int nb = n_boxes(p, t, kb);
+    for (int b = rank; b < nb; b += cs) {
+      const bool lo = seg1 ? b == 1 : b >= 2;
+      const int zz = seg1 ? z + 1 : z + ((b & 1) ? 2 : 0);
+      ptx::tma_load_3d_mc(st + kABytes + b * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
     }
   }
   static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
-    const int n0 = seg0_blocks(p, t);
+    const int nk = p.d / BK;
     const uint32_t a = st, b = st + kABytes;
-    if (kb < n0) {
-      constexpr uint32_t id = ptx::idesc_bf16(128, 256, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
-    } else {
-      const int k2 = kb - n0;
+    if (!t.is_k || kb < nk) {
       constexpr uint32_t id = ptx::idesc_bf16(128, 128, false, true);
+      const bool two = t.is_k && p.w_split;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem + 256, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
+      for (int kk = 0; kk < 4; ++kk) {
+        ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
+        if (two) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b + 2 * kBox, kk), id, 1u);
+      }
+    } else {
+      const int k2 = kb - nk;
+      constexpr uint32_t id = ptx::idesc_bf16(128, 64, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
+        if (p.w_split) ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b + kBox, kk), id, 1u);
+      }
     }
   }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float*, bool ok) {
-    if (!ok) return;
-    const int tl = t.row0 + r;  // token index inside the chunk
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
+    if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
+    const int tl = t.tok * BM + r;  // token index inside the chunk
     const bool valid = tl < p.valid;
+    const int j0 = t.js * 64;
     float va[32], vb[32];
     if (!t.is_k) {
-      bf16* dst = p.Hq + ((size_t)t.bh * p.Cp + tl) * p.dh + t.j0;
-      for (int c = 0; c < 128; c += 32) {
+      bf16* dst = p.Hq + ((size_t)t.bh * p.Cp + tl) * p.dh + j0;
+      for (int c = 0; c < 64; c += 32) {
         ptx::tmem_ld32(tm + c, va);
-        ptx::tmem_ld32(tm + 128 + c, vb);
+        ptx::tmem_ld32(tm + 64 + c, vb);
 #pragma unroll
         for (int i = 0; i < 32; ++i) va[i] = va[i] * sigmoidf_(va[i]) * vb[i];
         if (valid) st_bf16x32(dst + c, va);
       }
     } else {
+      // rows past the chunk's tokens get lr 0, so their E rows are zero
       const float eta = valid ? p.lr[(size_t)t.bh * p.T + p.chunk_start + tl] : 0.f;
       const size_t plane = (size_t)p.Cp * p.dh;
-      const size_t oA = ((size_t)t.bh * 3 * p.Cp + tl) * p.dh + t.j0;
+      const size_t oA = ((size_t)t.bh * 3 * p.Cp + tl) * p.dh + j0;
       bf16* dA = p.E + oA;
       bf16* dH = dA + plane;
       bf16* dB = dA + 2 * plane;
       float vd[32];
-      for (int c = 0; c < 128; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         ptx::tmem_ld32(tm + c, va);
-        ptx::tmem_ld32(tm + 128 + c, vb);
-        ptx::tmem_ld32(tm + 256 + c, vd);
+        ptx::tmem_ld32(tm + 64 + c, vb);
+        ptx::tmem_ld32(tm + 128 + c, vd);
         float oh[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -260,7 +274,7 @@ struct GradMcOp {
     t.nkb = max(0, min(total, t.kb0 + p.kb_per_split) - t.kb0);
   }
   static __device__ int num_kblocks(const Params&, const Tile& t) { return t.nkb; }
-  static __device__ uint32_t stage_tx(const Params& p, const Tile&) {
+  static __device__ uint32_t stage_tx(const Params& p, const Tile&, int) {
     return kAB + (p.e_split ? 2u : 1u) * kEB;
   }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar, int rank,
@@ -770,18 +784,22 @@ int tc_run(const Call& c) {
   }
 
   auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
-    FwdOp::Params p{};
+    FwdMcOp::Params p{};
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
-    const int tiles = (valid + BM - 1) / BM;
-    p.q_tiles = q ? tiles : 0;
-    p.k_tiles = k ? tiles : 0;
-    p.n_tiles = dh / 128;
+    p.n_tok = (valid + BM - 1) / BM;
+    // clusters of up to 4 consecutive token tiles share each weight slice
+    p.cs = p.n_tok >= 4 ? 4 : (p.n_tok >= 2 ? 2 : 1);
+    p.groups = (p.n_tok + p.cs - 1) / p.cs;
+    p.n_js = dh / 64;
+    p.BH = BH;
+    p.q = q ? 1 : 0;
+    p.k = k ? 1 : 0;
     p.w_split = split_fwd ? 1 : 0;
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
-    return launch_op<FwdOp>(TTT_KERNEL_FWD, p, dim3((p.q_tiles + p.k_tiles) * p.n_tiles, BH), st);
+    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, BH * p.n_js * p.groups * (p.q + p.k), st);
   };
   auto run_o = [&](int s, int valid) -> int {
     const int mt = (valid + BM - 1) / BM, nt = (d + P.bn_o - 1) / P.bn_o;
