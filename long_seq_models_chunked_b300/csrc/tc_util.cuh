@@ -123,7 +123,8 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 16-bit tensor map over a row-major array with dims (innermost first) and box.
 inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
-              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn || !base) return false;
   cuuint64_t gd[5], gs[4];
@@ -137,16 +138,17 @@ inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
     stride *= dims[i];
   }
   const CUresult r = fn(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 inline bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
-          CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+          CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+          CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   const uint64_t dims[3] = {d0, d1, d2};
   const uint32_t box[3] = {b0, b1, 1};
-  return make_map(m, base, 3, dims, box, dt);
+  return make_map(m, base, 3, dims, box, dt, swz);
 }
 
 }  // namespace tcu

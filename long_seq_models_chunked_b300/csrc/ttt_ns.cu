@@ -46,12 +46,12 @@ constexpr int kMaxGroup = 16;  // CTAs sharing one matrix in the element-wise ph
 enum { PH_GRAM = 0, PH_POLY = 1, PH_XUPD = 2 };
 
 struct NsParams {
-  CUtensorMap mXa[2][2];  // X operand [ping-pong][hi, lo]: {dh, d, Z}, box {64, 128}
-  CUtensorMap mXb[2][2];  //   box {64, BNS}  (Gram B operand, K-major)
-  CUtensorMap mXm[2][2];  //   box {64, 64}   (X update B operand, MN-major)
-  CUtensorMap mRa[2];          // R operand [hi, lo]: {d, d, Z}, box {64, 128}
-  CUtensorMap mRb[2];          //   box {64, BNS}
-  CUtensorMap mPa[2];          // P operand [hi, lo]: {d, d, Z}, box {64, 128}
+  CUtensorMap mXa[2][2];  // X operand [ping-pong][hi, lo]: {dh, d, Z}, box {32, 128}, 64-byte swizzle
+  CUtensorMap mXb[2][2];  //   box {32, BNS}, 64-byte swizzle  (Gram B operand, K-major)
+  CUtensorMap mXm[2][2];  //   box {64, 32}, 128-byte swizzle  (X update B operand, MN-major)
+  CUtensorMap mRa[2];          // R operand [hi, lo]: {d, d, Z}, box {32, 128}, 64-byte swizzle
+  CUtensorMap mRb[2];          //   box {32, BNS}
+  CUtensorMap mPa[2];          // P operand [hi, lo]: {d, d, Z}, box {32, 128}
   float* X;         // [Z][d][dh] fp32: the gradient on entry, the result U on exit
   void* Xop[2][2];  // operand copies of X [ping-pong][hi, lo]
   void* Rop[2];
@@ -71,15 +71,30 @@ struct NsParams {
 // Shared-memory ring. SPLIT stages hold both halves of both operands
 // [A hi | A lo | B hi | B lo], so one load serves all three products; SINGLE
 // stages hold [A | B].
+// Stages hold 32 elements of K: K-major operands in the 64-byte swizzle (rows
+// of 64 B, 8-row atoms of 512 B), the MN-major X operand of the update in
+// 128-byte-swizzled boxes of 64 x 32. Small stages keep more of the ring in
+// flight: four stages of 48 KB (SPLIT) or eight of 24 KB.
+constexpr int kNsBK = 32;
+constexpr uint32_t kNsABytes = BM * kNsBK * 2;       // 8 KB: 128 rows x 64 B
+constexpr uint32_t kNsMNBox = 64 * kNsBK * 2;        // 4 KB: one 64 x 32 MN-major box
+
 template <int BNS, int BNX, bool SPLIT>
 struct NsGeom {
   static constexpr int kOps = SPLIT ? 2 : 1;
   static constexpr int kBmax = BNS > BNX ? BNS : BNX;
-  static constexpr uint32_t kBBytes = (uint32_t)kBmax * BK * 2;
-  static constexpr uint32_t kStageBytes = kOps * (kABytes + kBBytes);
-  static constexpr int kStages = SPLIT ? 2 : 4;
+  static constexpr uint32_t kBBytes = (uint32_t)kBmax * kNsBK * 2;
+  static constexpr uint32_t kStageBytes = kOps * (kNsABytes + kBBytes);
+  static constexpr int kStages = SPLIT ? 4 : 8;
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 512;
 };
+
+// K-major operand in the 64-byte swizzle; K step kk of 16 elements
+__device__ __forceinline__ uint64_t kdesc64(uint32_t base, int kk) { return ptx::sdesc_l(base + kk * 32, 16, 512, 4); }
+// MN-major operand: 64-wide groups kNsMNBox apart, 128-byte swizzle; K step kk
+__device__ __forceinline__ uint64_t mdesc32(uint32_t base, int kk) {
+  return ptx::sdesc_l(base + kk * 2048, kNsMNBox, 1024, 2);
+}
 
 struct PhaseDesc {
   int mt, nt, nk1, bn;
@@ -91,11 +106,11 @@ __device__ __forceinline__ PhaseDesc phase_desc(const NsParams& p, int kind) {
   q.mt = (p.d + BM - 1) / BM;
   if (kind == PH_XUPD) {
     q.nt = p.dh / BNX;
-    q.nk1 = p.d / BK;
+    q.nk1 = p.d / kNsBK;
     q.bn = BNX;
   } else {
     q.nt = (p.d + BNS - 1) / BNS;
-    q.nk1 = (kind == PH_GRAM ? p.dh : p.d) / BK;
+    q.nk1 = (kind == PH_GRAM ? p.dh : p.d) / kNsBK;
     q.bn = BNS;
   }
   return q;
@@ -299,7 +314,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
       const int nkb = q.nk1;
       if (warp == 0) {
         if (lane == 0 && !*abort_flag) {
-          const uint32_t tx = Geo::kOps * (kABytes + (uint32_t)q.bn * BK * 2);
+          const uint32_t tx = Geo::kOps * (kNsABytes + (uint32_t)q.bn * kNsBK * 2);
           for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += G) {
             const int z = t / per_z, tl = t % per_z;
             const int m0 = (tl / q.nt) * BM, n0 = (tl % q.nt) * q.bn;
@@ -308,10 +323,10 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
               if (!tc_wait(&empty[s], ((pc / kNsStages) & 1u) ^ 1u, p.cm, abort_flag)) break;
               uint8_t* st = smem + (size_t)s * Geo::kStageBytes;
               ptx::mbar_expect_tx(&full[s], tx);
-              const int k = kb * BK;
+              const int k = kb * kNsBK;
               for (int h = 0; h < Geo::kOps; ++h) {
-                uint8_t* sa = st + h * kABytes;
-                uint8_t* sb = st + Geo::kOps * kABytes + h * Geo::kBBytes;
+                uint8_t* sa = st + h * kNsABytes;
+                uint8_t* sb = st + Geo::kOps * kNsABytes + h * Geo::kBBytes;
                 if (kind == PH_GRAM) {
                   ptx::tma_load_3d(sa, &p.mXa[cur][h], &full[s], k, m0, z);
                   ptx::tma_load_3d(sb, &p.mXb[cur][h], &full[s], k, n0, z);
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
                 } else {
                   ptx::tma_load_3d(sa, &p.mPa[h], &full[s], k, m0, z);
                   for (int g = 0; g < BNX / 64; ++g)
-                    ptx::tma_load_3d(sb + g * kBox, &p.mXm[cur][h], &full[s], n0 + g * 64, k, z);
+                    ptx::tma_load_3d(sb + g * kNsMNBox, &p.mXm[cur][h], &full[s], n0 + g * 64, k, z);
                 }
               }
               ++pc;
@@ -342,23 +357,23 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
               ptx::tc_fence_after();
               // [A hi, A lo] at sa0, sa0 + kABytes; [B hi, B lo] at sb0, sb0 + kBBytes
               const uint32_t sa0 = ptx::smem_u32(smem + (size_t)s * Geo::kStageBytes);
-              const uint32_t sb0 = sa0 + Geo::kOps * kABytes;
+              const uint32_t sb0 = sa0 + Geo::kOps * kNsABytes;
               // products: hi*hi, then (SPLIT) hi*lo and lo*hi
               constexpr int kProd = SPLIT ? 3 : 1;
 #pragma unroll
               for (int pr = 0; pr < kProd; ++pr) {
-                const uint32_t sa = sa0 + (pr == 2 ? kABytes : 0u);
+                const uint32_t sa = sa0 + (pr == 2 ? kNsABytes : 0u);
                 const uint32_t sb = sb0 + (pr == 1 ? Geo::kBBytes : 0u);
                 if (kind == PH_XUPD) {
                   constexpr uint32_t id = ptx::idesc_bf16(128, BNX, false, true, !SPLIT);
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    ptx::mma_bf16(dt, kdesc(sa, kk), mdesc(sb, kk), id, (kb | kk | pr) != 0);
+                  for (int kk = 0; kk < kNsBK / 16; ++kk)
+                    ptx::mma_bf16(dt, kdesc64(sa, kk), mdesc32(sb, kk), id, (kb | kk | pr) != 0);
                 } else {
                   constexpr uint32_t id = ptx::idesc_bf16(128, BNS, false, false, !SPLIT);
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    ptx::mma_bf16(dt, kdesc(sa, kk), kdesc(sb, kk), id, (kb | kk | pr) != 0);
+                  for (int kk = 0; kk < kNsBK / 16; ++kk)
+                    ptx::mma_bf16(dt, kdesc64(sa, kk), kdesc64(sb, kk), id, (kb | kk | pr) != 0);
                 }
               }
               ptx::mma_commit(&empty[s]);
@@ -389,25 +404,27 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
           for (int c = 0; c < q.bn; c += 32) {
             ptx::tmem_ld32(ta + c, v);
             const int n = n0 + c;
+            // warp-uniform: n, and whether this is the last iteration
             if (kind == PH_GRAM) {
-              if (row_ok && n < d) {
+              if (n < d) {
                 const size_t o = ((size_t)z * d + m) * d + n;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] += (m == n + i ? p.beta : 0.f);
-                st_op32<SPLIT>(p.Rop[0], p.Rop[1], o, v);
+                if (row_ok) st_op32<SPLIT>(p.Rop[0], p.Rop[1], o, v);
               }
             } else if (kind == PH_POLY) {
-              if (row_ok && n < d) {
+              if (n < d) {
                 const size_t o = ((size_t)z * d + m) * d + n;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = p.c * v[i] + (m == n + i ? p.alpha : 0.f);
-                st_op32<SPLIT>(p.Pop[0], p.Pop[1], o, v);
+                if (row_ok) st_op32<SPLIT>(p.Pop[0], p.Pop[1], o, v);
               }
             } else {
-              if (row_ok) {
-                const size_t o = (size_t)z * d * dh + (size_t)m * dh + n;
-                if (last) st_f32x32(p.X + o, v);
-                else st_op32<SPLIT>(p.Xop[cur ^ 1][0], p.Xop[cur ^ 1][1], o, v);
+              const size_t o = (size_t)z * d * dh + (size_t)m * dh + n;
+              if (last) {
+                if (row_ok) st_f32x32(p.X + o, v);
+              } else {
+                if (row_ok) st_op32<SPLIT>(p.Xop[cur ^ 1][0], p.Xop[cur ^ 1][1], o, v);
               }
             }
           }
@@ -633,17 +650,17 @@ int ns_fused_run(const NsFusedArgs& a, cudaStream_t st) {
   for (int i = 0; i < 2; ++i)
     for (int h = 0; h < 2; ++h) {
       const void* b = (h && split) ? a.Xl[i] : a.Xh[i];
-      ok &= map3(&p.mXa[i][h], b, dh, d, Z, 64, 128, dt);
-      ok &= map3(&p.mXb[i][h], b, dh, d, Z, 64, bns, dt);
-      ok &= map3(&p.mXm[i][h], b, dh, d, Z, 64, 64, dt);
+      ok &= map3(&p.mXa[i][h], b, dh, d, Z, kNsBK, 128, dt, CU_TENSOR_MAP_SWIZZLE_64B);
+      ok &= map3(&p.mXb[i][h], b, dh, d, Z, kNsBK, bns, dt, CU_TENSOR_MAP_SWIZZLE_64B);
+      ok &= map3(&p.mXm[i][h], b, dh, d, Z, 64, kNsBK, dt);
       p.Xop[i][h] = const_cast<void*>(b);
     }
   for (int h = 0; h < 2; ++h) {
     const void* rb = (h && split) ? a.Rl : a.Rh;
     const void* pb = (h && split) ? a.Pl : a.Ph;
-    ok &= map3(&p.mRa[h], rb, d, d, Z, 64, 128, dt);
-    ok &= map3(&p.mRb[h], rb, d, d, Z, 64, bns, dt);
-    ok &= map3(&p.mPa[h], pb, d, d, Z, 64, 128, dt);
+    ok &= map3(&p.mRa[h], rb, d, d, Z, kNsBK, 128, dt, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= map3(&p.mRb[h], rb, d, d, Z, kNsBK, bns, dt, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= map3(&p.mPa[h], pb, d, d, Z, kNsBK, 128, dt, CU_TENSOR_MAP_SWIZZLE_64B);
     p.Rop[h] = const_cast<void*>(rb);
     p.Pop[h] = const_cast<void*>(pb);
   }
