@@ -203,6 +203,27 @@ def kernel_flops_per_launch(spec, kind: int, launches: int) -> float:
     return f / launches
 
 
+def executed_mma_flops(spec) -> float:
+    """FLOP the tensor-core path actually issues per step in its default split
+    precision: products with one exact bf16 input (queries, keys, values) run
+    twice (W = hi + lo, E = hi + lo), products of two computed operands
+    (Newton-Schulz) three times; the queries' forward and the apply run once.
+    Context for the algorithmic figure, which counts every product once."""
+    if spec.fast_net != "swiglu":
+        return None
+    heads = spec.B * spec.H
+    mask = spec.update_mask()
+    upd_tok = sum(min(spec.T, (c + 1) * spec.chunk) - c * spec.chunk for c in range(spec.n_chunks) if mask[c])
+    n_upd = int(mask.sum())
+    d, dh = spec.d, spec.dh
+    m, n = min(d, dh), max(d, dh)
+    f = 4.0 * d * dh * spec.T + 2.0 * d * dh * spec.T          # queries' [A|B], apply
+    f += 2 * 6.0 * d * dh * upd_tok + 2 * 6.0 * d * dh * upd_tok  # keys' forward, gradient (split)
+    if spec.muon:
+        f += 3 * n_upd * 3 * spec.ns_iters * (4.0 * m * m * n + 2.0 * m ** 3)
+    return heads * f
+
+
 def linear_bytes_per_step(spec) -> float:
     """HBM bytes of the linear small-chunk layer: Q, K, V read and O written
     once (storage type), lr read once, W0 read and Wf written (fp32)."""
@@ -337,6 +358,8 @@ def run_ours(args, rank, local, world, pg):
     roof["traffic"] = read_traffic(top_name, spec.name)
     layer_flops = accounting.algorithmic_flops(spec)
     layer_tflops = layer_flops / (ms_local * 1e-3) / 1e12
+    mma = executed_mma_flops(spec)
+    mma_tflops = mma / (ms_local * 1e-3) / 1e12 if mma else None
     shares = {nm: {"share": round(v[1] / all_ms, 4), "launches_per_step": v[3] / args.steps,
                    "ms_per_launch": round(v[1] / max(v[2], 1), 5)} for nm, v in kinds.items()}
 
@@ -348,6 +371,8 @@ def run_ours(args, rank, local, world, pg):
         "roofline": roof, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk.summary(), "layer_tflops": layer_tflops,
         "layer_frac_of_peak": layer_tflops / peaks["bf16_tflops_sustained"] if spec.fast_net != "linear" else None,
+        "mma_tflops_executed": mma_tflops,
+        "mma_frac_executed": mma_tflops / peaks["bf16_tflops_sustained"] if mma_tflops else None,
         "kernel_shares": shares, "peaks_source": peak_src,
     }
 
@@ -527,6 +552,7 @@ def main():
             "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "layer_tflops": res["layer_tflops"], "layer_frac_of_peak": res["layer_frac_of_peak"],
+            "mma_tflops_executed": res["mma_tflops_executed"], "mma_frac_executed": res["mma_frac_executed"],
             "kernel_shares": res["kernel_shares"], "step_ms_all": res["step_ms_all"]}
     print(json.dumps(line), flush=True)
     if pg is not None:

@@ -1,5 +1,6 @@
 // C-ABI front end: argument validation, kernel-family selection, workspace
 // planning, the device status word and the host-buffer wrapper.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -11,6 +12,7 @@ namespace {
 
 constexpr int kAbiVersion = 1;
 constexpr int64_t kMaxElems = int64_t(1) << 40;
+constexpr int kMaxPipelineChunks = 512;  // per-chunk events of ttt_fwd_host
 
 int elem_bytes(int dtype) { return dtype == TTT_DTYPE_F32 ? 4 : 2; }
 
@@ -169,9 +171,17 @@ int ttt_workspace_bytes(const ttt_cfg* cfg, size_t* bytes) {
   return TTT_OK;
 }
 
-int ttt_fwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
-            const float* W0_1, const float* W0_2, const float* W0_3, void* O, float* Wf_1,
-            float* Wf_2, float* Wf_3, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace ttt {
+
+// The layer on device buffers. With `ready` / `done` (one event per chunk) the
+// tensor-core family waits for ready[c] before chunk c and records done[c]
+// after it; the other families wait for every ready event first.
+int fwd_device(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+               const float* W0_1, const float* W0_2, const float* W0_3, void* O, float* Wf_1, float* Wf_2,
+               float* Wf_3, void* workspace, size_t workspace_bytes, void* stream, const cudaEvent_t* ready,
+               const cudaEvent_t* done) {
   int v = validate_cfg(cfg);
   if (v != TTT_OK) return v;
   const ttt_cfg& g = *cfg;
@@ -225,6 +235,14 @@ int ttt_fwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, con
   if (g.update_mask)
     for (int i = 0; i < c.n_chunks; ++i)
       if (!g.update_mask[i]) { c.mask_all = false; break; }
+  if (ready && (impl != TTT_IMPL_TC || g.check_finite)) {
+    // no per-chunk pipelining: every input must have arrived before anything runs
+    for (int i = 0; i < c.n_chunks; ++i)
+      if (cudaStreamWaitEvent(c.stream, ready[i], 0) != cudaSuccess) return TTT_ERR_CUDA;
+  } else {
+    c.chunk_ready = ready;
+  }
+  c.chunk_done = impl == TTT_IMPL_TC ? done : nullptr;
   if (cudaMemsetAsync(workspace, 0, sizeof(int), c.stream) != cudaSuccess) return TTT_ERR_CUDA;
   if (g.check_finite) {
     v = launch_check_finite(c);
@@ -235,6 +253,17 @@ int ttt_fwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, con
     case TTT_IMPL_LINEAR: return linear_run(c);
     default: return simt_run(c);
   }
+}
+
+}  // namespace ttt
+
+extern "C" {
+
+int ttt_fwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+            const float* W0_1, const float* W0_2, const float* W0_3, void* O, float* Wf_1,
+            float* Wf_2, float* Wf_3, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_device(cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1, Wf_2, Wf_3, workspace, workspace_bytes, stream,
+                    nullptr, nullptr);
 }
 
 int ttt_status(void* workspace, void* stream) {
@@ -269,19 +298,20 @@ int ttt_fwd_host(const ttt_cfg* cfg, const void* Q, const void* K, const void* V
     return TTT_ERR_WORKSPACE;
   const ttt_cfg& g = *cfg;
   const Sizes s = tensor_sizes(g);
-  const void* hin[4] = {Q, K, V, lr};
-  const size_t in_bytes[4] = {s.tok_bytes, s.tok_bytes, s.tok_bytes, s.lr_bytes};
+  const void* hin[3] = {Q, K, V};
   const float* hw0[3] = {W0_1, W0_2, W0_3};
   float* hwf[3] = {Wf_1, Wf_2, Wf_3};
   for (const void* p : hin)
     if (!p) return TTT_ERR_ARG;
-  if (!O) return TTT_ERR_ARG;
+  if (!lr || !O) return TTT_ERR_ARG;
   for (int j = 0; j < s.nw; ++j)
     if (!hw0[j] || !hwf[j]) return TTT_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* p = static_cast<char*>(arena);
-  void* din[4];
-  for (int i = 0; i < 4; ++i) { din[i] = p; p += align_up(in_bytes[i], 256); }
+  void* din[3];
+  for (int i = 0; i < 3; ++i) { din[i] = p; p += align_up(s.tok_bytes, 256); }
+  float* dlr = reinterpret_cast<float*>(p);
+  p += align_up(s.lr_bytes, 256);
   float* dw0[3] = {nullptr, nullptr, nullptr};
   float* dwf[3] = {nullptr, nullptr, nullptr};
   for (int j = 0; j < s.nw; ++j) { dw0[j] = reinterpret_cast<float*>(p); p += align_up(s.w0_bytes[j], 256); }
@@ -291,20 +321,87 @@ int ttt_fwd_host(const ttt_cfg* cfg, const void* Q, const void* K, const void* V
   void* dws = p;
   size_t ws_bytes = 0;
   ttt_workspace_bytes(cfg, &ws_bytes);
-  for (int i = 0; i < 4; ++i)
-    if (cudaMemcpyAsync(din[i], hin[i], in_bytes[i], cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return TTT_ERR_CUDA;
-  for (int j = 0; j < s.nw; ++j)
+
+  // Chunk-pipelined copies: chunk c's queries, keys and values go in on one
+  // copy stream while earlier chunks compute, and chunk c's outputs come back
+  // on another as soon as they are written. Every (b, h) row block of a chunk
+  // is one strided 2D copy. With pageable host memory the copies still run,
+  // but without overlap.
+  const int n_chunks = (g.T + g.chunk - 1) / g.chunk;
+  const size_t es = g.dtype == TTT_DTYPE_F32 ? 4 : 2;
+  const size_t row_pitch = (size_t)g.T * g.d * es;  // one (b, h) block of Q, K, V or O
+  const size_t BH = (size_t)g.B * g.H;
+  const bool pipelined = select_impl(g) == TTT_IMPL_TC && n_chunks <= kMaxPipelineChunks;
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t ev[2 * kMaxPipelineChunks + 1];
+  int n_ev = 0;
+  int rc = TTT_OK;
+  auto fail = [&](int code) { rc = code; };
+  if (cudaMemcpyAsync(dlr, lr, s.lr_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) fail(TTT_ERR_CUDA);
+  for (int j = 0; j < s.nw && rc == TTT_OK; ++j)
     if (cudaMemcpyAsync(dw0[j], hw0[j], s.w0_bytes[j], cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return TTT_ERR_CUDA;
-  v = ttt_fwd(cfg, din[0], din[1], din[2], static_cast<const float*>(din[3]), dw0[0], dw0[1], dw0[2],
-              dO, dwf[0], dwf[1], dwf[2], dws, ws_bytes, stream);
-  if (v != TTT_OK) return v;
-  if (cudaMemcpyAsync(O, dO, s.tok_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return TTT_ERR_CUDA;
-  for (int j = 0; j < s.nw; ++j)
+      fail(TTT_ERR_CUDA);
+  if (rc == TTT_OK && pipelined) {
+    if (cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking) != cudaSuccess)
+      fail(TTT_ERR_CUDA);
+    for (int i = 0; i < 2 * n_chunks + 1 && rc == TTT_OK; ++i) {
+      if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) fail(TTT_ERR_CUDA);
+      else n_ev = i + 1;
+    }
+  }
+  if (rc == TTT_OK && pipelined) {
+    cudaEvent_t* ready = ev;
+    cudaEvent_t* done = ev + n_chunks;
+    cudaEvent_t start = ev[2 * n_chunks];
+    // the copy streams start after everything enqueued on `stream` so far
+    if (cudaEventRecord(start, st) != cudaSuccess || cudaStreamWaitEvent(cin, start, 0) != cudaSuccess)
+      fail(TTT_ERR_CUDA);
+    for (int ci = 0; ci < n_chunks && rc == TTT_OK; ++ci) {
+      const size_t off = (size_t)ci * g.chunk * g.d * es;
+      const size_t width = (size_t)std::min(g.chunk, g.T - ci * g.chunk) * g.d * es;
+      for (int i = 0; i < 3 && rc == TTT_OK; ++i)
+        if (cudaMemcpy2DAsync(static_cast<char*>(din[i]) + off, row_pitch, static_cast<const char*>(hin[i]) + off,
+                              row_pitch, width, BH, cudaMemcpyHostToDevice, cin) != cudaSuccess)
+          fail(TTT_ERR_CUDA);
+      if (rc == TTT_OK && cudaEventRecord(ready[ci], cin) != cudaSuccess) fail(TTT_ERR_CUDA);
+    }
+    if (rc == TTT_OK) {
+      const int r = fwd_device(cfg, din[0], din[1], din[2], dlr, dw0[0], dw0[1], dw0[2], dO, dwf[0], dwf[1],
+                               dwf[2], dws, ws_bytes, stream, ready, done);
+      if (r != TTT_OK) fail(r);
+    }
+    for (int ci = 0; ci < n_chunks && rc == TTT_OK; ++ci) {
+      const size_t off = (size_t)ci * g.chunk * g.d * es;
+      const size_t width = (size_t)std::min(g.chunk, g.T - ci * g.chunk) * g.d * es;
+      if (cudaStreamWaitEvent(cout, done[ci], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync(static_cast<char*>(O) + off, row_pitch, static_cast<const char*>(dO) + off, row_pitch,
+                            width, BH, cudaMemcpyDeviceToHost, cout) != cudaSuccess)
+        fail(TTT_ERR_CUDA);
+    }
+  } else if (rc == TTT_OK) {
+    for (int i = 0; i < 3 && rc == TTT_OK; ++i)
+      if (cudaMemcpyAsync(din[i], hin[i], s.tok_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        fail(TTT_ERR_CUDA);
+    if (rc == TTT_OK) {
+      const int r = fwd_device(cfg, din[0], din[1], din[2], dlr, dw0[0], dw0[1], dw0[2], dO, dwf[0], dwf[1],
+                               dwf[2], dws, ws_bytes, stream, nullptr, nullptr);
+      if (r != TTT_OK) fail(r);
+    }
+    if (rc == TTT_OK && cudaMemcpyAsync(O, dO, s.tok_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      fail(TTT_ERR_CUDA);
+  }
+  for (int j = 0; j < s.nw && rc == TTT_OK; ++j)
     if (cudaMemcpyAsync(hwf[j], dwf[j], s.wf_bytes[j], cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return TTT_ERR_CUDA;
-  return ttt_status(dws, stream);
+      fail(TTT_ERR_CUDA);
+  // wait for everything this call enqueued, then release the streams and events
+  if (cin && cudaStreamSynchronize(cin) != cudaSuccess) fail(TTT_ERR_CUDA);
+  if (cout && cudaStreamSynchronize(cout) != cudaSuccess) fail(TTT_ERR_CUDA);
+  const int status = ttt_status(dws, stream);
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+  if (cin) cudaStreamDestroy(cin);
+  if (cout) cudaStreamDestroy(cout);
+  return rc != TTT_OK ? rc : status;
 }
 
 const char* ttt_strerror(int status) {

@@ -26,6 +26,11 @@ struct Call {
   cudaStream_t stream;
   bool mask_all;                // every chunk updates
   const uint8_t* mask;          // host flags (may be NULL when mask_all)
+  // host-buffer pipelining (tensor-core family): the stream waits for
+  // chunk_ready[c] before chunk c reads its inputs and records chunk_done[c]
+  // once chunk c's outputs are written (both NULL: no per-chunk events)
+  const cudaEvent_t* chunk_ready;
+  const cudaEvent_t* chunk_done;
 };
 
 inline bool call_updates(const Call& c, int chunk) {

@@ -11,13 +11,16 @@
 // the kernel is bound by HBM bandwidth and per-chunk latency, not by tensor
 // throughput. Design:
 //   * one CTA per (batch, head), two CTAs per SM (every head resident at once);
+//   * every warp takes 16 rows of the queries' and the keys' products, then 16
+//     rows of G, so the four warps carry equal work between the two barriers;
 //   * W lives in registers in fp32 (each thread owns 32 entries in the layout of
 //     the G accumulator), with a bf16 hi/lo copy in shared memory for the MMAs;
 //   * Q, K, V tiles (64 x 64 bf16, 128-byte swizzle) and the lr tile stream in
 //     through a 3-stage TMA ring, so the next chunks load while one computes;
 //   * the 64 x 64 x 64 products run on warp-level bf16 MMAs (m16n8k16) with fp32
-//     accumulation; the keys' product and G use hi + lo operands (the inputs are
-//     exact bf16), so W accumulates its updates at ~16-bit operand precision.
+//     accumulation; in SPLIT precision (the default) the keys' product and G use
+//     hi + lo operands (the inputs are exact bf16), so W accumulates its updates
+//     at ~16-bit operand precision; SINGLE precision drops the lo products.
 // Waits on the TMA barriers are bounded (timeout -> status word, no trap).
 #include "tc_kernel.cuh"
 #include "tc_util.cuh"
@@ -48,6 +51,7 @@ struct LinParams {
   MaskBits mask;
   int has_mask;
   int stall;               // test hook: never start the loads, so the first wait runs out
+  int split;               // W and eta*R carried as bf16 hi + lo (TTT_PREC_SPLIT)
   TcCommon cm;
 };
 
@@ -194,27 +198,23 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     const float* slr = reinterpret_cast<const float*>(st + 3 * kTileBytes);
     const int t_base = u * kTile;
 
-    // ---- phase 1: warps 0-1 O = Q W^T (rows 32w..), warps 2-3 R = K W^T - V
-    const bool keys = warp >= 2;
-    if (!keys || (upd && p.mse)) {
-      const uint32_t sx = keys ? sk : sq;
-      const int r0 = 32 * (warp & 1);
-      float acc[2][8][4];
+    // ---- phase 1: warp w computes rows [16w, 16w + 16) of O = Q W^T and, for
+    // an MSE update, of R = K W^T - V (the keys' product with W = hi + lo)
+    {
+      const int r0 = 16 * warp;
+      const bool do_r = upd && p.mse;
+      float ao[8][4], ar[8][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
+        for (int q = 0; q < 4; ++q) ao[nt][q] = ar[nt][q] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int row = r0 + 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int col = 16 * ks + 8 * (lane >> 4);
-          ldsm_x4(sx + swz(row, col), a[mt][0], a[mt][1], a[mt][2], a[mt][3]);
-        }
+        const int arow = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int acol = 16 * ks + 8 * (lane >> 4);
+        uint32_t aq[4], ak[4];
+        ldsm_x4(sq + swz(arow, acol), aq[0], aq[1], aq[2], aq[3]);
+        if (do_r) ldsm_x4(sk + swz(arow, acol), ak[0], ak[1], ak[2], ak[3]);
 #pragma unroll
         for (int np = 0; np < 4; ++np) {  // pairs of n-tiles
           // matrices: (n 0-7, k 0-7), (n 0-7, k 8-15), (n 8-15, k 0-7), (n 8-15, k 8-15)
@@ -222,64 +222,47 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
           const int kcol = 16 * ks + 8 * ((lane >> 3) & 1);
           uint32_t b[4];
           ldsm_x4(wh_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            mma16816(acc[mt][2 * np], a[mt], b[0], b[1]);
-            mma16816(acc[mt][2 * np + 1], a[mt], b[2], b[3]);
-          }
-          if (keys) {
-            ldsm_x4(wl_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-              mma16816(acc[mt][2 * np], a[mt], b[0], b[1]);
-              mma16816(acc[mt][2 * np + 1], a[mt], b[2], b[3]);
+          mma16816(ao[2 * np], aq, b[0], b[1]);
+          mma16816(ao[2 * np + 1], aq, b[2], b[3]);
+          if (do_r) {
+            mma16816(ar[2 * np], ak, b[0], b[1]);
+            mma16816(ar[2 * np + 1], ak, b[2], b[3]);
+            if (p.split) {
+              ldsm_x4(wl_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
+              mma16816(ar[2 * np], ak, b[0], b[1]);
+              mma16816(ar[2 * np + 1], ak, b[2], b[3]);
             }
           }
         }
       }
-      if (!keys) {
-        // O rows: token t_base + row, bf16
+      // O rows: token t_base + row, bf16
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+      for (int hq = 0; hq < 2; ++hq) {
+        const int row = r0 + g + 8 * hq;
+        if (t_base + row < p.T) {
+          __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
 #pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const int row = r0 + 16 * mt + g + 8 * hq;
-            if (t_base + row < p.T) {
-              __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
-#pragma unroll
-              for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<uint32_t*>(dst + nt * 8 + 2 * c4) = bf2(acc[mt][nt][2 * hq], acc[mt][nt][2 * hq + 1]);
-            }
-          }
-      } else {
-        // eta * (K W^T - V) -> hi/lo operands, [t][i]
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const int row = r0 + 16 * mt + g + 8 * hq;
-            const float eta = slr[row];
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-              const int col = nt * 8 + 2 * c4;
-              const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(sv + swz(row, col));
-              const float x = eta * (acc[mt][nt][2 * hq] - __low2float(v2));
-              const float y = eta * (acc[mt][nt][2 * hq + 1] - __high2float(v2));
-              *reinterpret_cast<uint32_t*>(rh + swz(row, col)) = bf2(x, y);
-              *reinterpret_cast<uint32_t*>(rl + swz(row, col)) = bf2(bf_lo(x), bf_lo(y));
-            }
-          }
+          for (int nt = 0; nt < 8; ++nt)
+            *reinterpret_cast<uint32_t*>(dst + nt * 8 + 2 * c4) = bf2(ao[nt][2 * hq], ao[nt][2 * hq + 1]);
+        }
       }
-    } else if (upd) {
-      // inner-product loss: dl/df = -v, so eta * R = -eta * v (exact in bf16 up to eta)
-      const int r0 = 32 * (warp & 1);
-      for (int e = lane; e < 32 * 32; e += 32) {
-        const int row = r0 + e / 32, col = 2 * (e % 32);
-        const float eta = slr[row];
-        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(sv + swz(row, col));
-        const float x = -eta * __low2float(v2), y = -eta * __high2float(v2);
-        *reinterpret_cast<uint32_t*>(rh + swz(row, col)) = bf2(x, y);
-        *reinterpret_cast<uint32_t*>(rl + swz(row, col)) = bf2(bf_lo(x), bf_lo(y));
+      if (upd) {
+        // eta * dl/df -> hi/lo operands, [t][i]: (K W^T - V) for MSE, -V for the
+        // inner product
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          const int row = r0 + g + 8 * hq;
+          const float eta = slr[row];
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) {
+            const int col = nt * 8 + 2 * c4;
+            const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(sv + swz(row, col));
+            const float x = eta * (ar[nt][2 * hq] - __low2float(v2));
+            const float y = eta * (ar[nt][2 * hq + 1] - __high2float(v2));
+            *reinterpret_cast<uint32_t*>(rh + swz(row, col)) = bf2(x, y);
+            *reinterpret_cast<uint32_t*>(rl + swz(row, col)) = bf2(bf_lo(x), bf_lo(y));
+          }
+        }
       }
     }
     __syncthreads();
@@ -304,8 +287,10 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
           ldsm_x4_t(sk + swz(kt, jc), b[0], b[1], b[2], b[3]);
           mma16816(Gacc[2 * np], ah, b[0], b[1]);
           mma16816(Gacc[2 * np + 1], ah, b[2], b[3]);
-          mma16816(Gacc[2 * np], al, b[0], b[1]);
-          mma16816(Gacc[2 * np + 1], al, b[2], b[3]);
+          if (p.split) {
+            mma16816(Gacc[2 * np], al, b[0], b[1]);
+            mma16816(Gacc[2 * np + 1], al, b[2], b[3]);
+          }
         }
       }
       if (chunk_end) {
@@ -392,6 +377,7 @@ int linear_run(const Call& c) {
   p.step = g.step;
   p.has_mask = c.mask_all ? 0 : 1;
   p.stall = g_linear_stall_next ? 1 : 0;
+  p.split = g.precision == TTT_PREC_SPLIT ? 1 : 0;
   g_linear_stall_next = 0;
   if (p.has_mask)
     for (int i = 0; i < c.n_chunks; ++i)

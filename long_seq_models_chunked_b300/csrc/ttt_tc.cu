@@ -632,6 +632,33 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
   return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+// A side stream (and two events) per device and host thread, created on first
+// use, for the apply that overlaps the gradient. Returns NULL if it cannot be
+// created (the caller then runs everything on its own stream).
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t fwd_done, apply_done;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDev = 64;
+  thread_local SideStream slots[kMaxDev];
+  thread_local bool made[kMaxDev] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  if (!made[dev]) {
+    SideStream& x = slots[dev];
+    if (cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&x.fwd_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.apply_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    made[dev] = true;
+  }
+  return &slots[dev];
+}
+
 struct Plan {
   int BH, Z, d, dh, C, Cp, T, split;
   int bn_o;               // N tile of the apply GEMM (over d)
@@ -801,16 +828,16 @@ int tc_run(const Call& c) {
     p.cm = cm;
     return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, BH * p.n_js * p.groups * (p.q + p.k), st);
   };
-  auto run_o = [&](int s, int valid) -> int {
+  auto run_o = [&](int s, int valid, cudaStream_t os) -> int {
     const int mt = (valid + BM - 1) / BM, nt = (d + P.bn_o - 1) / P.bn_o;
     auto fill = [&](auto& p) {
       p.mH = mHq; p.mW2 = mW2o; p.O = static_cast<bf16*>(c.O);
       p.d = d; p.dh = dh; p.T = T; p.chunk_start = s; p.valid = valid; p.m_tiles = mt; p.n_tiles = nt; p.cm = cm;
     };
     const dim3 grid(mt * nt, BH);
-    if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(TTT_KERNEL_APPLY, p, grid, st); }
-    if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, st); }
-    typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(TTT_KERNEL_APPLY, p, grid, st);
+    if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(TTT_KERNEL_APPLY, p, grid, os); }
+    if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, os); }
+    typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(TTT_KERNEL_APPLY, p, grid, os);
   };
   auto run_grad = [&](int ci, int s, int valid) -> int {
     const bool full = (s + P.C <= T) && ci < n_full;
@@ -857,14 +884,32 @@ int tc_run(const Call& c) {
     return g.muon ? ns_fused_run(nsa, st) : run_update();
   };
 
+  // In shifted mode the apply of a chunk (O = H_q W2^T) and its gradient are
+  // independent: the apply runs on a side stream between the forward and the
+  // Muon step (which rewrites the weights the apply reads).
+  SideStream* side = side_stream();
   for (int ci = 0; ci < c.n_chunks; ++ci) {
     const int s = ci * g.chunk;
     const int valid = std::min(g.chunk, T - s);
     const bool upd = call_updates(c, ci);
+    if (c.chunk_ready && cudaStreamWaitEvent(st, c.chunk_ready[ci], 0) != cudaSuccess) return TTT_ERR_CUDA;
     if (g.mode == TTT_MODE_SHIFTED) {
       rc = run_fwd(s, valid, true, upd);
-      if (rc == TTT_OK) rc = run_o(s, valid);
-      if (rc == TTT_OK && upd) rc = do_update(ci, s, valid);
+      if (rc == TTT_OK && upd && side) {
+        cudaStream_t os = side->stream;
+        if (cudaEventRecord(side->fwd_done, st) != cudaSuccess || cudaStreamWaitEvent(os, side->fwd_done, 0) != cudaSuccess)
+          return TTT_ERR_CUDA;
+        rc = run_o(s, valid, os);
+        if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], os) != cudaSuccess) rc = TTT_ERR_CUDA;
+        if (rc == TTT_OK && cudaEventRecord(side->apply_done, os) != cudaSuccess) rc = TTT_ERR_CUDA;
+        if (rc == TTT_OK) rc = run_grad(ci, s, valid);
+        if (rc == TTT_OK && cudaStreamWaitEvent(st, side->apply_done, 0) != cudaSuccess) rc = TTT_ERR_CUDA;
+        if (rc == TTT_OK) rc = g.muon ? ns_fused_run(nsa, st) : run_update();
+      } else {
+        if (rc == TTT_OK) rc = run_o(s, valid, st);
+        if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], st) != cudaSuccess) rc = TTT_ERR_CUDA;
+        if (rc == TTT_OK && upd) rc = do_update(ci, s, valid);
+      }
     } else {
       rc = TTT_OK;
       if (upd) {
@@ -872,7 +917,8 @@ int tc_run(const Call& c) {
         if (rc == TTT_OK) rc = do_update(ci, s, valid);
       }
       if (rc == TTT_OK) rc = run_fwd(s, valid, true, false);
-      if (rc == TTT_OK) rc = run_o(s, valid);
+      if (rc == TTT_OK) rc = run_o(s, valid, st);
+      if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], st) != cudaSuccess) rc = TTT_ERR_CUDA;
     }
     if (rc != TTT_OK) return rc;
   }
