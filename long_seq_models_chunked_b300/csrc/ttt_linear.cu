@@ -11,8 +11,8 @@
 // the kernel is bound by HBM bandwidth and per-chunk latency, not by tensor
 // throughput. Design:
 //   * one CTA per (batch, head), two CTAs per SM (every head resident at once);
-//   * every warp takes 16 rows of the queries' and the keys' products, then 16
-//     rows of G, so the four warps carry equal work between the two barriers;
+//   * eight warps: each takes a 16 x 32 block of the queries' and the keys'
+//     products, then of G, so all carry equal work between the two barriers;
 //   * W lives in registers in fp32 (each thread owns 32 entries in the layout of
 //     the G accumulator), with a bf16 hi/lo copy in shared memory for the MMAs;
 //   * Q, K, V tiles (64 x 64 bf16, 128-byte swizzle) and the lr tile stream in
@@ -32,7 +32,7 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kLinThreads = 128;
+constexpr int kLinThreads = 256;  // 8 warps: 4 row blocks x 2 column halves
 constexpr int kLinD = 64;
 constexpr int kTile = 64;               // tokens per tile
 constexpr int kLinStages = 3;
@@ -132,26 +132,28 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
   if (tid == 0)
     for (int u = 0; u < kLinStages && u < p.n_tiles && !p.stall; ++u) issue(u);
 
-  // ---- W in registers: warp w owns rows i in [16w, 16w + 16), the layout of
-  // a 16 x 64 accumulator (8 n-tiles x 4 values per thread)
-  float W[8][4];
+  // ---- W in registers: warp w owns rows i in [16 mr, 16 mr + 16) and columns
+  // [32 nh, 32 nh + 32) (mr = w % 4, nh = w / 4), the layout of a 16 x 32
+  // accumulator (4 n-tiles x 4 values per thread)
+  const int mr = warp & 3, nh = warp >> 2;
+  float W[4][4];
   {
     const float* w0 = p.W0 + (size_t)(p.w0_per_batch ? bh : h) * kLinD * kLinD;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int i = 16 * warp + g + (q >> 1) * 8, j = nt * 8 + 2 * c4 + (q & 1);
-        W[nt][q] = w0[i * kLinD + j];
+        const int i = 16 * mr + g + (q >> 1) * 8, j = (4 * nh + ln) * 8 + 2 * c4 + (q & 1);
+        W[ln][q] = w0[i * kLinD + j];
       }
   }
   auto write_w_operands = [&]() {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
-        const int i = 16 * warp + g + hq * 8, j = nt * 8 + 2 * c4;
-        const float x = W[nt][2 * hq], y = W[nt][2 * hq + 1];
+        const int i = 16 * mr + g + hq * 8, j = (4 * nh + ln) * 8 + 2 * c4;
+        const float x = W[ln][2 * hq], y = W[ln][2 * hq + 1];
         *reinterpret_cast<uint32_t*>(wh + swz(i, j)) = bf2(x, y);
         *reinterpret_cast<uint32_t*>(wl + swz(i, j)) = bf2(bf_lo(x), bf_lo(y));
       }
@@ -159,11 +161,11 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
   write_w_operands();
   __syncthreads();
 
-  float Gacc[8][4];
+  float Gacc[4][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) Gacc[nt][q] = 0.f;
+    for (int q = 0; q < 4; ++q) Gacc[ln][q] = 0.f;
 
   const int tiles_per_chunk = p.chunk / kTile;
   const uint32_t wh_a = ptx::smem_u32(wh), wl_a = ptx::smem_u32(wl);
@@ -198,16 +200,17 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     const float* slr = reinterpret_cast<const float*>(st + 3 * kTileBytes);
     const int t_base = u * kTile;
 
-    // ---- phase 1: warp w computes rows [16w, 16w + 16) of O = Q W^T and, for
-    // an MSE update, of R = K W^T - V (the keys' product with W = hi + lo)
+    // ---- phase 1: warp (mr, nh) computes rows [16 mr, +16) x columns [32 nh, +32)
+    // of O = Q W^T and, for an MSE update, of R = K W^T - V (keys' product with
+    // W = hi + lo)
     {
-      const int r0 = 16 * warp;
+      const int r0 = 16 * mr;
       const bool do_r = upd && p.mse;
-      float ao[8][4], ar[8][4];
+      float ao[4][4], ar[4][4];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+      for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ao[nt][q] = ar[nt][q] = 0.f;
+        for (int q = 0; q < 4; ++q) ao[ln][q] = ar[ln][q] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const int arow = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -216,21 +219,21 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
         ldsm_x4(sq + swz(arow, acol), aq[0], aq[1], aq[2], aq[3]);
         if (do_r) ldsm_x4(sk + swz(arow, acol), ak[0], ak[1], ak[2], ak[3]);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {  // pairs of n-tiles
+        for (int lp = 0; lp < 2; ++lp) {  // this warp's pairs of n-tiles
           // matrices: (n 0-7, k 0-7), (n 0-7, k 8-15), (n 8-15, k 0-7), (n 8-15, k 8-15)
-          const int nrow = 16 * np + (lane & 7) + 8 * (lane >> 4);
+          const int nrow = 16 * (2 * nh + lp) + (lane & 7) + 8 * (lane >> 4);
           const int kcol = 16 * ks + 8 * ((lane >> 3) & 1);
           uint32_t b[4];
           ldsm_x4(wh_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
-          mma16816(ao[2 * np], aq, b[0], b[1]);
-          mma16816(ao[2 * np + 1], aq, b[2], b[3]);
+          mma16816(ao[2 * lp], aq, b[0], b[1]);
+          mma16816(ao[2 * lp + 1], aq, b[2], b[3]);
           if (do_r) {
-            mma16816(ar[2 * np], ak, b[0], b[1]);
-            mma16816(ar[2 * np + 1], ak, b[2], b[3]);
+            mma16816(ar[2 * lp], ak, b[0], b[1]);
+            mma16816(ar[2 * lp + 1], ak, b[2], b[3]);
             if (p.split) {
               ldsm_x4(wl_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
-              mma16816(ar[2 * np], ak, b[0], b[1]);
-              mma16816(ar[2 * np + 1], ak, b[2], b[3]);
+              mma16816(ar[2 * lp], ak, b[0], b[1]);
+              mma16816(ar[2 * lp + 1], ak, b[2], b[3]);
             }
           }
         }
@@ -242,8 +245,8 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
         if (t_base + row < p.T) {
           __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
 #pragma unroll
-          for (int nt = 0; nt < 8; ++nt)
-            *reinterpret_cast<uint32_t*>(dst + nt * 8 + 2 * c4) = bf2(ao[nt][2 * hq], ao[nt][2 * hq + 1]);
+          for (int ln = 0; ln < 4; ++ln)
+            *reinterpret_cast<uint32_t*>(dst + (4 * nh + ln) * 8 + 2 * c4) = bf2(ao[ln][2 * hq], ao[ln][2 * hq + 1]);
         }
       }
       if (upd) {
@@ -254,11 +257,11 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
           const int row = r0 + g + 8 * hq;
           const float eta = slr[row];
 #pragma unroll
-          for (int nt = 0; nt < 8; ++nt) {
-            const int col = nt * 8 + 2 * c4;
+          for (int ln = 0; ln < 4; ++ln) {
+            const int col = (4 * nh + ln) * 8 + 2 * c4;
             const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(sv + swz(row, col));
-            const float x = eta * (ar[nt][2 * hq] - __low2float(v2));
-            const float y = eta * (ar[nt][2 * hq + 1] - __high2float(v2));
+            const float x = eta * (ar[ln][2 * hq] - __low2float(v2));
+            const float y = eta * (ar[ln][2 * hq + 1] - __high2float(v2));
             *reinterpret_cast<uint32_t*>(rh + swz(row, col)) = bf2(x, y);
             *reinterpret_cast<uint32_t*>(rl + swz(row, col)) = bf2(bf_lo(x), bf_lo(y));
           }
@@ -267,39 +270,40 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     }
     __syncthreads();
 
-    // ---- phase 2: G += (eta R)^T K, warp w rows i in [16w, 16w + 16)
+    // ---- phase 2: G += (eta R)^T K, warp (mr, nh): rows i in [16 mr, +16),
+    // columns j in [32 nh, +32)
     if (upd) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per step
         // A = (eta R)^T: rows i, cols t; stored [t][i] -> transposed loads
         const int trow = 16 * ks + (lane & 7) + 8 * (lane >> 4);
-        const int icol = 16 * warp + 8 * ((lane >> 3) & 1);
+        const int icol = 16 * mr + 8 * ((lane >> 3) & 1);
         uint32_t ah[4], al[4];
         ldsm_x4_t(rh_a + swz(trow, icol), ah[0], ah[1], ah[2], ah[3]);
         ldsm_x4_t(rl_a + swz(trow, icol), al[0], al[1], al[2], al[3]);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
+        for (int lp = 0; lp < 2; ++lp) {
           // B = K: rows t (k), cols j (n), stored [t][j] -> transposed loads;
           // matrices: (t 0-7, j 0-7), (t 8-15, j 0-7), (t 0-7, j 8-15), (t 8-15, j 8-15)
           const int kt = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int jc = 16 * np + 8 * (lane >> 4);
+          const int jc = 16 * (2 * nh + lp) + 8 * (lane >> 4);
           uint32_t b[4];
           ldsm_x4_t(sk + swz(kt, jc), b[0], b[1], b[2], b[3]);
-          mma16816(Gacc[2 * np], ah, b[0], b[1]);
-          mma16816(Gacc[2 * np + 1], ah, b[2], b[3]);
+          mma16816(Gacc[2 * lp], ah, b[0], b[1]);
+          mma16816(Gacc[2 * lp + 1], ah, b[2], b[3]);
           if (p.split) {
-            mma16816(Gacc[2 * np], al, b[0], b[1]);
-            mma16816(Gacc[2 * np + 1], al, b[2], b[3]);
+            mma16816(Gacc[2 * lp], al, b[0], b[1]);
+            mma16816(Gacc[2 * lp + 1], al, b[2], b[3]);
           }
         }
       }
       if (chunk_end) {
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            W[nt][q] -= p.step * Gacc[nt][q];
-            Gacc[nt][q] = 0.f;
+            W[ln][q] -= p.step * Gacc[ln][q];
+            Gacc[ln][q] = 0.f;
           }
         write_w_operands();  // phase 1 of this tile is finished; nobody reads W now
       }
@@ -314,11 +318,11 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
   if (!*abort_flag) {
     float* wf = p.Wf + (size_t)bh * kLinD * kLinD;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int ln = 0; ln < 4; ++ln)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int i = 16 * warp + g + (q >> 1) * 8, j = nt * 8 + 2 * c4 + (q & 1);
-        wf[i * kLinD + j] = W[nt][q];
+        const int i = 16 * mr + g + (q >> 1) * 8, j = (4 * nh + ln) * 8 + 2 * c4 + (q & 1);
+        wf[i * kLinD + j] = W[ln][q];
       }
   } else if (tid == 0) {
     // let the copies in flight land before the CTA exits (bounded)
