@@ -32,7 +32,9 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kLinThreads = 256;  // 8 warps: 4 row blocks x 2 column halves
+constexpr int kNQ = 2;                    // column groups of 64 / kNQ columns (2 measured fastest)
+constexpr int kNT = 8 / kNQ;              // n-tiles (8 columns) per warp
+constexpr int kLinThreads = 128 * kNQ;    // 4 row blocks x kNQ column groups
 constexpr int kLinD = 64;
 constexpr int kTile = 64;               // tokens per tile
 constexpr int kLinStages = 3;
@@ -133,26 +135,26 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     for (int u = 0; u < kLinStages && u < p.n_tiles && !p.stall; ++u) issue(u);
 
   // ---- W in registers: warp w owns rows i in [16 mr, 16 mr + 16) and columns
-  // [32 nh, 32 nh + 32) (mr = w % 4, nh = w / 4), the layout of a 16 x 32
-  // accumulator (4 n-tiles x 4 values per thread)
-  const int mr = warp & 3, nh = warp >> 2;
-  float W[4][4];
+  // [8 kNT nh, 8 kNT (nh + 1)) (mr = w % 4, nh = w / 4), the layout of a
+  // 16 x 8 kNT accumulator (kNT n-tiles x 4 values per thread)
+  const int mr = warp & 3, nh = warp >> 2;  // row block, column group
+  float W[kNT][4];
   {
     const float* w0 = p.W0 + (size_t)(p.w0_per_batch ? bh : h) * kLinD * kLinD;
 #pragma unroll
-    for (int ln = 0; ln < 4; ++ln)
+    for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int i = 16 * mr + g + (q >> 1) * 8, j = (4 * nh + ln) * 8 + 2 * c4 + (q & 1);
+        const int i = 16 * mr + g + (q >> 1) * 8, j = (kNT * nh + ln) * 8 + 2 * c4 + (q & 1);
         W[ln][q] = w0[i * kLinD + j];
       }
   }
   auto write_w_operands = [&]() {
 #pragma unroll
-    for (int ln = 0; ln < 4; ++ln)
+    for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
-        const int i = 16 * mr + g + hq * 8, j = (4 * nh + ln) * 8 + 2 * c4;
+        const int i = 16 * mr + g + hq * 8, j = (kNT * nh + ln) * 8 + 2 * c4;
         const float x = W[ln][2 * hq], y = W[ln][2 * hq + 1];
         *reinterpret_cast<uint32_t*>(wh + swz(i, j)) = bf2(x, y);
         *reinterpret_cast<uint32_t*>(wl + swz(i, j)) = bf2(bf_lo(x), bf_lo(y));
@@ -161,9 +163,9 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
   write_w_operands();
   __syncthreads();
 
-  float Gacc[4][4];
+  float Gacc[kNT][4];
 #pragma unroll
-  for (int ln = 0; ln < 4; ++ln)
+  for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
     for (int q = 0; q < 4; ++q) Gacc[ln][q] = 0.f;
 
@@ -200,15 +202,15 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     const float* slr = reinterpret_cast<const float*>(st + 3 * kTileBytes);
     const int t_base = u * kTile;
 
-    // ---- phase 1: warp (mr, nh) computes rows [16 mr, +16) x columns [32 nh, +32)
+    // ---- phase 1: warp (mr, nh) computes rows [16 mr, +16) x its column group
     // of O = Q W^T and, for an MSE update, of R = K W^T - V (keys' product with
     // W = hi + lo)
     {
       const int r0 = 16 * mr;
       const bool do_r = upd && p.mse;
-      float ao[4][4], ar[4][4];
+      float ao[kNT][4], ar[kNT][4];
 #pragma unroll
-      for (int ln = 0; ln < 4; ++ln)
+      for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
         for (int q = 0; q < 4; ++q) ao[ln][q] = ar[ln][q] = 0.f;
 #pragma unroll
@@ -219,9 +221,9 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
         ldsm_x4(sq + swz(arow, acol), aq[0], aq[1], aq[2], aq[3]);
         if (do_r) ldsm_x4(sk + swz(arow, acol), ak[0], ak[1], ak[2], ak[3]);
 #pragma unroll
-        for (int lp = 0; lp < 2; ++lp) {  // this warp's pairs of n-tiles
+        for (int lp = 0; lp < kNT / 2; ++lp) {  // this warp's pairs of n-tiles
           // matrices: (n 0-7, k 0-7), (n 0-7, k 8-15), (n 8-15, k 0-7), (n 8-15, k 8-15)
-          const int nrow = 16 * (2 * nh + lp) + (lane & 7) + 8 * (lane >> 4);
+          const int nrow = 16 * (kNT / 2 * nh + lp) + (lane & 7) + 8 * (lane >> 4);
           const int kcol = 16 * ks + 8 * ((lane >> 3) & 1);
           uint32_t b[4];
           ldsm_x4(wh_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
         if (t_base + row < p.T) {
           __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
 #pragma unroll
-          for (int ln = 0; ln < 4; ++ln)
-            *reinterpret_cast<uint32_t*>(dst + (4 * nh + ln) * 8 + 2 * c4) = bf2(ao[ln][2 * hq], ao[ln][2 * hq + 1]);
+          for (int ln = 0; ln < kNT; ++ln)
+            *reinterpret_cast<uint32_t*>(dst + (kNT * nh + ln) * 8 + 2 * c4) = bf2(ao[ln][2 * hq], ao[ln][2 * hq + 1]);
         }
       }
       if (upd) {
@@ -257,8 +259,8 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
           const int row = r0 + g + 8 * hq;
           const float eta = slr[row];
 #pragma unroll
-          for (int ln = 0; ln < 4; ++ln) {
-            const int col = (4 * nh + ln) * 8 + 2 * c4;
+          for (int ln = 0; ln < kNT; ++ln) {
+            const int col = (kNT * nh + ln) * 8 + 2 * c4;
             const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(sv + swz(row, col));
             const float x = eta * (ar[ln][2 * hq] - __low2float(v2));
             const float y = eta * (ar[ln][2 * hq + 1] - __high2float(v2));
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
     __syncthreads();
 
     // ---- phase 2: G += (eta R)^T K, warp (mr, nh): rows i in [16 mr, +16),
-    // columns j in [32 nh, +32)
+    // columns j in its column group
     if (upd) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per step
@@ -282,11 +284,11 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
         ldsm_x4_t(rh_a + swz(trow, icol), ah[0], ah[1], ah[2], ah[3]);
         ldsm_x4_t(rl_a + swz(trow, icol), al[0], al[1], al[2], al[3]);
 #pragma unroll
-        for (int lp = 0; lp < 2; ++lp) {
+        for (int lp = 0; lp < kNT / 2; ++lp) {
           // B = K: rows t (k), cols j (n), stored [t][j] -> transposed loads;
           // matrices: (t 0-7, j 0-7), (t 8-15, j 0-7), (t 0-7, j 8-15), (t 8-15, j 8-15)
           const int kt = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int jc = 16 * (2 * nh + lp) + 8 * (lane >> 4);
+          const int jc = 16 * (kNT / 2 * nh + lp) + 8 * (lane >> 4);
           uint32_t b[4];
           ldsm_x4_t(sk + swz(kt, jc), b[0], b[1], b[2], b[3]);
           mma16816(Gacc[2 * lp], ah, b[0], b[1]);
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
       }
       if (chunk_end) {
 #pragma unroll
-        for (int ln = 0; ln < 4; ++ln)
+        for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             W[ln][q] -= p.step * Gacc[ln][q];
@@ -318,10 +320,10 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
   if (!*abort_flag) {
     float* wf = p.Wf + (size_t)bh * kLinD * kLinD;
 #pragma unroll
-    for (int ln = 0; ln < 4; ++ln)
+    for (int ln = 0; ln < kNT; ++ln)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int i = 16 * mr + g + (q >> 1) * 8, j = (4 * nh + ln) * 8 + 2 * c4 + (q & 1);
+        const int i = 16 * mr + g + (q >> 1) * 8, j = (kNT * nh + ln) * 8 + 2 * c4 + (q & 1);
         wf[i * kLinD + j] = W[ln][q];
       }
   } else if (tid == 0) {
