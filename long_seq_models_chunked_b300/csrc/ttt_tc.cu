@@ -816,8 +816,9 @@ int tc_run(const Call& c) {
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
-    // clusters of up to 4 consecutive token tiles share each weight slice
-    p.cs = p.n_tok >= 4 ? 4 : (p.n_tok >= 2 ? 2 : 1);
+    // pairs of consecutive token tiles share each weight slice: clusters of two
+    // fill all 148 SMs (clusters of four leave 16 idle)
+    p.cs = p.n_tok >= 2 ? 2 : 1;
     p.groups = (p.n_tok + p.cs - 1) / p.cs;
     p.n_js = dh / 64;
     p.BH = BH;
