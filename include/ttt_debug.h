@@ -24,6 +24,18 @@ extern "C" {
 TTT_API int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, float* D,
                               int Z, int M, int N, int K, void* stream);
 
+/* D[z] = A[z] * B[z]^T on 256 x 256 tiles computed by CTA pairs (tcgen05
+ * cta_group::2: the even CTA of a two-CTA cluster issues M = 256 MMAs over both
+ * CTAs' shared memory and TMEM), with the Newton-Schulz operand layouts.
+ *   A  bf16, DEVICE: [Z, M, K] (K-major)
+ *   B  bf16, DEVICE: [Z, N, K] when b_mn_major == 0, else [Z, K, N]
+ *   D  fp32, DEVICE: [Z, M, N], written
+ * M, N positive multiples of 256, K a positive multiple of 32; pointers 16-byte
+ * aligned. Synchronises `stream`; returns TTT_OK, TTT_ERR_ARG, TTT_ERR_CUDA or
+ * TTT_ERR_TIMEOUT (a wait ran out). */
+TTT_API int ttt_dbg_gemm_pair_bf16(const void* A, const void* B, int b_mn_major, float* D, int Z, int M, int N,
+                                   int K, void* stream);
+
 /* CTAs of the fused Muon kernel's cooperative grid for *cfg on the current
  * device; *resident (may be NULL) receives how many of its CTAs fit at once.
  * Returns TTT_OK, TTT_ERR_ARG (cfg not on the tensor-core path) or TTT_ERR_CUDA. */
@@ -40,6 +52,21 @@ TTT_API int ttt_dbg_split_mask(int mask);
  * default) for every later launch in this process. For tuning sweeps and tests.
  * Returns TTT_OK or TTT_ERR_ARG. */
 TTT_API int ttt_dbg_ns_force_grid(int ctas);
+
+/* Whether the fused Muon kernel may run its GEMM phases on CTA pairs
+ * (cta_group::2 tiles of 256 rows; taken when d and dh are multiples of 256).
+ * Default 1. Process-global, for comparisons and tests. Returns TTT_OK. */
+TTT_API int ttt_dbg_ns_pairs(int on);
+
+/* Phase timeline of the fused Muon kernel. With tracing on, every later launch
+ * records %globaltimer stamps (ns) into a device table: slot 0 the start,
+ * slot 1 the last CTA's exit, and for grid barrier i >= 1 (the phases end at
+ * barriers) slots 3i, 3i+1, 3i+2 the first and the last CTA's arrival and CTA
+ * 0's departure. A traced launch synchronises its stream first. read copies
+ * the first n (<= 96) slots of the last traced launch to HOST memory `out`.
+ * Return TTT_OK, TTT_ERR_ARG or TTT_ERR_CUDA. */
+TTT_API int ttt_dbg_ns_trace(int on);
+TTT_API int ttt_dbg_ns_trace_read(unsigned long long* out, int n);
 
 /* Failure-detection test: the next launch of the linear small-chunk kernel
  * issues none of its loads, so its first wait (bounded by cfg->timeout_us)

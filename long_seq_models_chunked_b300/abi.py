@@ -39,7 +39,8 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16", "ttt_prof_enable",
             "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name",
             "ttt_fwd_static_scratch", "ttt_dbg_ns_plan", "ttt_dbg_ns_force_grid",
-            "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear")
+            "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_gemm_pair_bf16", "ttt_dbg_ns_trace",
+            "ttt_dbg_ns_trace_read", "ttt_dbg_ns_pairs")
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
 TTT_KERNEL_NS = 10
@@ -93,6 +94,15 @@ def _load():
     lib.ttt_dbg_gemm_bf16.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                       c_int, c_void_p]
     lib.ttt_dbg_gemm_bf16.restype = c_int
+    lib.ttt_dbg_gemm_pair_bf16.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
+                                           c_void_p]
+    lib.ttt_dbg_gemm_pair_bf16.restype = c_int
+    lib.ttt_dbg_ns_pairs.argtypes = [c_int]
+    lib.ttt_dbg_ns_pairs.restype = c_int
+    lib.ttt_dbg_ns_trace.argtypes = [c_int]
+    lib.ttt_dbg_ns_trace.restype = c_int
+    lib.ttt_dbg_ns_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), c_int]
+    lib.ttt_dbg_ns_trace_read.restype = c_int
     lib.ttt_dbg_ns_plan.argtypes = [P, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
     lib.ttt_dbg_ns_plan.restype = c_int
     lib.ttt_dbg_ns_force_grid.argtypes = [c_int]
@@ -222,6 +232,31 @@ def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: in
     """Test hook: D[z] = A[z] B[z]^T on the tcgen05 tile kernel (include/ttt_debug.h)."""
     return _lib.ttt_dbg_gemm_bf16(_ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N,
                                   K, _stream_handle(stream))
+
+
+def ttt_dbg_gemm_pair_bf16(A, B, b_mn_major: bool, D, Z: int, M: int, N: int, K: int, stream=None) -> int:
+    """Test hook: D[z] = A[z] B[z]^T on CTA-pair (cta_group::2) tiles (include/ttt_debug.h)."""
+    return _lib.ttt_dbg_gemm_pair_bf16(_ptr(A), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N, K,
+                                       _stream_handle(stream))
+
+
+def ttt_dbg_ns_pairs(on: bool) -> int:
+    """Test hook: allow CTA-pair tiles in the fused Muon kernel (include/ttt_debug.h)."""
+    return _lib.ttt_dbg_ns_pairs(int(on))
+
+
+def ttt_dbg_ns_trace(on: bool) -> int:
+    """Test hook: record the fused Muon kernel's phase timeline (include/ttt_debug.h)."""
+    return _lib.ttt_dbg_ns_trace(int(on))
+
+
+def ttt_dbg_ns_trace_read(n: int = 96):
+    """Test hook: the last traced launch's timestamps (ns) as a list of n ints."""
+    buf = (ctypes.c_ulonglong * n)()
+    rc = _lib.ttt_dbg_ns_trace_read(buf, n)
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_ns_trace_read")
+    return list(buf)
 
 
 def ttt_dbg_ns_plan(cfg: ttt_cfg):

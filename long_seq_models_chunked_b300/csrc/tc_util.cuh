@@ -121,7 +121,8 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 16-bit tensor map over a row-major array with dims (innermost first) and box.
+// Tensor map over a row-major array with dims (innermost first) and box; the
+// elements are 4 bytes for FLOAT32, else 2.
 inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box,
               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
@@ -129,7 +130,7 @@ inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
   if (!fn || !base) return false;
   cuuint64_t gd[5], gs[4];
   cuuint32_t bx[5], es[5];
-  uint64_t stride = 2;
+  uint64_t stride = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
     bx[i] = box[i];

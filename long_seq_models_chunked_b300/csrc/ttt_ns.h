@@ -13,7 +13,7 @@ struct NsFusedArgs {
   const ttt_cfg* cfg;
   int Z;                 // matrices: 3 per (batch, head)
   bool split;            // SPLIT (bf16 hi/lo operands) or SINGLE (fp16) precision
-  float* X;              // [Z][d][dh] fp32: the chunk gradient on entry; U on exit
+  float* X;              // [Z][d][dh] fp32: the chunk gradient (read only)
   void* Xh[2];           // operand ping-pong buffers (hi)
   void* Xl[2];           //                          (lo; SPLIT only)
   void* Rh; void* Rl;    // R = X X^T + beta I operand (hi, lo), [Z][d][d] each

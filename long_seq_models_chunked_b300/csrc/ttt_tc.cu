@@ -726,9 +726,11 @@ Plan make_plan(const ttt_cfg& g) {
 
 bool tc_supported(const ttt_cfg& g) {
   // d <= 1024: the gradient's clusters hold d / 128 <= 8 CTAs
-  // (the fused Muon step completes the square of its quintic, so it needs c != 0)
+  // (the fused Muon step completes the square of its quintic, so it needs c != 0,
+  // and fuses the update into its last iteration, so it needs at least one)
   return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU && g.loss == TTT_LOSS_IP && g.d % 64 == 0 &&
-         g.dh % 128 == 0 && g.d <= g.dh && g.d <= 1024 && g.dh <= 16384 && (!g.muon || g.ns_c != 0.f);
+         g.dh % 128 == 0 && g.d <= g.dh && g.d <= 1024 && g.dh <= 16384 &&
+         (!g.muon || (g.ns_c != 0.f && g.ns_iters >= 1));
 }
 
 size_t tc_workspace_bytes(const ttt_cfg& g) { return make_plan(g).total; }

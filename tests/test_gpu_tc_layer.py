@@ -29,6 +29,8 @@ CASES = {
                                  lr_a=0.005, seed=45),
     "multi_head_batch": BASE.replace(name="multi_head_batch", B=2, H=3, d=128, dh=256, T=384, seed=46),
     "long_small": BASE.replace(name="long_small", T=2048, chunk=128, seed=48),   # 16 updates
+    # d and dh multiples of 256: Newton-Schulz on CTA-pair (cta_group::2) tiles
+    "pair_d256": BASE.replace(name="pair_d256", B=2, H=2, d=256, dh=512, T=1024, chunk=256, seed=49),
 }
 
 
@@ -39,7 +41,7 @@ def test_tc_matches_oracle(name):
     compare(spec, run_gpu(spec, x, impl=TC), run_oracle(spec, x), TOL)
 
 
-@pytest.mark.parametrize("name", ["small_muon", "small_single", "small_odd_ragged"])
+@pytest.mark.parametrize("name", ["small_muon", "small_single", "small_odd_ragged", "pair_d256"])
 def test_tc_single_precision_short(name):
     spec = CASES[name]
     x = synth.layer_inputs(spec)
