@@ -530,6 +530,12 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
         for (int t = unit; t < n_tiles; t += n_units) {
           if (*abort_flag) break;  // uniform within the warp (read after a barrier or a wait)
           const uint32_t acc = et & 1u;
+          if (kind == PH_XUPD && last) {
+            // while this tile's MMAs run, pull this thread's row of M into L2
+            const int zz = t / per_z, tt = t % per_z;
+            const int mm = (tt / q.nt) * Geo::kRowsPerTile + BM * (int)prank + r;
+            if (mm < d) ptx::prefetch_l2_bulk(p.M + ((size_t)zz * d + mm) * dh + (tt % q.nt) * q.bn, (uint32_t)q.bn * 4u);
+          }
           int ok = 0;
           if (lane == 0) ok = tc_wait(&accf[acc], (et >> 1) & 1u, p.cm, abort_flag) && !*abort_flag;
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -543,6 +549,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
           const int j = z % 3;
           float rs = 0.f;  // last X update, weight norm on, W2: this row's sum of squares over the tile
           float v[32];
+          float4 mA[8], mB[8];  // last X update: M of an even chunk and of the next one, loaded together
           // each 32 x 32 block of the warp goes through its staging buffer and
           // one TMA store per operand half; warp-uniform control flow
           for (int c = 0; c < q.bn; c += 32) {
@@ -573,17 +580,29 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
             } else {
               // the update, fused: M <- M - step*U
               if (row_ok) {
-                const float* mrow = p.M + (size_t)z * d * dh + (size_t)m * dh + n;
-                float4 mv[8];
+                const bool odd = ((c >> 5) & 1) != 0;  // warp-uniform
+                if (!odd) {
+                  const float* mrow = p.M + (size_t)z * d * dh + (size_t)m * dh + n;
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) mv[q4] = ldcg4(mrow + 4 * q4);
+                  for (int q4 = 0; q4 < 8; ++q4) mA[q4] = ldcg4(mrow + 4 * q4);
+                  if (c + 32 < q.bn) {
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                  v[4 * q4 + 0] = mv[q4].x - p.step * v[4 * q4 + 0];
-                  v[4 * q4 + 1] = mv[q4].y - p.step * v[4 * q4 + 1];
-                  v[4 * q4 + 2] = mv[q4].z - p.step * v[4 * q4 + 2];
-                  v[4 * q4 + 3] = mv[q4].w - p.step * v[4 * q4 + 3];
+                    for (int q4 = 0; q4 < 8; ++q4) mB[q4] = ldcg4(mrow + 32 + 4 * q4);
+                  }
                 }
+                auto upd = [&](const float4(&mq)[8]) {
+#pragma unroll
+                  for (int q4 = 0; q4 < 8; ++q4) {
+                    v[4 * q4 + 0] = mq[q4].x - p.step * v[4 * q4 + 0];
+                    v[4 * q4 + 1] = mq[q4].y - p.step * v[4 * q4 + 1];
+                    v[4 * q4 + 2] = mq[q4].z - p.step * v[4 * q4 + 2];
+                    v[4 * q4 + 3] = mq[q4].w - p.step * v[4 * q4 + 3];
+                  }
+                };
+                if (odd)
+                  upd(mB);
+                else
+                  upd(mA);
               } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
