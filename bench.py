@@ -428,9 +428,15 @@ def run_e2e(args, spec, x, holder, dev, stream):
 
 # ------------------------------------------------------------------ the oracle (CPU)
 def oracle_sample(spec, budget_s: float):
-    """Time the fp64 oracle on a bounded sample of the workload: whole chunks of
-    head (0, 0), in order, until the time budget is spent (at least one chunk).
-    Returns (tokens/s scaled to the whole layer, description, threads)."""
+    """Time the fp64 oracle on a bounded sample of the workload and scale it to the
+    layer's tokens/s. The sample walks the heads (b, h) in order. In shifted mode it
+    runs each head's chunks in order, carrying the weights from chunk to chunk. In
+    single-chunk mode it runs contiguous blocks of 32768 tokens of the head's chunk,
+    each an update then an apply from the head's W0 (the same per-token work). It
+    stops once the time budget is spent (after at least one unit) or the workload
+    is exhausted. A layer token (b, t) is H head-tokens of work, so the layer's
+    tokens/s is the sample's head-tokens/s divided by H.
+    Returns (tokens/s, description, seconds spent)."""
     import numpy as np
 
     from long_seq_models_chunked_b300 import synth
@@ -438,39 +444,41 @@ def oracle_sample(spec, budget_s: float):
 
     cfg = OracleCfg.from_spec(spec)
     C = spec.chunk
-    w0 = [w[0].astype(np.float64) for w in synth.initial_weights(spec)]
+    w0 = synth.initial_weights(spec)  # each [H, out, in]
     block = 65536 if C > 65536 else 0
-    # one chunk at a time: for the single-chunk workload a contiguous token
-    # block of the chunk stands in (same per-token work)
-    sample_tokens = min(C, 32768 if spec.mode == "single" else C)
-    done_tokens, t_spent, chunks = 0, 0.0, 0
-    W = tuple(w0)
-    while True:
-        s = chunks * C if spec.mode != "single" else 0
-        e = min(spec.T, s + sample_tokens)
-        ht = synth.head_tokens(spec, 0, 0, s, e)
-        sub = OracleCfg(chunk=e - s, fast_net=cfg.fast_net, loss=cfg.loss, mode=cfg.mode, muon=cfg.muon,
-                        ns_iters=cfg.ns_iters, wnorm=cfg.wnorm, step=cfg.step,
-                        mask=[int(spec.update_mask()[min(chunks, spec.n_chunks - 1)])])
-        t0 = time.perf_counter()
-        _, W = ttt_head(sub, ht["Q64"], ht["K64"], ht["V64"], ht["lr"], W, block=block)
-        t_spent += time.perf_counter() - t0
-        done_tokens += e - s
-        chunks += 1
-        if t_spent >= budget_s or (spec.mode != "single" and chunks >= spec.n_chunks) or spec.mode == "single":
+    single = spec.mode == "single"
+    unit = min(C, 32768) if single else C
+    units_per_head = -(-spec.T // unit) if single else spec.n_chunks
+    mask = spec.update_mask()
+    done, spent, units, heads = 0, 0.0, 0, 0
+    for hi in range(spec.B * spec.H):
+        b, h = divmod(hi, spec.H)
+        heads += 1
+        W = tuple(w[h].astype(np.float64) for w in w0)
+        for u in range(units_per_head):
+            s = u * unit
+            e = min(spec.T, s + unit)
+            ht = synth.head_tokens(spec, b, h, s, e)
+            sub = OracleCfg(chunk=e - s, fast_net=cfg.fast_net, loss=cfg.loss, mode=cfg.mode, muon=cfg.muon,
+                            ns_iters=cfg.ns_iters, wnorm=cfg.wnorm, step=cfg.step,
+                            mask=[int(mask[0 if single else u])])
+            w_in = tuple(w[h].astype(np.float64) for w in w0) if single else W
+            t0 = time.perf_counter()
+            _, w_out = ttt_head(sub, ht["Q64"], ht["K64"], ht["V64"], ht["lr"], w_in, block=block)
+            spent += time.perf_counter() - t0
+            if not single:
+                W = w_out
+            done += e - s
+            units += 1
+            if spent >= budget_s:
+                break
+        if spent >= budget_s:
             break
-    # whole-layer tokens carry B*H heads each; the sample ran on one head
-    heads = spec.B * spec.H
-    if spec.mode == "single":
-        # one update over the whole chunk + one apply: per-token work is uniform
-        value = done_tokens / t_spent / heads
-        desc = (f"head (0,0), {done_tokens} of {spec.T} tokens of the single chunk "
-                f"(update then apply), scaled by 1/{heads} heads")
-    else:
-        value = done_tokens / t_spent / heads
-        desc = (f"head (0,0), first {chunks} of {spec.n_chunks} chunks ({done_tokens} tokens), "
-                f"scaled by 1/{heads} heads")
-    return value, desc, t_spent
+    value = done / spent / spec.H
+    kind = "token blocks of the single chunk (update then apply)" if single else "chunks"
+    desc = (f"{units} {kind}, {done} head-tokens over {heads} head(s) from (0,0) in order; "
+            f"layer tokens/s = head-tokens/s / H ({spec.H})")
+    return value, desc, spent
 
 
 def blas_threads() -> int:
