@@ -53,6 +53,12 @@ TTT_API int ttt_dbg_split_mask(int mask);
  * Returns TTT_OK or TTT_ERR_ARG. */
 TTT_API int ttt_dbg_ns_force_grid(int ctas);
 
+/* Whether the forward tiles run on CTA pairs (tcgen05 cta_group::2: two token
+ * tiles as one M = 256 MMA, each CTA holding half of the weight slice) or on
+ * clusters that share the weight slice by TMA multicast. Default 1. Both give
+ * bitwise equal results. Process-global, for comparisons and tests. Returns TTT_OK. */
+TTT_API int ttt_dbg_fwd_pairs(int on);
+
 /* Whether the fused Muon kernel may run its GEMM phases on CTA pairs
  * (cta_group::2 tiles of 256 rows; taken when d and dh are multiples of 256).
  * Default 1. Process-global, for comparisons and tests. Returns TTT_OK. */

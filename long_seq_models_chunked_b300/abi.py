@@ -40,7 +40,8 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name",
             "ttt_fwd_static_scratch", "ttt_dbg_ns_plan", "ttt_dbg_ns_force_grid",
             "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_gemm_pair_bf16", "ttt_dbg_ns_trace",
-            "ttt_dbg_ns_trace_read", "ttt_dbg_ns_pairs")
+            "ttt_dbg_ns_trace_read", "ttt_dbg_ns_pairs",
+            "ttt_dbg_fwd_pairs")
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
 TTT_KERNEL_NS = 10
@@ -97,6 +98,8 @@ def _load():
     lib.ttt_dbg_gemm_pair_bf16.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
                                            c_void_p]
     lib.ttt_dbg_gemm_pair_bf16.restype = c_int
+    lib.ttt_dbg_fwd_pairs.argtypes = [c_int]
+    lib.ttt_dbg_fwd_pairs.restype = c_int
     lib.ttt_dbg_ns_pairs.argtypes = [c_int]
     lib.ttt_dbg_ns_pairs.restype = c_int
     lib.ttt_dbg_ns_trace.argtypes = [c_int]
@@ -238,6 +241,11 @@ def ttt_dbg_gemm_pair_bf16(A, B, b_mn_major: bool, D, Z: int, M: int, N: int, K:
     """Test hook: D[z] = A[z] B[z]^T on CTA-pair (cta_group::2) tiles (include/ttt_debug.h)."""
     return _lib.ttt_dbg_gemm_pair_bf16(_ptr(A), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N, K,
                                        _stream_handle(stream))
+
+
+def ttt_dbg_fwd_pairs(on: bool) -> int:
+    """Test hook: run the forward tiles on CTA pairs (include/ttt_debug.h)."""
+    return _lib.ttt_dbg_fwd_pairs(int(on))
 
 
 def ttt_dbg_ns_pairs(on: bool) -> int:

@@ -42,6 +42,11 @@ __device__ inline void st_val(void* p, size_t i, int dtype, float v) {
 
 __device__ inline float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// The same through the fast intrinsics (a few ulp of fp32; for the bf16
+// tensor-core epilogues, whose operands round to 2^-9). For x < -88 the
+// exponential overflows to +inf and the quotient is 0, the limit.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
 // Nanosecond clock shared by all SMs (for bounded waits).
 __device__ inline uint64_t globaltimer_ns() {
   uint64_t t;

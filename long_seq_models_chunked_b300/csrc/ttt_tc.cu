@@ -25,6 +25,7 @@
 #include "../../include/ttt_debug.h"
 #include "tc_kernel.cuh"
 #include "tc_mc.cuh"
+#include "tc_pair.cuh"
 #include "tc_util.cuh"
 #include "ttt_internal.h"
 #include "ttt_ns.h"
@@ -35,6 +36,7 @@ namespace {
 using namespace tcu;
 
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
+bool g_fwd_pairs = false;  // test hook: the forward on CTA pairs (measured slower) or multicast clusters
 
 
 // ============================================================ forward, multicast
@@ -50,6 +52,7 @@ struct FwdMcOp {
   struct Params {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
     CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
+    CUtensorMap mWh, mWhl;   // the same, box {32, 64, 1} in the 64-byte swizzle (half a W2 slice; pairs)
     const float* lr;
     bf16* Hq;                // [BH][Cp][dh]
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
@@ -139,7 +142,7 @@ struct FwdMcOp {
         ptx::tmem_ld32(tm + c, va);
         ptx::tmem_ld32(tm + 64 + c, vb);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) va[i] = va[i] * sigmoidf_(va[i]) * vb[i];
+        for (int i = 0; i < 32; ++i) va[i] = va[i] * sigmoid_fast(va[i]) * vb[i];
         if (valid) st_bf16x32(dst + c, va);
       }
     } else {
@@ -160,7 +163,7 @@ struct FwdMcOp {
         for (int i = 0; i < 32; ++i) {
           const float a = va[i], b = vb[i];
           const float g = -eta * vd[i];         // dl/dh = W2^T (-lr v)
-          const float sg = sigmoidf_(a);
+          const float sg = sigmoid_fast(a);
           const float s = a * sg;
           oh[i] = -eta * s * b;                 // -lr * h  (G2 = V^T He)
           va[i] = g * b * sg * (1.f + a * (1.f - sg));
@@ -178,6 +181,78 @@ struct FwdMcOp {
       }
     }
   }
+};
+
+// ============================================================ forward, CTA pairs
+// The same forward on CTA pairs (cta_group::2): the two token tiles of a pair
+// are one M = 256 MMA. Each CTA holds half of the weight slice, so a k-block
+// loads a third less into each SM than in FwdMcOp:
+//   [A|B] (N = 128): the even CTA holds the W1 box (hidden j0..j0+63), the odd
+//                    CTA the W3 box; TMEM columns 0-63 get A, 64-127 get B
+//   Dm (N = 64):     each CTA holds 32 hidden columns of W2 (64-byte-swizzled
+//                    MN-major boxes of 32 x 64); TMEM columns 128-191
+// Work items, tiles and the epilogue are FwdMcOp's with clusters of two.
+__device__ __forceinline__ uint64_t mdesc_half(uint32_t base, int kk) {
+  // MN-major operand of 32 columns in the 64-byte swizzle: rows of 64 B, 8-row
+  // atoms of 512 B; a K step of 16 advances 1024 B
+  return ptx::sdesc_l(base + kk * 1024, 4096, 512, 4);
+}
+
+struct FwdPairOp {
+  using Params = FwdMcOp::Params;
+  using Tile = FwdMcOp::Tile;
+  static constexpr int kStages = 6;
+  static constexpr int kStageBytes = kABytes + 2 * kBox;
+  static constexpr int kAccCols = 256;
+
+  static __device__ int num_work(const Params& p) { return FwdMcOp::num_work(p); }
+  static __device__ void tile_of(const Params& p, int w, int prank, Tile& t) { FwdMcOp::tile_of(p, w, prank, t); }
+  static __device__ int num_kblocks(const Params& p, const Tile& t) { return FwdMcOp::num_kblocks(p, t); }
+  static __device__ bool seg1(const Params& p, const Tile& t, int kb) { return t.is_k && kb >= p.d / BK; }
+  static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int kb) {
+    const uint32_t halves = (t.is_k && p.w_split) ? 2u : 1u;
+    return kABytes + halves * (seg1(p, t, kb) ? kBox / 2 : kBox);
+  }
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint32_t fb, int prank) {
+    const int nk = p.d / BK;
+    const bool s1 = seg1(p, t, kb);
+    const int k = (s1 ? kb - nk : kb) * BK;
+    const CUtensorMap* x = s1 ? &p.mV : (t.is_k ? &p.mK : &p.mQ);
+    ptx::tma_load_3d_pair(st, x, fb, k, p.chunk_start + t.tok * BM, t.bh);
+    const int z = t.bh * 3;
+    const bool lo = t.is_k && p.w_split;
+    if (!s1) {
+      const int zz = z + (prank ? 2 : 0);  // W1 in the even CTA, W3 in the odd one
+      ptx::tma_load_3d_pair(st + kABytes, &p.mW, fb, t.js * 64, k, zz);
+      if (lo) ptx::tma_load_3d_pair(st + kABytes + kBox, &p.mWl, fb, t.js * 64, k, zz);
+    } else {
+      const int c0 = t.js * 64 + 32 * prank;
+      ptx::tma_load_3d_pair(st + kABytes, &p.mWh, fb, c0, k, z + 1);
+      if (lo) ptx::tma_load_3d_pair(st + kABytes + kBox / 2, &p.mWhl, fb, c0, k, z + 1);
+    }
+  }
+  static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
+    const int nk = p.d / BK;
+    const uint32_t a = st, b = st + kABytes;
+    const bool two = t.is_k && p.w_split;
+    if (!seg1(p, t, kb)) {
+      constexpr uint32_t id = ptx::idesc_bf16(256, 128, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        ptx::mma2_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
+        if (two) ptx::mma2_bf16(tmem, kdesc(a, kk), mdesc(b + kBox, kk), id, 1u);
+      }
+    } else {
+      const int k2 = kb - nk;
+      constexpr uint32_t id = ptx::idesc_bf16(256, 64, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        ptx::mma2_bf16(tmem + 128, kdesc(a, kk), mdesc_half(b, kk), id, (k2 | kk) != 0);
+        if (two) ptx::mma2_bf16(tmem + 128, kdesc(a, kk), mdesc_half(b + kBox / 2, kk), id, 1u);
+      }
+    }
+  }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) { FwdMcOp::epilogue(p, t, tm, r); }
 };
 
 // ============================================================ apply-2: O = H_q W2^T
@@ -632,6 +707,64 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
   return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+// Two-CTA clusters of tc_pair_kernel<Op> that fit on the device at once.
+template <class Op>
+int pair_max_clusters() {
+  static int cached = 0, cached_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cached_dev == dev) return cached;
+  auto kern = tc_pair_kernel<Op>;
+  const size_t smem = tc_pair_smem_bytes<Op>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cached = n;
+  cached_dev = dev;
+  return n;
+}
+
+template <class Op>
+int launch_pair(int kind, const typename Op::Params& p, int n_work, cudaStream_t st) {
+  auto kern = tc_pair_kernel<Op>;
+  const size_t smem = tc_pair_smem_bytes<Op>();
+  const int max_pairs = pair_max_clusters<Op>();
+  if (max_pairs <= 0) return TTT_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return TTT_ERR_CUDA;
+  const int n_pairs = std::max(1, std::min(n_work, max_pairs));
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2 * n_pairs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  prof_before(kind, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  prof_after(kind, st);
+  return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 // A side stream (and two events) per device and host thread, created on first
 // use, for the apply that overlaps the gradient. Returns NULL if it cannot be
 // created (the caller then runs everything on its own stream).
@@ -767,7 +900,7 @@ int tc_run(const Call& c) {
   const int n_full = T / P.C;
 
   // ---- tensor maps ([0] = hi or single operand, [1] = lo; lo maps alias hi in SINGLE precision)
-  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mHq, mW2o, mE[2];
+  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mWh[2], mHq, mW2o, mE[2];
   bool ok = true;
   ok &= map3(&mQ, c.Q, d, T, BH, 64, 128);
   ok &= map3(&mK, c.K, d, T, BH, 64, 128);
@@ -795,6 +928,9 @@ int tc_run(const Call& c) {
   }
   ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
   ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
+  ok &= map3(&mWh[0], Ms, dh, d, Z, 32, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= map3(&mWh[1], split_fwd ? Msl : Ms, dh, d, Z, 32, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             CU_TENSOR_MAP_SWIZZLE_64B);
   ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
   ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
   ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
@@ -814,13 +950,14 @@ int tc_run(const Call& c) {
 
   auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
     FwdMcOp::Params p{};
-    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
+    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1]; p.mWh = mWh[0]; p.mWhl = mWh[1];
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
     // pairs of consecutive token tiles share each weight slice: clusters of two
-    // fill all 148 SMs (clusters of four leave 16 idle)
-    p.cs = p.n_tok >= 2 ? 2 : 1;
+    // fill all 148 SMs (clusters of four leave 16 idle); on CTA pairs the two
+    // tiles are one M = 256 MMA (the second may lie past the chunk's tokens)
+    p.cs = (g_fwd_pairs || p.n_tok >= 2) ? 2 : 1;
     p.groups = (p.n_tok + p.cs - 1) / p.cs;
     p.n_js = dh / 64;
     p.BH = BH;
@@ -829,7 +966,9 @@ int tc_run(const Call& c) {
     p.w_split = split_fwd ? 1 : 0;
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
-    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, BH * p.n_js * p.groups * (p.q + p.k), st);
+    const int n_work = BH * p.n_js * p.groups * (p.q + p.k);
+    if (g_fwd_pairs) return launch_pair<FwdPairOp>(TTT_KERNEL_FWD, p, n_work, st);
+    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st);
   };
   auto run_o = [&](int s, int valid, cudaStream_t os) -> int {
     const int mt = (valid + BM - 1) / BM, nt = (d + P.bn_o - 1) / P.bn_o;
@@ -980,4 +1119,9 @@ extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, i
   if (a_mn_major) return go(PlainOp<true, false>{});
   if (b_mn_major) return go(PlainOp<false, true>{});
   return go(PlainOp<false, false>{});
+}
+
+extern "C" int ttt_dbg_fwd_pairs(int on) {
+  ttt::g_fwd_pairs = on != 0;
+  return TTT_OK;
 }

@@ -74,3 +74,20 @@ def test_tc_is_deterministic():
     a = run_gpu(spec, x, impl=TC)
     b = run_gpu(spec, x, impl=TC)
     assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
+
+
+@pytest.mark.parametrize("name", ["small_odd_ragged", "pair_d256", "d192_split_k"])
+def test_forward_on_cta_pairs_equals_multicast_clusters(name):
+    """The forward on CTA pairs (two token tiles as one M = 256 MMA, each CTA
+    holding half of the weight slice) forms every product in the same order as
+    the multicast-cluster forward, so the layer's outputs are bitwise equal."""
+    spec = CASES[name]
+    x = synth.layer_inputs(spec)
+    try:
+        abi.ttt_dbg_fwd_pairs(True)
+        a = run_gpu(spec, x, impl=TC)
+        abi.ttt_dbg_fwd_pairs(False)
+        b = run_gpu(spec, x, impl=TC)
+    finally:
+        abi.ttt_dbg_fwd_pairs(True)
+    assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
