@@ -30,8 +30,14 @@
 //                                  int rank, int cs, uint16_t mask)
 //        issues this CTA's own loads and its multicast slice (mask = every CTA)
 //   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t stage_addr, uint32_t tmem)
-//   static __device__ void epilogue(const Params&, const Tile&, uint32_t tmem_lane_base, int row)
-//        warp-uniform control flow around tcgen05.ld is required
+//   static constexpr uint32_t kEpiBytes   shared memory for the epilogue (a multiple of 4 KB
+//                                         per epilogue warp, or 0)
+//   static __device__ void epilogue(const Params&, const Tile&, uint32_t tmem_lane_base, int row,
+//                                   uint8_t* epi, uint32_t& es)
+//        warp-uniform control flow around tcgen05.ld is required; epi = this warp's
+//        kEpiBytes / 4 of staging, es = a per-warp counter the epilogue may use for
+//        its buffers; TMA stores it issues (lane 0, bulk groups) complete before
+//        the CTA exits
 #pragma once
 
 #include "tc_kernel.cuh"
@@ -40,14 +46,15 @@ namespace ttt {
 
 template <class Op>
 __host__ __device__ constexpr size_t tc_mc_smem_bytes() {
-  return (size_t)Op::kStages * Op::kStageBytes + 1024 + 256;
+  return (size_t)Op::kStages * Op::kStageBytes + Op::kEpiBytes + 1024 + 256;
 }
 
 template <class Op>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_constant__ typename Op::Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)Op::kStages * Op::kStageBytes);
+  uint8_t* epi = smem + (size_t)Op::kStages * Op::kStageBytes;  // epilogue staging (kEpiBytes)
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + Op::kEpiBytes);
   uint64_t* empty = full + Op::kStages;
   uint64_t* accf = empty + Op::kStages;
   uint64_t* acce = accf + 2;
@@ -141,7 +148,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
     }
   } else {
     const int g = warp & 3;
-    uint32_t et = 0;
+    uint32_t et = 0, es = 0;
+    uint8_t* epi_w = epi + (size_t)g * (Op::kEpiBytes / 4);
     for (int w = cluster; w < n_work; w += n_clusters) {
       if (*abort_flag) break;
       typename Op::Tile t;
@@ -152,12 +160,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane);
+      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane, epi_w, es);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acce[acc]);
       ++et;
     }
+    if (Op::kEpiBytes && lane == 0) ptx::bulk_wait_all();  // the epilogue's TMA stores are done
+    __syncwarp();
   }
   ptx::tc_fence_before();
   __syncwarp();

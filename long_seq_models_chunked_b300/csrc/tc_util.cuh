@@ -95,6 +95,53 @@ __device__ __forceinline__ void ld_f32x32(const float* src, float* v) {
   }
 }
 
+// Row `lane` of a 32 x 32 block of 2-byte elements staged for a TMA store in
+// the 64-byte swizzle: 16-byte chunk q of row r at 64 r + 16 (q ^ ((r >> 1) & 3)),
+// so a warp's 16-byte writes are bank-conflict free. 2 KB per block.
+__device__ __forceinline__ uint32_t stage_off64(int lane, int q) { return 64u * lane + 16u * (q ^ ((lane >> 1) & 3)); }
+
+__device__ __forceinline__ float bf_rest(float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); }
+
+// bf16 (hi) at buf; with `lo`, bf16(x - hi) at buf + 2048
+template <bool LO>
+__device__ __forceinline__ void stage_bf16x32(uint8_t* buf, int lane, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 h;
+    h.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    h.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    h.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    h.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(buf + stage_off64(lane, q)) = h;
+    if (LO) {
+      uint4 l;
+      l.x = pack_bf16(bf_rest(v[8 * q + 0]), bf_rest(v[8 * q + 1]));
+      l.y = pack_bf16(bf_rest(v[8 * q + 2]), bf_rest(v[8 * q + 3]));
+      l.z = pack_bf16(bf_rest(v[8 * q + 4]), bf_rest(v[8 * q + 5]));
+      l.w = pack_bf16(bf_rest(v[8 * q + 6]), bf_rest(v[8 * q + 7]));
+      *reinterpret_cast<uint4*>(buf + 2048 + stage_off64(lane, q)) = l;
+    }
+  }
+}
+
+// One operand: a bf16 (hi, lo) pair (SPLIT) or fp16.
+template <bool SPLIT>
+__device__ __forceinline__ void stage_op32(uint8_t* buf, int lane, const float* v) {
+  if (SPLIT) {
+    stage_bf16x32<true>(buf, lane, v);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 h;
+      h.x = pack_f16(v[8 * q + 0], v[8 * q + 1]);
+      h.y = pack_f16(v[8 * q + 2], v[8 * q + 3]);
+      h.z = pack_f16(v[8 * q + 4], v[8 * q + 5]);
+      h.w = pack_f16(v[8 * q + 6], v[8 * q + 7]);
+      *reinterpret_cast<uint4*>(buf + stage_off64(lane, q)) = h;
+    }
+  }
+}
+
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // K-major operand descriptor for K step kk of a 64-deep stage.

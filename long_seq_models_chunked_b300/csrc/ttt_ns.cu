@@ -138,7 +138,6 @@ __device__ __forceinline__ PhaseDesc phase_desc(const NsParams& p, int kind) {
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
-__device__ __forceinline__ float bf_rest(float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); }
 
 // Four consecutive values as operands: bf16 (hi, lo) pairs (SPLIT) or fp16.
 template <bool SPLIT>
@@ -168,38 +167,6 @@ __device__ __forceinline__ float sumsq4(float4 v, float acc) {
 }
 
 constexpr int kStream = 16;  // independent 16-byte loads in flight per thread in the SIMT phases
-
-// Row `lane` of a 32 x 32 block staged for a TMA store: 2-byte elements in the
-// 64-byte swizzle (16-byte chunk q of row r at 64 r + 16 (q ^ ((r >> 1) & 3))),
-// fp32 in the 128-byte swizzle (at 128 r + 16 (q ^ (r & 7))). Conflict-free.
-template <bool SPLIT>
-__device__ __forceinline__ void stage_op32(uint8_t* buf, int lane, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 h;
-    if (SPLIT) {
-      h.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-      h.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-      h.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-      h.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    } else {
-      h.x = pack_f16(v[8 * q + 0], v[8 * q + 1]);
-      h.y = pack_f16(v[8 * q + 2], v[8 * q + 3]);
-      h.z = pack_f16(v[8 * q + 4], v[8 * q + 5]);
-      h.w = pack_f16(v[8 * q + 6], v[8 * q + 7]);
-    }
-    const uint32_t off = 64u * lane + 16u * (q ^ ((lane >> 1) & 3));
-    *reinterpret_cast<uint4*>(buf + off) = h;
-    if (SPLIT) {
-      uint4 l;
-      l.x = pack_bf16(bf_rest(v[8 * q + 0]), bf_rest(v[8 * q + 1]));
-      l.y = pack_bf16(bf_rest(v[8 * q + 2]), bf_rest(v[8 * q + 3]));
-      l.z = pack_bf16(bf_rest(v[8 * q + 4]), bf_rest(v[8 * q + 5]));
-      l.w = pack_bf16(bf_rest(v[8 * q + 6]), bf_rest(v[8 * q + 7]));
-      *reinterpret_cast<uint4*>(buf + 2048 + off) = l;
-    }
-  }
-}
 
 __device__ __forceinline__ void stage_f32x32(uint8_t* buf, int lane, const float* v) {
 #pragma unroll

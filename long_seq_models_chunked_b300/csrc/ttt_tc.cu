@@ -53,6 +53,8 @@ struct FwdMcOp {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
     CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
     CUtensorMap mWh, mWhl;   // the same, box {32, 64, 1} in the 64-byte swizzle (half a W2 slice; pairs)
+    CUtensorMap sHq;         // stores: H_q {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
+    CUtensorMap sE, sEl;     //         E (hi, lo) {dh, Cp, 3BH}, box {32, 32, 1}
     const float* lr;
     bf16* Hq;                // [BH][Cp][dh]
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
@@ -70,6 +72,7 @@ struct FwdMcOp {
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = kABytes + 4 * kBox;
   static constexpr int kAccCols = 256;
+  static constexpr uint32_t kEpiBytes = 4 * 2 * 4096;  // two 4 KB staging buffers per epilogue warp
 
   static __device__ int num_work(const Params& p) { return p.BH * p.n_js * p.groups * (p.q + p.k); }
   static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
@@ -130,7 +133,8 @@ struct FwdMcOp {
       }
     }
   }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
+  // Row-by-row stores from registers (the CTA-pair forward).
+  static __device__ void epilogue_direct(const Params& p, const Tile& t, uint32_t tm, int r) {
     if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
     const int tl = t.tok * BM + r;  // token index inside the chunk
     const bool valid = tl < p.valid;
@@ -178,6 +182,73 @@ struct FwdMcOp {
           st_bf16x32(dH + c, oh);
           st_bf16x32(dB + c, vb);
         }
+      }
+    }
+  }
+
+  // The SwiGLU (backward) epilogue through shared memory: each warp stages its
+  // 32 x 32 blocks (64-byte swizzle) in one of its two buffers and writes them
+  // with TMA stores, hi and lo halves alike. Rows past the chunk's tokens get
+  // lr 0 (zero E rows) and zero H_q rows.
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t* epi,
+                                  uint32_t& es) {
+    if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
+    const int lane = r & 31;
+    const int tl = t.tok * BM + r;        // token index inside the chunk
+    const int row0 = tl - lane;           // this warp's first row (warp-uniform)
+    const bool valid = tl < p.valid;
+    const int j0 = t.js * 64;
+    // stage one 32 x 32 block and store it at (column x, this warp's rows, plane z)
+    auto put = [&](const float* v, bool lo, const CUtensorMap* mh, const CUtensorMap* ml, int x, int z) {
+      uint8_t* buf = epi + (es & 1u) * 4096u;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that used this buffer has read it
+      __syncwarp();
+      if (lo)
+        stage_bf16x32<true>(buf, lane, v);
+      else
+        stage_bf16x32<false>(buf, lane, v);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(mh, buf, x, row0, z);
+        if (lo) ptx::tma_store_3d(ml, buf + 2048, x, row0, z);
+        ptx::bulk_commit();
+      }
+      ++es;
+    };
+    float va[32], vb[32];
+    if (!t.is_k) {
+      for (int c = 0; c < 64; c += 32) {
+        ptx::tmem_ld32(tm + c, va);
+        ptx::tmem_ld32(tm + 64 + c, vb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) va[i] = valid ? va[i] * sigmoid_fast(va[i]) * vb[i] : 0.f;
+        put(va, false, &p.sHq, &p.sHq, j0 + c, t.bh);
+      }
+    } else {
+      // rows past the chunk's tokens get lr 0, so their E rows are zero
+      const float eta = valid ? p.lr[(size_t)t.bh * p.T + p.chunk_start + tl] : 0.f;
+      const bool lo = p.e_split != 0;
+      float vd[32];
+      for (int c = 0; c < 64; c += 32) {
+        ptx::tmem_ld32(tm + c, va);
+        ptx::tmem_ld32(tm + 64 + c, vb);
+        ptx::tmem_ld32(tm + 128 + c, vd);
+        float oh[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a = va[i], b = vb[i];
+          const float g = -eta * vd[i];         // dl/dh = W2^T (-lr v)
+          const float sg = sigmoid_fast(a);
+          const float s = a * sg;
+          oh[i] = -eta * s * b;                 // -lr * h  (G2 = V^T He)
+          va[i] = g * b * sg * (1.f + a * (1.f - sg));
+          vb[i] = g * s;
+        }
+        const int z = t.bh * 3;
+        put(va, lo, &p.sE, &p.sEl, j0 + c, z);
+        put(oh, lo, &p.sE, &p.sEl, j0 + c, z + 1);
+        put(vb, lo, &p.sE, &p.sEl, j0 + c, z + 2);
       }
     }
   }
@@ -252,7 +323,9 @@ struct FwdPairOp {
       }
     }
   }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) { FwdMcOp::epilogue(p, t, tm, r); }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
+    FwdMcOp::epilogue_direct(p, t, tm, r);
+  }
 };
 
 // ============================================================ apply-2: O = H_q W2^T
@@ -334,6 +407,7 @@ struct GradMcOp {
   static constexpr int kStages = 5;
   static constexpr int kStageBytes = kAB + 2 * kEB;
   static constexpr int kAccCols = BN;
+  static constexpr uint32_t kEpiBytes = 0;
 
   static __device__ int num_work(const Params& p) { return p.Z * p.nt * p.splits; }
   static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
@@ -380,7 +454,7 @@ struct GradMcOp {
       if (p.e_split) ptx::mma_bf16(tmem, a, ptx::sdesc(el + kk * 2048, kBoxG, 1024), id, 1u);
     }
   }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&) {
     const int m = t.m0 + r;
     float v[32];
     float* dst = p.splits > 1 ? p.split_out + (size_t)t.split * p.Z * p.d * p.dh : p.G;
@@ -935,6 +1009,11 @@ int tc_run(const Call& c) {
   ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
   ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
   ok &= map3(&mE[1], split_grad ? El : E, dh, P.Cp, Z, 64, 32);
+  CUtensorMap sHq, sE[2];
+  ok &= map3(&sHq, Hq, dh, P.Cp, BH, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= map3(&sE[0], E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= map3(&sE[1], split_grad ? El : E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return TTT_ERR_CUDA;
 
   int rc;
@@ -951,6 +1030,7 @@ int tc_run(const Call& c) {
   auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
     FwdMcOp::Params p{};
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1]; p.mWh = mWh[0]; p.mWhl = mWh[1];
+    p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
