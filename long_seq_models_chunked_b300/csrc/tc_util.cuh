@@ -44,34 +44,6 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void st_f16x32(f16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_f16(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_f16(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_f16(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_f16(v[8 * q + 6], v[8 * q + 7]);
-    d[q] = w;
-  }
-}
-
-// Stores 32 values as one fp16 operand (SINGLE) or as a bf16 hi/lo pair (SPLIT):
-// hi = bf16(v), lo = bf16(v - hi), so hi + lo carries ~16 significant bits.
-template <bool SPLIT>
-__device__ __forceinline__ void st_op32(void* hi, void* lo, size_t o, const float* v) {
-  if (SPLIT) {
-    float l[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
-    st_bf16x32(static_cast<bf16*>(hi) + o, v);
-    st_bf16x32(static_cast<bf16*>(lo) + o, l);
-  } else {
-    st_f16x32(static_cast<f16*>(hi) + o, v);
-  }
-}
-
 __device__ __forceinline__ void st_bf16pair32(bf16* hi, bf16* lo, const float* v) {
   float l[32];
 #pragma unroll
@@ -84,15 +56,6 @@ __device__ __forceinline__ void st_f32x32(float* dst, const float* v) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
   for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
-__device__ __forceinline__ void ld_f32x32(const float* src, float* v) {
-  const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 x = s[q];
-    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-  }
 }
 
 // Row `lane` of a 32 x 32 block of 2-byte elements staged for a TMA store in
@@ -141,8 +104,6 @@ __device__ __forceinline__ void stage_op32(uint8_t* buf, int lane, const float* 
     }
   }
 }
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // K-major operand descriptor for K step kk of a 64-deep stage.
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk) { return ptx::sdesc(base + kk * 32, 16, 1024); }

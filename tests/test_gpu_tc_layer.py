@@ -91,3 +91,20 @@ def test_forward_on_cta_pairs_equals_multicast_clusters(name):
     finally:
         abi.ttt_dbg_fwd_pairs(True)
     assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
+
+
+def test_muon_on_cta_pairs_matches_oracle():
+    """The Muon step's GEMM phases on CTA-pair tiles (cta_group::2, off by
+    default; taken when d and dh are multiples of 256), with the update fused
+    into the last X update: parity with the oracle, on a small case and on the
+    lm workload's shapes."""
+    spec = CASES["pair_d256"]
+    x = synth.layer_inputs(spec)
+    lm = synth.WORKLOADS["lm_chunk2k"].replace(T=4096)
+    try:
+        abi.ttt_dbg_ns_pairs(True)
+        got = run_gpu(spec, x, impl=TC)
+        full_workload_check(lm, [(0, 0), (lm.B - 1, lm.H - 1)], TOL, impl=TC)
+    finally:
+        abi.ttt_dbg_ns_pairs(False)
+    compare(spec, got, run_oracle(spec, x), TOL)
