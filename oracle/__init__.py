@@ -10,6 +10,12 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
                                 per-token sum)
   newton_schulz               - pinned (closed form through the SVD)
   weight_norm                 - pinned (row-norm and direction invariants)
+  update (momentum buffer)    - pinned (geometric-series closed form of the linear
+                                momentum optimiser; the buffer, not the gradient,
+                                feeds Newton-Schulz)
+  chunk_grad (rates [n, 3])   - pinned (brute-force weighted sum of per-token
+                                gradients; equal columns = the shared rate; a zero
+                                column leaves its matrix unchanged)
   ttt_head / ttt_layer        - pinned in the special cases with closed forms
                                 (delta rule, block-shifted linear attention,
                                 single-chunk linear attention, zero update) and by

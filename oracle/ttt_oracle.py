@@ -34,8 +34,13 @@ The readings used here:
 * SwiGLU fast net f(x) = W2 (silu(W1 x) * (W3 x)); linear f(x) = W x;
 * Muon (when on): Newton-Schulz quintic iteration of the public Muon method on
   the wide orientation, X0 = G / (||G||_F + eps), X <- aX + (bA + cA^2)X with
-  A = X X^T, coefficients (a, b, c) given by the caller; no momentum;
-* update W <- W - step * U, U = NS(G) or G;
+  A = X X^T, coefficients (a, b, c) given by the caller;
+* momentum (off by default, mu = 0): a buffer per matrix, M <- mu M + G, carried
+  from update to update and fed to Newton-Schulz (or, with Muon off, used as the
+  step: the plain momentum optimiser the LaCT page compares Muon with, §2.2.1);
+* update W <- W - step * U, U = NS(M) or M (M = G without momentum);
+* per-token learning rates: one per token shared by the matrices ([T]), or one
+  per token and matrix ([T, n_matrices]); G_j = sum_t eta_{t,j} grad_{W_j} l_t;
 * weight norm (when on): each row of each out x in matrix is rescaled to the
   row norm it had in W0:  W[r,:] <- W[r,:] * n0[r] / max(||W[r,:]||, floor);
 * shifted mode: for each chunk, apply with the current W, then (if the chunk's
@@ -155,7 +160,7 @@ class OracleCfg:
                  mode: str = "shifted", muon: bool = True, ns_iters: int = 5,
                  ns_coef: Tuple[float, float, float] = (3.4445, -4.7750, 2.0315),
                  ns_eps: float = 1e-7, wnorm: bool = True, wnorm_floor: float = 1e-12,
-                 step: float = 1.0, mask: Optional[Sequence[int]] = None):
+                 step: float = 1.0, mask: Optional[Sequence[int]] = None, momentum: float = 0.0):
         self.chunk = int(chunk)
         self.fast_net = fast_net
         self.loss = loss
@@ -168,6 +173,7 @@ class OracleCfg:
         self.wnorm_floor = float(wnorm_floor)
         self.step = float(step)
         self.mask = None if mask is None else [int(m) for m in mask]
+        self.momentum = float(momentum)
 
     @classmethod
     def from_spec(cls, spec) -> "OracleCfg":
@@ -183,7 +189,15 @@ def _apply(cfg: OracleCfg, W: Weights, X: np.ndarray) -> np.ndarray:
 
 def chunk_grad(cfg: OracleCfg, W: Weights, K: np.ndarray, V: np.ndarray,
                eta: np.ndarray, block: int = 0) -> Weights:
-    """Chunk gradient: the sum over the chunk's tokens (LaCT page §2.1)."""
+    """Chunk gradient: the sum over the chunk's tokens (LaCT page §2.1).
+
+    eta is [n] (one rate per token for every matrix) or [n, len(W)] (one per
+    token and matrix): matrix j's gradient is then the sum weighted by column j.
+    """
+    eta = np.asarray(eta, dtype=np.float64)
+    if eta.ndim == 2:
+        # the gradient is linear in the token weights: G_j from column j alone
+        return tuple(chunk_grad(cfg, W, K, V, eta[:, j], block)[j] for j in range(len(W)))
     fn = swiglu_grad if cfg.fast_net == "swiglu" else linear_grad
     n = K.shape[0]
     if block <= 0 or block >= n:
@@ -196,11 +210,17 @@ def chunk_grad(cfg: OracleCfg, W: Weights, K: np.ndarray, V: np.ndarray,
     return tuple(total)
 
 
-def update(cfg: OracleCfg, W: Weights, G: Weights, n0: Sequence[np.ndarray]) -> Weights:
-    """One fast-weight update: optional Muon, the step, optional weight norm."""
+def update(cfg: OracleCfg, W: Weights, G: Weights, n0: Sequence[np.ndarray],
+           mom: Optional[List[np.ndarray]] = None) -> Weights:
+    """One fast-weight update: optional momentum, optional Muon, the step,
+    optional weight norm. `mom` (the momentum buffers, one per matrix) is
+    updated in place when given; without it the update has no momentum."""
     a, b, c = cfg.ns_coef
     new = []
-    for Wj, Gj, nj in zip(W, G, n0):
+    for j, (Wj, Gj, nj) in enumerate(zip(W, G, n0)):
+        if mom is not None:
+            mom[j] = cfg.momentum * mom[j] + Gj
+            Gj = mom[j]
         Uj = newton_schulz(Gj, cfg.ns_iters, a, b, c, cfg.ns_eps) if cfg.muon else Gj
         Wj = Wj - cfg.step * Uj
         if cfg.wnorm:
@@ -221,16 +241,18 @@ def ttt_head(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.ndarray,
     W = tuple(np.asarray(w, dtype=np.float64) for w in W0)
     n0 = [row_norms(w) for w in W]
     lr = np.asarray(lr, dtype=np.float64)
+    # momentum buffers start at zero; with mu = 0 the buffer is the gradient itself
+    mom = [np.zeros_like(w) for w in W] if cfg.momentum != 0.0 else None
     O = np.empty((T, W[0].shape[0] if cfg.fast_net == "linear" else W[1].shape[0]))
     for ci in range(n):
         s, e = ci * C, min(T, (ci + 1) * C)
         if cfg.mode == "shifted":
             O[s:e] = _apply_blocks(cfg, W, Q[s:e], block)
             if mask[ci]:
-                W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0)
+                W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0, mom)
         elif cfg.mode == "single":
             if mask[ci]:
-                W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0)
+                W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0, mom)
             O[s:e] = _apply_blocks(cfg, W, Q[s:e], block)
         else:
             raise ValueError(cfg.mode)

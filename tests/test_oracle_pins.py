@@ -378,3 +378,96 @@ def test_toy_scalar_ttt_on_a_noisy_sinusoid():
     assert abs(Wf[0, 0] - w) <= 1e-12
     # the adapted scalar predicts better than the initial w = 0 on the last half
     assert ((O[500:, 0] - V[500:, 0]) ** 2).mean() < (V[500:, 0] ** 2).mean()
+
+
+# ------------------------------------------------------------------ momentum, per-matrix rates
+@pytest.mark.parametrize("mu", [0.5, 0.9])
+def test_linear_ip_momentum_is_a_geometric_sum_of_chunk_gradients(mu):
+    """Linear net, inner-product loss, momentum optimiser (Muon off, no weight
+    norm): a chunk's gradient g_c = -sum_s eta_s v_s k_s^T does not depend on W,
+    the buffer after the i-th update is sum_{k<=i} mu^(i-k) g_(k), so after m
+    updates W = W0 - step * sum_k g_(k) (1 - mu^(m-k+1)) / (1 - mu): a geometric
+    series written out, not the recursion. Skipped chunks leave the buffer as is."""
+    rng = np.random.default_rng(31)
+    d, C, T, step = 5, 4, 23, 0.7
+    mask = [1, 0, 1, 1, 0, 1]
+    W0 = rng.standard_normal((d, d))
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.5, T)
+    cfg = orc.OracleCfg(chunk=C, fast_net="linear", loss="ip", muon=False, wnorm=False,
+                        mask=mask, momentum=mu, step=step)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    n = (T + C - 1) // C
+    g = [-sum(eta[s] * np.outer(V[s], K[s]) for s in range(c * C, min(T, (c + 1) * C))) for c in range(n)]
+    upd = [c for c in range(n) if mask[c]]
+
+    def weights_after(m):  # after the first m updates
+        return W0 - step * sum(g[upd[k]] * (1 - mu ** (m - k)) / (1 - mu) for k in range(m))
+
+    for t in range(T):
+        m = sum(1 for c in upd if c < t // C)
+        assert np.abs(O[t] - weights_after(m) @ Q[t]).max() <= 1e-12
+    assert np.abs(Wf - weights_after(len(upd))).max() <= 1e-12
+
+
+def test_momentum_feeds_newton_schulz():
+    """With Muon on, the buffer (not the gradient) is orthogonalised: when the
+    second chunk's rates are all zero its gradient vanishes, the buffer is
+    mu * (first gradient), and Newton-Schulz of it is that of the first gradient
+    (its normalisation removes the scale, up to eps). Momentum applied after
+    Newton-Schulz would step by mu times that instead."""
+    rng = np.random.default_rng(32)
+    d, dh, C = 4, 8, 6
+    T = 2 * C
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = np.concatenate([rng.uniform(0.1, 0.5, C), np.zeros(C)])
+    cfg = orc.OracleCfg(chunk=C, mode="shifted", muon=True, wnorm=False, momentum=0.6)
+    _, W = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    G = orc.chunk_grad(cfg, W0, K[:C], V[:C], eta[:C])
+    for j in range(3):
+        U = orc.newton_schulz(G[j], 5, *cfg.ns_coef, 1e-7)
+        assert np.abs(W[j] - (W0[j] - 2.0 * U)).max() <= 1e-6 * np.abs(U).max()
+
+
+def test_per_matrix_rates_weight_each_matrix_by_its_own_column():
+    """eta [n, 3]: matrix j's gradient is sum_t eta_(t,j) times token t's own
+    gradient (the gradient with a one-hot weight on t), by brute force."""
+    rng = np.random.default_rng(33)
+    d, dh, C = 4, 8, 5
+    W = _rand_weights("swiglu", d, dh, rng)
+    K, V = rng.standard_normal((C, d)), rng.standard_normal((C, d))
+    eta3 = rng.uniform(0.0, 1.0, (C, 3))
+    cfg = orc.OracleCfg(chunk=C)
+    G = orc.chunk_grad(cfg, W, K, V, eta3)
+    for j in range(3):
+        ref = sum(eta3[t, j] * orc.swiglu_grad(W, K[t:t + 1], V[t:t + 1], np.ones(1), "ip")[j]
+                  for t in range(C))
+        assert np.abs(G[j] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_per_matrix_rates_equal_to_the_shared_rate_give_the_same_layer():
+    rng = np.random.default_rng(34)
+    d, dh, C, T = 4, 8, 5, 17
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0.0, 0.3, T)
+    cfg = orc.OracleCfg(chunk=C, muon=True, wnorm=True)
+    O1, W1 = orc.ttt_head(cfg, Q, K, V, eta, W0)
+    O3, W3 = orc.ttt_head(cfg, Q, K, V, np.stack([eta] * 3, axis=1), W0)
+    assert np.array_equal(O1, O3) and all(np.array_equal(a, b) for a, b in zip(W1, W3))
+
+
+def test_a_zero_rate_leaves_its_matrix_unchanged():
+    """SGD without weight norm: a matrix whose rates are all zero never moves,
+    the others do."""
+    rng = np.random.default_rng(35)
+    d, dh, C, T = 4, 8, 5, 15
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta3 = rng.uniform(0.1, 0.3, (T, 3))
+    eta3[:, 1] = 0.0
+    cfg = orc.OracleCfg(chunk=C, muon=False, wnorm=False)
+    _, W = orc.ttt_head(cfg, Q, K, V, eta3, W0)
+    assert np.array_equal(W[1], W0[1])
+    assert np.abs(W[0] - W0[0]).max() > 1e-3 and np.abs(W[2] - W0[2]).max() > 1e-3
