@@ -88,9 +88,9 @@ enum {
   TTT_KERNEL_FWD = 0,     /* fused [A|B] = X[W1;W3]^T, Dm = V W2, SwiGLU (backward) epilogue */
   TTT_KERNEL_APPLY = 1,   /* O = H_q W2^T                                                   */
   TTT_KERNEL_GRAD = 2,    /* chunk gradients G1^T, G2, G3^T (+ split-K reduction)            */
-  TTT_KERNEL_GRAM = 3,    /* Newton-Schulz S = X X^T                                         */
-  TTT_KERNEL_POLY = 4,    /* Newton-Schulz P = bS + cS^2                                     */
-  TTT_KERNEL_XUPD = 5,    /* Newton-Schulz X <- aX + P X                                     */
+  TTT_KERNEL_GRAM = 3,    /* Newton-Schulz R = X X^T + beta I  \  phases of TTT_KERNEL_NS;   */
+  TTT_KERNEL_POLY = 4,    /* Newton-Schulz P = c R^2 + alpha I  > no launch of their own:    */
+  TTT_KERNEL_XUPD = 5,    /* Newton-Schulz X <- P X            /  classes of the FLOP split   */
   TTT_KERNEL_UPDATE = 6,  /* W <- W - step U, row weight norm, shadows                        */
   TTT_KERNEL_AUX = 7,     /* import/export of the weights, normalisation, finiteness scan     */
   TTT_KERNEL_LINEAR = 8,  /* linear small-chunk persistent kernel                            */
