@@ -68,7 +68,8 @@ enum { TTT_PREC_SPLIT = 0, TTT_PREC_SINGLE = 1 };
 
 /* Layer configuration. Fill it with ttt_cfg_default() and override fields. */
 typedef struct ttt_cfg {
-  int32_t B, H, T;        /* batch, heads, tokens per sequence                  */
+  int32_t B, H, T;        /* batch, heads, tokens per sequence; each >= 1 (an empty
+                             sequence is TTT_ERR_ARG: there is nothing to apply) */
   int32_t d;              /* head dim (input and output width of f)             */
   int32_t dh;             /* SwiGLU hidden width (ignored for the linear net)    */
   int32_t chunk;          /* tokens per chunk; the last chunk may be shorter     */

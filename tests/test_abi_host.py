@@ -53,7 +53,7 @@ def test_workspace_query_and_selection():
     assert abi.ttt_select_impl(tiny) == abi.TTT_IMPL_SIMT
 
 
-@pytest.mark.parametrize("field,value", [("B", 0), ("T", -1), ("d", 0), ("chunk", 0),
+@pytest.mark.parametrize("field,value", [("B", 0), ("T", -1), ("T", 0), ("H", 0), ("d", 0), ("chunk", 0),
                                          ("fast_net", 2), ("loss", 5), ("mode", 3),
                                          ("dtype", 7), ("ns_iters", -1), ("wnorm_eps", 0.0),
                                          ("impl", 9), ("muon", 2)])
@@ -96,6 +96,6 @@ def test_fwd_rejects_before_launch(over, code):
 
 
 def test_strerror_covers_every_code():
-    for code in range(0, -8, -1):
+    for code in range(0, abi.TTT_ERR_SCRATCH_LIMIT - 1, -1):
         assert abi.ttt_strerror(code) != "unknown status"
     assert abi.ttt_strerror(12345) == "unknown status"
