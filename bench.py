@@ -256,11 +256,23 @@ def workload_spec(args):
     return spec
 
 
+def check_library_for_world(features: int, world: int) -> None:
+    """A process that runs beside ranks on other GPUs must load the build
+    without cluster multicast; refuse anything else."""
+    from long_seq_models_chunked_b300.abi import TTT_FEATURE_CLUSTER_MULTICAST
+    if world > 1 and features & TTT_FEATURE_CLUSTER_MULTICAST:
+        raise SystemExit(f"refusing --gpus {world}: the loaded library uses cluster multicast, which is "
+                         "built for processes that use one GPU alone; multi-GPU runs load "
+                         "libttt_b300_local.so (TTT_B300_LIBRARY=local)")
+
+
 def run_ours(args, rank, local, world, pg):
     import numpy as np
     import torch
 
     from long_seq_models_chunked_b300 import abi, accounting, synth
+
+    check_library_for_world(abi.ttt_build_features(), world)
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -300,14 +312,15 @@ def run_ours(args, rank, local, world, pg):
         clk.__exit__(None, None, None)
         raise abi.TTTError(rc, "warm-up")
 
-    # ---- timed region: device time per step, L2 flushed before each step
+    # ---- timed region: device time per step, L2 flushed before each step.
+    # Per-launch timing is off here: the headline is timed clean.
+    abi.ttt_prof_enable(False)
     abi.ttt_prof_reset()
-    abi.ttt_prof_enable(True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    launches0 = abi.ttt_launch_count()
     barrier(pg, dev if world > 1 else None)
     torch.cuda.synchronize(dev)
+    launches0 = abi.ttt_launch_count()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
@@ -315,9 +328,8 @@ def run_ours(args, rank, local, world, pg):
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     clk.__exit__(None, None, None)
-    barrier(pg, dev if world > 1 else None)
     launches = abi.ttt_launch_count() - launches0
-    abi.ttt_prof_enable(False)
+    barrier(pg, dev if world > 1 else None)
     rc = abi.ttt_status(ws, stream)
     if rc != abi.TTT_OK:
         raise abi.TTTError(rc, "timed steps")
@@ -327,7 +339,20 @@ def run_ours(args, rank, local, world, pg):
     tokens = sum_over_ranks(pg, float(spec.B * spec.T), dev if world > 1 else None)
     value = tokens / (ms * 1e-3)
 
-    # ---- per-kernel shares (events recorded around each launch on its stream)
+    # ---- per-kernel shares: a second pass of the same steps with CUDA events
+    # recorded around every launch on its own stream
+    abi.ttt_prof_reset()
+    abi.ttt_prof_enable(True)
+    prof_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        prof_ev[i][0].record(stream)
+        step()
+        prof_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    abi.ttt_prof_enable(False)
+    prof_step_ms = sum(a.elapsed_time(b) for a, b in prof_ev) / len(prof_ev)
     kinds = {}
     for k in range(abi.TTT_KERNEL_COUNT):
         tot_ms, timed, n = abi.ttt_prof_read(k)
@@ -337,7 +362,7 @@ def run_ours(args, rank, local, world, pg):
     peaks, peak_src = load_peaks()
     top_name, (top_k, top_ms, top_timed, top_n) = max(kinds.items(), key=lambda kv: kv[1][1])
     per_launch_ms = top_ms / max(top_timed, 1)
-    launches_per_step = top_n / args.steps
+    launches_per_step = top_timed / args.steps
     if spec.fast_net == "linear":
         bytes_launch = linear_bytes_per_step(spec) / max(launches_per_step, 1)
         achieved = bytes_launch / (per_launch_ms * 1e-3) / 1e9
@@ -355,6 +380,9 @@ def run_ours(args, rank, local, world, pg):
                 "flop_per_launch": fl}
     roof["launch_ms"] = per_launch_ms
     roof["share"] = top_ms / all_ms
+    roof["timing"] = ("CUDA events around every launch on its stream, in a second pass of the same "
+                      f"{args.steps} steps (that pass: {prof_step_ms:.3f} ms/step; the headline steps ran "
+                      "without per-launch events)")
     roof["traffic"] = read_traffic(top_name, spec.name)
     layer_flops = accounting.algorithmic_flops(spec)
     layer_tflops = layer_flops / (ms_local * 1e-3) / 1e12
@@ -493,15 +521,16 @@ def blas_threads() -> int:
 
 
 def run_reference(args, spec):
-    vals, descs = [], []
+    vals, descs, secs = [], [], []
     for _ in range(args.warmup):
         oracle_sample(spec, 0.0)
     for _ in range(args.steps):
-        v, desc, _ = oracle_sample(spec, args.cpu_budget / max(args.steps, 1))
+        v, desc, spent = oracle_sample(spec, args.cpu_budget / max(args.steps, 1))
         vals.append(v)
         descs.append(desc)
+        secs.append(spent)
     value = statistics.median(vals)
-    return value, descs[0]
+    return value, descs[0], statistics.median(secs)
 
 
 # ------------------------------------------------------------------ main
@@ -531,10 +560,13 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
-        value, desc = run_reference(args, spec)
+        value, desc, sample_s = run_reference(args, spec)
         cores = blas_threads()
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": spec.B * spec.T / value * 1e3,
+                "ms_per_step_kind": ("extrapolated: the whole workload's tokens divided by the sampled "
+                                     "tokens/s; each timed step is a bounded sample, not the whole workload"),
+                "sample_seconds_per_step": sample_s,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config, "impl": "reference",
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -543,6 +575,9 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.gpus > 1:
+        # ranks on several GPUs load the build without cluster multicast
+        os.environ["TTT_B300_LIBRARY"] = "local"
     rank, local, world, pg = dist_setup(args.gpus)
     res = run_ours(args, rank, local, world, pg)
     if rank != 0:

@@ -116,7 +116,10 @@ TTT_API int ttt_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
  *   workspace device scratch of >= ttt_workspace_bytes() bytes, 256-byte aligned;
  *             its first 256 bytes hold the device status word
  *   stream    a cudaStream_t (NULL = the legacy default stream)
- * Outputs must not overlap inputs or the workspace.
+ * Outputs must not overlap inputs or the workspace. Every tensor pointer and
+ * the workspace must be device memory (cudaMalloc or a pool on top of it) of
+ * the calling thread's current device: host, managed or another device's
+ * memory is TTT_ERR_ARG, detected before any launch.
  *
  * The work is enqueued on `stream`; the call returns without waiting. Host-
  * detectable errors (TTT_ERR_ARG, _UNSUPPORTED, _WORKSPACE) return before any
@@ -161,14 +164,16 @@ TTT_API int ttt_fwd_host(const ttt_cfg* cfg,
  * scratch in one array of TTT_STATIC_SCRATCH_BYTES that the library holds in
  * device memory, on every GPU that loads the library, until the process exits.
  * Arguments are those of ttt_fwd without the workspace; `status` is an
- * optional DEVICE int (NULL = not wanted) that receives the device-side status
- * word (TTT_OK, TTT_ERR_NONFINITE, ...) once the layer has run on `stream`.
+ * optional DEVICE int (NULL = not wanted, 4-byte aligned, overlapping no
+ * input or output) that receives the device-side status word (TTT_OK,
+ * TTT_ERR_NONFINITE, ...) once the layer has run on `stream`.
  *
  * - The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  *   routine. It runs on the calling thread's current device.
- * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) and caches it; make that first call before any
- *   stream capture.
+ * - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *   which allocates nothing) with the calling thread's device current. The
+ *   first lookup on a device loads the library's device code there; make that
+ *   first call before any stream capture.
  * - A request whose scratch (ttt_workspace_bytes with impl = SIMT) exceeds
  *   TTT_STATIC_SCRATCH_BYTES returns TTT_ERR_SCRATCH_LIMIT before any launch.
  * - Every call uses the same array, which keeps the previous call's contents
@@ -188,6 +193,17 @@ TTT_API int ttt_select_impl(const ttt_cfg* cfg);
 
 /* Static description of a status code. */
 TTT_API const char* ttt_strerror(int status);
+
+/* Build features, as bit flags.
+ * TTT_FEATURE_CLUSTER_MULTICAST: the tensor-core kernels share operand tiles
+ * across the CTAs of a thread-block cluster with TMA multicast loads (and
+ * signal each other's barriers with multicast commits). Every such load reads
+ * this GPU's own memory (ttt_fwd rejects pointers that are not), but this build
+ * is meant for processes that use one GPU alone. The library built without it
+ * (libttt_b300_local.so: clusters of one CTA, no multicast and no CTA pairs
+ * anywhere) is the one a process that runs beside ranks on other GPUs loads. */
+#define TTT_FEATURE_CLUSTER_MULTICAST 1
+TTT_API int ttt_build_features(void);
 
 /* ABI version (incremented on any incompatible change of this header). */
 TTT_API int ttt_abi_version(void);

@@ -53,15 +53,9 @@ TTT_API int ttt_dbg_split_mask(int mask);
  * Returns TTT_OK or TTT_ERR_ARG. */
 TTT_API int ttt_dbg_ns_force_grid(int ctas);
 
-/* Whether the forward tiles run on CTA pairs (tcgen05 cta_group::2: two token
- * tiles as one M = 256 MMA, each CTA holding half of the weight slice) or on
- * clusters that share the weight slice by TMA multicast. Default 1. Both give
- * bitwise equal results. Process-global, for comparisons and tests. Returns TTT_OK. */
-TTT_API int ttt_dbg_fwd_pairs(int on);
-
 /* Whether the fused Muon kernel may run its GEMM phases on CTA pairs
  * (cta_group::2 tiles of 256 rows; taken when d and dh are multiples of 256).
- * Default 1. Process-global, for comparisons and tests. Returns TTT_OK. */
+ * Default 0 (single-CTA tiles). Process-global, for comparisons and tests. Returns TTT_OK. */
 TTT_API int ttt_dbg_ns_pairs(int on);
 
 /* Phase timeline of the fused Muon kernel. With tracing on, every later launch
@@ -79,6 +73,20 @@ TTT_API int ttt_dbg_ns_trace_read(unsigned long long* out, int n);
  * runs out; the kernel records TTT_ERR_TIMEOUT in the status word and returns
  * with nothing in flight. Later launches are unaffected. */
 TTT_API void ttt_dbg_stall_next_linear(void);
+
+/* Failure-detection test: the next launch of the tensor-core forward (the
+ * first kernel of a chunk) issues none of its TMA loads, so its MMA warps' first
+ * wait runs out after cfg->timeout_us; the kernel records TTT_ERR_TIMEOUT and
+ * every CTA returns with nothing in flight. The call's later kernels see the
+ * status word and stop early or run on stale workspace data; the next call
+ * starts from W0 again and is unaffected. */
+TTT_API void ttt_dbg_stall_next_fwd(void);
+
+/* Failure-detection test: in the next launch of the fused Muon kernel the last
+ * CTA does not arrive at the first grid barrier, so every CTA's bounded wait
+ * runs out; TTT_ERR_TIMEOUT is recorded, every CTA skips the remaining work,
+ * frees its TMEM and returns. Later launches are unaffected. */
+TTT_API void ttt_dbg_stall_next_ns_barrier(void);
 
 /* ---- launch accounting and per-kernel timing ------------------------------
  * Every kernel launch of the library is counted by class. With timing on, each

@@ -3,7 +3,9 @@
 Functions keep the C names. Tensor arguments are torch tensors (device memory
 for ttt_fwd, host memory for ttt_fwd_host); only their data pointers cross the
 boundary. Every step of the layer runs in the CUDA library: if
-libttt_b300.so is missing this module fails to import.
+the library is missing this module fails to import. The multicast build
+(libttt_b300.so) is loaded unless TTT_B300_LIBRARY=local selects the build
+without cluster multicast (libttt_b300_local.so).
 """
 from __future__ import annotations
 
@@ -41,7 +43,8 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_fwd_static_scratch", "ttt_dbg_ns_plan", "ttt_dbg_ns_force_grid",
             "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_gemm_pair_bf16", "ttt_dbg_ns_trace",
             "ttt_dbg_ns_trace_read", "ttt_dbg_ns_pairs",
-            "ttt_dbg_fwd_pairs")
+            "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns_barrier", "ttt_build_features")
+TTT_FEATURE_CLUSTER_MULTICAST = 1
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
 TTT_KERNEL_NS = 10
@@ -98,8 +101,8 @@ def _load():
     lib.ttt_dbg_gemm_pair_bf16.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
                                            c_void_p]
     lib.ttt_dbg_gemm_pair_bf16.restype = c_int
-    lib.ttt_dbg_fwd_pairs.argtypes = [c_int]
-    lib.ttt_dbg_fwd_pairs.restype = c_int
+    lib.ttt_build_features.argtypes = []
+    lib.ttt_build_features.restype = c_int
     lib.ttt_dbg_ns_pairs.argtypes = [c_int]
     lib.ttt_dbg_ns_pairs.restype = c_int
     lib.ttt_dbg_ns_trace.argtypes = [c_int]
@@ -114,6 +117,9 @@ def _load():
     lib.ttt_dbg_split_mask.restype = c_int
     lib.ttt_dbg_stall_next_linear.argtypes = []
     lib.ttt_dbg_stall_next_linear.restype = None
+    for name in ("ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns_barrier"):
+        getattr(lib, name).argtypes = []
+        getattr(lib, name).restype = None
     lib.ttt_prof_enable.argtypes = [c_int]
     lib.ttt_prof_enable.restype = None
     lib.ttt_prof_reset.argtypes = []
@@ -243,9 +249,9 @@ def ttt_dbg_gemm_pair_bf16(A, B, b_mn_major: bool, D, Z: int, M: int, N: int, K:
                                        _stream_handle(stream))
 
 
-def ttt_dbg_fwd_pairs(on: bool) -> int:
-    """Test hook: run the forward tiles on CTA pairs (include/ttt_debug.h)."""
-    return _lib.ttt_dbg_fwd_pairs(int(on))
+def ttt_build_features() -> int:
+    """Bit flags of the loaded build (TTT_FEATURE_CLUSTER_MULTICAST)."""
+    return _lib.ttt_build_features()
 
 
 def ttt_dbg_ns_pairs(on: bool) -> int:
@@ -294,6 +300,16 @@ def ttt_dbg_split_mask(mask: int) -> None:
 def ttt_dbg_stall_next_linear() -> None:
     """Test hook: the next linear-kernel launch withholds its loads and times out."""
     _lib.ttt_dbg_stall_next_linear()
+
+
+def ttt_dbg_stall_next_fwd() -> None:
+    """Test hook: the next tensor-core forward launch withholds its loads and times out."""
+    _lib.ttt_dbg_stall_next_fwd()
+
+
+def ttt_dbg_stall_next_ns_barrier() -> None:
+    """Test hook: the next fused Muon launch loses one arrival at its first grid barrier."""
+    _lib.ttt_dbg_stall_next_ns_barrier()
 
 
 def ttt_prof_enable(on: bool) -> None:

@@ -38,6 +38,7 @@ namespace ttt {
 struct TcCommon {
   int* status;
   unsigned long long timeout_ns;
+  int stall;  // failure-detection test: the producer issues no load, so the first wait runs out
 };
 
 constexpr int kTcThreads = 192;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
   const int nkb = Op::num_kblocks(p, tile);
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.cm.stall) {
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % Op::kStages;

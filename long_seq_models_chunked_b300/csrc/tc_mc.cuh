@@ -69,6 +69,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
   const int n_clusters = (int)(gridDim.x / (unsigned)cs);
   const uint16_t mask = (uint16_t)((1u << cs) - 1u);
   const int n_work = Op::num_work(p);
+#if !TTT_HAS_MULTICAST
+  // this build shares nothing across CTAs: only clusters of one CTA are valid
+  if (cs != 1) {
+    if (threadIdx.x == 0) set_status(p.cm.status, TTT_ERR_DEVICE);
+    return;
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Op::kStages; ++s) {
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
 
   uint32_t pc = 0;  // producer: stages filled
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.cm.stall) {
       for (int w = cluster; w < n_work && !*abort_flag; w += n_clusters) {
         typename Op::Tile t;
         Op::tile_of(p, w, rank, t);
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
           }
           ptx::tc_fence_after();
           Op::consume(p, t, kb, ptx::smem_u32(smem + (size_t)s * Op::kStageBytes), tmem + acc * Op::kAccCols);
-          ptx::mma_commit_mc(&empty[s], mask);
+          ptx::mma_commit_shared(&empty[s], mask);
           ++mc;
         }
         if (!ok) break;

@@ -106,27 +106,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// TMA tile load delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (this cluster); each destination's mbarrier at `bar`'s offset
-// receives the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
-                                               int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
-                                               int c2, int c3, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // TMA tile store from this CTA's shared memory (layout of the map's box and
 // swizzle) to global memory, in the current bulk group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
@@ -234,16 +213,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrives on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once
-// every tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -334,15 +303,15 @@ __device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// Arrives on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once the
-// pair MMAs issued so far by this thread are done.
-__device__ __forceinline__ void mma2_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 }  // namespace ptx
 }  // namespace ttt
+
+// The primitives by which the CTAs of a cluster share operands and barrier
+// signals: cluster multicast in builds that run on one GPU alone, plain
+// CTA-local forms (clusters of one CTA) in builds that a process running on
+// several GPUs loads.
+#ifdef TTT_NO_MULTICAST
+#include "tc_ptx_local.cuh"
+#else
+#include "tc_ptx_mc.cuh"
+#endif

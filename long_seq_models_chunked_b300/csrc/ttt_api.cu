@@ -94,6 +94,30 @@ Sizes tensor_sizes(const ttt_cfg& g) {
   return s;
 }
 
+}  // namespace
+
+// Every tensor pointer must be device memory of the calling thread's current
+// device: the tensor-core kernels read it through TMA tensor maps (some of them
+// shared by a cluster through multicast), which must only ever cover this GPU's
+// own memory. Host memory (pinned or not), managed memory and memory of
+// another device are rejected before anything is launched.
+int check_device_ptrs(const void* const* ptrs, int n) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TTT_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    if (!ptrs[i]) continue;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+      cudaGetLastError();  // clear the sticky-free error of the failed query
+      return TTT_ERR_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return TTT_ERR_ARG;
+  }
+  return TTT_OK;
+}
+
+namespace {
+
 __global__ void check_finite_kernel(const void* p, size_t n, int dtype, int* status) {
   bool bad = false;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -211,6 +235,16 @@ int fwd_device(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, 
       if (overlap(outs[i], r)) return TTT_ERR_ARG;
     for (int k = i + 1; k < 4; ++k)
       if (overlap(outs[i], outs[k])) return TTT_ERR_ARG;
+  }
+  {
+    const void* ptrs[12] = {Q, K, V, lr, O, workspace};
+    int n = 6;
+    for (int j = 0; j < s.nw; ++j) {
+      ptrs[n++] = w0[j];
+      ptrs[n++] = wf[j];
+    }
+    v = check_device_ptrs(ptrs, n);
+    if (v != TTT_OK) return v;
   }
   Call c{};
   c.cfg = g;

@@ -53,6 +53,9 @@ int linear_run(const Call& c);
 
 // ---- misc ------------------------------------------------------------------
 int launch_check_finite(const Call& c);
+// TTT_OK when every non-NULL pointer is device memory of the current device,
+// else TTT_ERR_ARG (TTT_ERR_CUDA if the current device cannot be queried).
+int check_device_ptrs(const void* const* ptrs, int n);
 
 // Launch accounting (and optional event timing) around every kernel launch.
 void prof_before(int kind, cudaStream_t st);

@@ -30,6 +30,7 @@
 // Every wait (mbarriers, grid barriers) is bounded (timeout -> status word, no
 // trap); after an abort every thread still passes every barrier and skips the work.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "tc_kernel.cuh"
@@ -73,6 +74,7 @@ struct NsParams {
   float* colpart;   // [Z][d / 32][dh] partial sums of squares of the columns of M1 / M3, one per 32 rows
   unsigned* bar;    // grid-barrier counter (zeroed before the launch)
   int trace;        // test hook: record phase timestamps in g_ns_trace
+  int stall_barrier;  // test hook: the last CTA never arrives at the first grid barrier
   float alpha, beta, c, eps, step, wnorm_eps;
   int Z, d, dh, iters, gs, wnorm;
   TcCommon cm;
@@ -115,6 +117,18 @@ __device__ __forceinline__ uint64_t kdesc64(uint32_t base, int kk) { return ptx:
 __device__ __forceinline__ uint64_t mdesc32(uint32_t base, int kk) {
   return ptx::sdesc_l(base + kk * 2048, kNsMNBox, 1024, 2);
 }
+
+// Commit of the MMAs issued so far to the barrier at `bar`'s offset in the CTAs
+// of `mask`: the CTA's own barrier, or (CTA pairs, single-GPU build only) both
+// CTAs' barriers through a multicast commit.
+template <bool PAIR>
+__device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask);
+template <>
+__device__ __forceinline__ void commit_to<false>(uint64_t* bar, uint16_t) { ptx::mma_commit(bar); }
+#if TTT_HAS_MULTICAST
+template <>
+__device__ __forceinline__ void commit_to<true>(uint64_t* bar, uint16_t mask) { ptx::mma2_commit_mc(bar, mask); }
+#endif
 
 struct PhaseDesc {
   int mt, nt, nk1, bn;
@@ -231,7 +245,8 @@ __device__ __forceinline__ void grid_barrier(const NsParams& p, unsigned& n_bar,
       atomicMax(&g_ns_trace[3 * n_bar + 1], now);
     }
     __threadfence();
-    atomicAdd(p.bar, 1u);
+    // (test hook: withholding one arrival makes every CTA's wait run out)
+    if (!(p.stall_barrier && n_bar == 1 && blockIdx.x == gridDim.x - 1)) atomicAdd(p.bar, 1u);
     if (!*abort_flag) {
       const uint64_t t0 = globaltimer_ns();
       uint32_t it = 0;
@@ -476,17 +491,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
                   }
                 }
               }
-              if (PAIR)
-                ptx::mma2_commit_mc(&empty[s], pair_mask);
-              else
-                ptx::mma_commit(&empty[s]);
+              commit_to<PAIR>(&empty[s], pair_mask);
               ++mc;
             }
             if (!ok) break;
-            if (PAIR)
-              ptx::mma2_commit_mc(&accf[acc], pair_mask);
-            else
-              ptx::mma_commit(&accf[acc]);
+            commit_to<PAIR>(&accf[acc], pair_mask);
             ++at;
           }
         }
@@ -726,10 +735,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
   }
   if (warp == 1 && lane == 0 && *abort_flag && (!PAIR || prank == 0)) {
     // and the MMAs this thread issued must finish before TMEM is freed
-    if (PAIR)
-      ptx::mma2_commit_mc(drainb, (uint16_t)(1u << lead));
-    else
-      ptx::mma_commit(drainb);
+    commit_to<PAIR>(drainb, (uint16_t)(1u << lead));
     tc_drain(drainb, 0, p.cm);
   }
   ptx::tc_fence_before();
@@ -745,6 +751,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
   if (p.trace && threadIdx.x == 0) atomicMax(&g_ns_trace[1], globaltimer_ns());
 }
 
+#if TTT_HAS_MULTICAST
 // ---------------------------------------------------------------- CTA-pair GEMM
 // D[z] = A[z] B[z]^T on 256 x 256 tiles computed by CTA pairs (cta_group::2),
 // with the operand layouts of the Newton-Schulz phases (32-deep k-blocks,
@@ -921,6 +928,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) pair_gemm_kernel(const __grid_c
   if (warp == 1) ptx::tmem_dealloc2(tmem, 2 * kAccCols);
 }
 
+#endif  // TTT_HAS_MULTICAST
+
 // Grid of the launch: every CTA resident at once (one per SM at this
 // shared-memory size), so that the grid barriers cannot wait on a CTA that is
 // not running. Single CTAs: the cooperative-launch occupancy; pairs: twice the
@@ -961,6 +970,7 @@ int grid_size(int* resident) {
 }
 
 int g_forced_grid = 0;  // test hook: 0 = every SM, else this many CTAs
+std::atomic<int> g_stall_next_barrier{0};  // test hook: the next launch's first grid barrier loses an arrival
 bool g_trace = false;   // test hook: record the phase timeline of every launch
 
 template <int BNS, int BNX, bool SPLIT, bool PAIR>
@@ -973,6 +983,7 @@ int launch_ns(NsParams& p, cudaStream_t st) {
   p.gs = std::max(1, std::min(kMaxGroup, G / p.Z));
   if (cudaMemsetAsync(p.bar, 0, sizeof(unsigned), st) != cudaSuccess) return TTT_ERR_CUDA;
   p.trace = g_trace ? 1 : 0;
+  p.stall_barrier = g_stall_next_barrier.exchange(0);
   if (g_trace) {
     unsigned long long init[kTraceSlots];
     for (int i = 0; i < kTraceSlots; ++i) init[i] = (i >= 3 && i % 3 == 0) ? ~0ull : 0ull;
@@ -1006,7 +1017,7 @@ int launch_ns(NsParams& p, cudaStream_t st) {
 bool g_pairs = false;  // test hook: CTA pairs allowed (measured slower on the Muon step's phases)
 
 // CTA pairs whenever every tile is whole: d and dh multiples of 256.
-bool ns_use_pairs(const ttt_cfg& g) { return g_pairs && g.d % 256 == 0 && g.dh % 256 == 0; }
+bool ns_use_pairs(const ttt_cfg& g) { return TTT_HAS_MULTICAST && g_pairs && g.d % 256 == 0 && g.dh % 256 == 0; }
 
 }  // namespace
 
@@ -1063,7 +1074,9 @@ int ns_fused_run(const NsFusedArgs& a, cudaStream_t st) {
   }
   NsParams p = t_params;
   p.cm = a.cm;
+#if TTT_HAS_MULTICAST
   if (pair) return split ? launch_ns<256, 256, true, true>(p, st) : launch_ns<256, 256, false, true>(p, st);
+#endif
 #define TTT_NS_LAUNCH(BS, BX)                                                                      \
   if (bns == BS && bnx == BX)                                                                      \
     return split ? launch_ns<BS, BX, true, false>(p, st) : launch_ns<BS, BX, false, false>(p, st);
@@ -1131,7 +1144,9 @@ int ns_fused_plan(const ttt_cfg& g, int* resident) {
   const bool split = g.precision == TTT_PREC_SPLIT;
   const int bns = (g.d % 256 == 0) ? 256 : 128;
   const int bnx = (g.dh % 256 == 0) ? 256 : 128;
+#if TTT_HAS_MULTICAST
   if (ns_use_pairs(g)) return split ? grid_size<256, 256, true, true>(resident) : grid_size<256, 256, false, true>(resident);
+#endif
 #define TTT_NS_PLAN(BS, BX)                                                                                   \
   if (bns == BS && bnx == BX)                                                                                 \
     return split ? grid_size<BS, BX, true, false>(resident) : grid_size<BS, BX, false, false>(resident);
@@ -1155,6 +1170,10 @@ size_t ns_fused_scratch_floats(const ttt_cfg& g, int Z) {
 extern "C" int ttt_dbg_gemm_pair_bf16(const void* A, const void* B, int b_mn_major, float* D, int Z, int M, int N,
                                       int K, void* stream) {
   using namespace ttt;
+#if !TTT_HAS_MULTICAST
+  (void)A; (void)B; (void)b_mn_major; (void)D; (void)Z; (void)M; (void)N; (void)K; (void)stream;
+  return TTT_ERR_UNSUPPORTED;  // CTA pairs are built only into the single-GPU library
+#else
   if (!A || !B || !D || Z < 1 || M < 256 || N < 256 || K < 32 || M % 256 || N % 256 || K % 32) return TTT_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(D)) & 15u)
     return TTT_ERR_ARG;
@@ -1209,6 +1228,7 @@ extern "C" int ttt_dbg_gemm_pair_bf16(const void* A, const void* B, int b_mn_maj
   cudaFree(status);
   if (rc == TTT_OK && h != 0) rc = h;
   return rc;
+#endif
 }
 
 extern "C" int ttt_dbg_ns_trace(int on) {
@@ -1222,6 +1242,8 @@ extern "C" int ttt_dbg_ns_trace_read(unsigned long long* out, int n) {
              ? TTT_OK
              : TTT_ERR_CUDA;
 }
+
+extern "C" void ttt_dbg_stall_next_ns_barrier(void) { ttt::g_stall_next_barrier.store(1); }
 
 extern "C" int ttt_dbg_ns_pairs(int on) {
   ttt::g_pairs = on != 0;

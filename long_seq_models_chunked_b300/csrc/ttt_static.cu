@@ -9,8 +9,6 @@
 //
 // The array is TTT_STATIC_SCRATCH_BYTES large and lives on every device that
 // loads the library, until the process exits. Every call shares it.
-#include <mutex>
-
 #include "ttt_common.cuh"
 #include "ttt_internal.h"
 
@@ -21,24 +19,15 @@ namespace {
 // kStatusBytes, then the SIMT family's per-head slices.
 static __device__ __align__(256) unsigned char g_static_scratch[TTT_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_addr[kMaxDevices];  // device address of g_static_scratch, per device
-
 // Host code may not pass g_static_scratch to a kernel (on the host that name is
-// only a stand-in for the device array); the device address is looked up once
-// per device, with that device current, and cached.
+// only a stand-in for the device array). Its device address is looked up on
+// every call, with the calling thread's device current: the lookup allocates
+// nothing, and a stale address can never survive a cudaDeviceReset that
+// reloads the module.
 int static_scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TTT_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TTT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return TTT_ERR_CUDA;
-    g_static_addr[dev] = p;
-  }
-  *out = g_static_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return TTT_ERR_CUDA;
+  *out = p;
   return TTT_OK;
 }
 
@@ -96,7 +85,24 @@ extern "C" int ttt_fwd_static_scratch(const ttt_cfg* cfg, const void* Q, const v
       if (overlaps(outs[i], out_bytes[i], outs[k], out_bytes[k])) return TTT_ERR_ARG;
     if (status && overlaps(outs[i], out_bytes[i], status, sizeof(int))) return TTT_ERR_ARG;
   }
+  // the status word is written last: it may not overlap an input either
+  if (status) {
+    for (int k = 0; k < 4; ++k)
+      if (overlaps(status, sizeof(int), in[k], in_bytes[k])) return TTT_ERR_ARG;
+    for (int j = 0; j < nw; ++j)
+      if (overlaps(status, sizeof(int), w0[j], w0_bytes)) return TTT_ERR_ARG;
+  }
 
+  {
+    const void* ptrs[12] = {Q, K, V, lr, O, status};
+    int n = 6;
+    for (int j = 0; j < nw; ++j) {
+      ptrs[n++] = w0[j];
+      ptrs[n++] = wf[j];
+    }
+    const int v = check_device_ptrs(ptrs, n);
+    if (v != TTT_OK) return v;
+  }
   void* scratch = nullptr;
   int rc = static_scratch_address(&scratch);
   if (rc != TTT_OK) return rc;

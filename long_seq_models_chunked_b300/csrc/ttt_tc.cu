@@ -20,12 +20,12 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "../../include/ttt_debug.h"
 #include "tc_kernel.cuh"
 #include "tc_mc.cuh"
-#include "tc_pair.cuh"
 #include "tc_util.cuh"
 #include "ttt_internal.h"
 #include "ttt_ns.h"
@@ -36,7 +36,7 @@ namespace {
 using namespace tcu;
 
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
-bool g_fwd_pairs = false;  // test hook: the forward on CTA pairs (measured slower) or multicast clusters
+std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch withholds its loads
 
 
 // ============================================================ forward, multicast
@@ -52,7 +52,6 @@ struct FwdMcOp {
   struct Params {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
     CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
-    CUtensorMap mWh, mWhl;   // the same, box {32, 64, 1} in the 64-byte swizzle (half a W2 slice; pairs)
     CUtensorMap sHq;         // stores: H_q {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
     CUtensorMap sE, sEl;     //         E (hi, lo) {dh, Cp, 3BH}, box {32, 32, 1}
     const float* lr;
@@ -109,7 +108,7 @@ struct FwdMcOp {
     for (int b = rank; b < nb; b += cs) {
       const bool lo = seg1 ? b == 1 : b >= 2;
       const int zz = seg1 ? z + 1 : z + ((b & 1) ? 2 : 0);
-      ptx::tma_load_3d_mc(st + kABytes + b * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
+      ptx::tma_load_3d_shared(st + kABytes + b * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
     }
   }
   static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
@@ -133,59 +132,6 @@ struct FwdMcOp {
       }
     }
   }
-  // Row-by-row stores from registers (the CTA-pair forward).
-  static __device__ void epilogue_direct(const Params& p, const Tile& t, uint32_t tm, int r) {
-    if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
-    const int tl = t.tok * BM + r;  // token index inside the chunk
-    const bool valid = tl < p.valid;
-    const int j0 = t.js * 64;
-    float va[32], vb[32];
-    if (!t.is_k) {
-      bf16* dst = p.Hq + ((size_t)t.bh * p.Cp + tl) * p.dh + j0;
-      for (int c = 0; c < 64; c += 32) {
-        ptx::tmem_ld32(tm + c, va);
-        ptx::tmem_ld32(tm + 64 + c, vb);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) va[i] = va[i] * sigmoid_fast(va[i]) * vb[i];
-        if (valid) st_bf16x32(dst + c, va);
-      }
-    } else {
-      // rows past the chunk's tokens get lr 0, so their E rows are zero
-      const float eta = valid ? p.lr[(size_t)t.bh * p.T + p.chunk_start + tl] : 0.f;
-      const size_t plane = (size_t)p.Cp * p.dh;
-      const size_t oA = ((size_t)t.bh * 3 * p.Cp + tl) * p.dh + j0;
-      bf16* dA = p.E + oA;
-      bf16* dH = dA + plane;
-      bf16* dB = dA + 2 * plane;
-      float vd[32];
-      for (int c = 0; c < 64; c += 32) {
-        ptx::tmem_ld32(tm + c, va);
-        ptx::tmem_ld32(tm + 64 + c, vb);
-        ptx::tmem_ld32(tm + 128 + c, vd);
-        float oh[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a = va[i], b = vb[i];
-          const float g = -eta * vd[i];         // dl/dh = W2^T (-lr v)
-          const float sg = sigmoid_fast(a);
-          const float s = a * sg;
-          oh[i] = -eta * s * b;                 // -lr * h  (G2 = V^T He)
-          va[i] = g * b * sg * (1.f + a * (1.f - sg));
-          vb[i] = g * s;
-        }
-        if (p.e_split) {
-          st_bf16pair32(dA + c, p.El + oA + c, va);
-          st_bf16pair32(dH + c, p.El + oA + plane + c, oh);
-          st_bf16pair32(dB + c, p.El + oA + 2 * plane + c, vb);
-        } else {
-          st_bf16x32(dA + c, va);
-          st_bf16x32(dH + c, oh);
-          st_bf16x32(dB + c, vb);
-        }
-      }
-    }
-  }
-
   // The SwiGLU (backward) epilogue through shared memory: each warp stages its
   // 32 x 32 blocks (64-byte swizzle) in one of its two buffers and writes them
   // with TMA stores, hi and lo halves alike. Rows past the chunk's tokens get
@@ -254,80 +200,6 @@ struct FwdMcOp {
   }
 };
 
-// ============================================================ forward, CTA pairs
-// The same forward on CTA pairs (cta_group::2): the two token tiles of a pair
-// are one M = 256 MMA. Each CTA holds half of the weight slice, so a k-block
-// loads a third less into each SM than in FwdMcOp:
-//   [A|B] (N = 128): the even CTA holds the W1 box (hidden j0..j0+63), the odd
-//                    CTA the W3 box; TMEM columns 0-63 get A, 64-127 get B
-//   Dm (N = 64):     each CTA holds 32 hidden columns of W2 (64-byte-swizzled
-//                    MN-major boxes of 32 x 64); TMEM columns 128-191
-// Work items, tiles and the epilogue are FwdMcOp's with clusters of two.
-__device__ __forceinline__ uint64_t mdesc_half(uint32_t base, int kk) {
-  // MN-major operand of 32 columns in the 64-byte swizzle: rows of 64 B, 8-row
-  // atoms of 512 B; a K step of 16 advances 1024 B
-  return ptx::sdesc_l(base + kk * 1024, 4096, 512, 4);
-}
-
-struct FwdPairOp {
-  using Params = FwdMcOp::Params;
-  using Tile = FwdMcOp::Tile;
-  static constexpr int kStages = 6;
-  static constexpr int kStageBytes = kABytes + 2 * kBox;
-  static constexpr int kAccCols = 256;
-
-  static __device__ int num_work(const Params& p) { return FwdMcOp::num_work(p); }
-  static __device__ void tile_of(const Params& p, int w, int prank, Tile& t) { FwdMcOp::tile_of(p, w, prank, t); }
-  static __device__ int num_kblocks(const Params& p, const Tile& t) { return FwdMcOp::num_kblocks(p, t); }
-  static __device__ bool seg1(const Params& p, const Tile& t, int kb) { return t.is_k && kb >= p.d / BK; }
-  static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int kb) {
-    const uint32_t halves = (t.is_k && p.w_split) ? 2u : 1u;
-    return kABytes + halves * (seg1(p, t, kb) ? kBox / 2 : kBox);
-  }
-  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint32_t fb, int prank) {
-    const int nk = p.d / BK;
-    const bool s1 = seg1(p, t, kb);
-    const int k = (s1 ? kb - nk : kb) * BK;
-    const CUtensorMap* x = s1 ? &p.mV : (t.is_k ? &p.mK : &p.mQ);
-    ptx::tma_load_3d_pair(st, x, fb, k, p.chunk_start + t.tok * BM, t.bh);
-    const int z = t.bh * 3;
-    const bool lo = t.is_k && p.w_split;
-    if (!s1) {
-      const int zz = z + (prank ? 2 : 0);  // W1 in the even CTA, W3 in the odd one
-      ptx::tma_load_3d_pair(st + kABytes, &p.mW, fb, t.js * 64, k, zz);
-      if (lo) ptx::tma_load_3d_pair(st + kABytes + kBox, &p.mWl, fb, t.js * 64, k, zz);
-    } else {
-      const int c0 = t.js * 64 + 32 * prank;
-      ptx::tma_load_3d_pair(st + kABytes, &p.mWh, fb, c0, k, z + 1);
-      if (lo) ptx::tma_load_3d_pair(st + kABytes + kBox / 2, &p.mWhl, fb, c0, k, z + 1);
-    }
-  }
-  static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
-    const int nk = p.d / BK;
-    const uint32_t a = st, b = st + kABytes;
-    const bool two = t.is_k && p.w_split;
-    if (!seg1(p, t, kb)) {
-      constexpr uint32_t id = ptx::idesc_bf16(256, 128, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        ptx::mma2_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
-        if (two) ptx::mma2_bf16(tmem, kdesc(a, kk), mdesc(b + kBox, kk), id, 1u);
-      }
-    } else {
-      const int k2 = kb - nk;
-      constexpr uint32_t id = ptx::idesc_bf16(256, 64, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        ptx::mma2_bf16(tmem + 128, kdesc(a, kk), mdesc_half(b, kk), id, (k2 | kk) != 0);
-        if (two) ptx::mma2_bf16(tmem + 128, kdesc(a, kk), mdesc_half(b + kBox / 2, kk), id, 1u);
-      }
-    }
-  }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r) {
-    FwdMcOp::epilogue_direct(p, t, tm, r);
-  }
-};
-
 // ============================================================ apply-2: O = H_q W2^T
 template <int BN>
 struct OOp {
@@ -378,10 +250,12 @@ struct OOp {
 };
 
 // ============================================================ chunk gradients, multicast
-// Cluster of cs = ceil(d/128) CTAs per work item (z, n-block, token split):
-// CTA `rank` computes rows [128 rank, +128) of G_z^T (d x dh) over the item's
-// tokens; the E operand (the item's dh columns) is the same for every rank and
-// is multicast, each CTA loading a share of its 64-column boxes.
+// Cluster of cs CTAs per work item (z, n-block, token split, row group): CTA
+// `rank` computes rows [128 (g cs + rank), +128) of G_z^T (d x dh) over the
+// item's tokens; the E operand (the item's dh columns) is the same for every
+// rank and is multicast, each CTA loading a share of its 64-column boxes. With
+// multicast cs = ceil(d/128) and one row group; without it cs = 1 and
+// ceil(d/128) row groups.
 //   z = bh*3 + j:  j=0  G1^T = K^T DA;  j=1  G2 = V^T He;  j=2  G3^T = K^T DB
 // With split E (hi + lo) both halves sit in one stage and every A tile feeds
 // two MMAs.
@@ -394,6 +268,7 @@ struct GradMcOp {
     float* G;              // [Z][d][dh] fp32 (splits == 1)
     float* split_out;      // [splits][Z][d][dh] fp32 (splits > 1)
     int d, dh, Z, chunk_idx, chunk_start, valid, use4d, nt, splits, kb_per_split, e_split;
+    int mg, cs;            // row groups per item and CTAs per cluster (mg * cs = ceil(d / 128))
     TcCommon cm;
   };
   struct Tile {
@@ -409,15 +284,18 @@ struct GradMcOp {
   static constexpr int kAccCols = BN;
   static constexpr uint32_t kEpiBytes = 0;
 
-  static __device__ int num_work(const Params& p) { return p.Z * p.nt * p.splits; }
+  static __device__ int num_work(const Params& p) { return p.Z * p.nt * p.mg * p.splits; }
   static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
-    t.split = w / (p.Z * p.nt);
-    const int r = w % (p.Z * p.nt);
+    const int per_split = p.Z * p.nt * p.mg;
+    t.split = w / per_split;
+    int r = w % per_split;
+    const int g = r % p.mg;
+    r /= p.mg;
     t.z = r / p.nt;
     t.n0 = (r % p.nt) * BN;
     t.bh = t.z / 3;
     t.j = t.z % 3;
-    t.m0 = rank * BM;
+    t.m0 = (g * p.cs + rank) * BM;
     const int total = (p.valid + kTok - 1) / kTok;
     t.kb0 = t.split * p.kb_per_split;
     t.nkb = max(0, min(total, t.kb0 + p.kb_per_split) - t.kb0);
@@ -439,7 +317,7 @@ struct GradMcOp {
     const int boxes = nb * (p.e_split ? 2 : 1);
     for (int b = rank; b < boxes; b += cs) {
       const int half = b / nb, g = b % nb;
-      ptx::tma_load_3d_mc(st + kAB + half * kEB + g * kBoxG, half ? &p.mEl : &p.mE, bar, t.n0 + g * 64, tok,
+      ptx::tma_load_3d_shared(st + kAB + half * kEB + g * kBoxG, half ? &p.mEl : &p.mE, bar, t.n0 + g * 64, tok,
                           t.z, mask);
     }
   }
@@ -781,64 +659,6 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
   return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
-// Two-CTA clusters of tc_pair_kernel<Op> that fit on the device at once.
-template <class Op>
-int pair_max_clusters() {
-  static int cached = 0, cached_dev = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (cached_dev == dev) return cached;
-  auto kern = tc_pair_kernel<Op>;
-  const size_t smem = tc_pair_smem_bytes<Op>();
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return -1;
-  }
-  cached = n;
-  cached_dev = dev;
-  return n;
-}
-
-template <class Op>
-int launch_pair(int kind, const typename Op::Params& p, int n_work, cudaStream_t st) {
-  auto kern = tc_pair_kernel<Op>;
-  const size_t smem = tc_pair_smem_bytes<Op>();
-  const int max_pairs = pair_max_clusters<Op>();
-  if (max_pairs <= 0) return TTT_ERR_CUDA;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return TTT_ERR_CUDA;
-  const int n_pairs = std::max(1, std::min(n_work, max_pairs));
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2 * n_pairs);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  prof_before(kind, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
-  prof_after(kind, st);
-  return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
-}
-
 // A side stream (and two events) per device and host thread, created on first
 // use, for the apply that overlaps the gradient. Returns NULL if it cannot be
 // created (the caller then runs everything on its own stream).
@@ -869,7 +689,8 @@ SideStream* side_stream() {
 struct Plan {
   int BH, Z, d, dh, C, Cp, T, split;
   int bn_o;               // N tile of the apply GEMM (over d)
-  int g_cs, g_bn, g_nt;   // gradient: cluster size (d / 128 row tiles), N tile over dh, N tiles
+  int g_cs, g_mg;         // gradient: cluster size and row groups (g_cs * g_mg = ceil(d / 128) row tiles)
+  int g_bn, g_nt;         //           N tile over dh, N tiles
   int g_splits_max;       // token splits the workspace has room for
   size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_Sh,
       off_Sl, off_Ph, off_Pl, off_split, off_nsq, total;
@@ -892,12 +713,13 @@ Plan make_plan(const ttt_cfg& g) {
   P.C = std::min(g.chunk, g.T);
   P.Cp = (P.C + BM - 1) / BM * BM;
   P.bn_o = pick_bn_d(g.d);
-  P.g_cs = (g.d + BM - 1) / BM;
+  P.g_cs = TTT_HAS_MULTICAST ? (g.d + BM - 1) / BM : 1;
+  P.g_mg = (g.d + BM - 1) / BM / P.g_cs;
   P.g_bn = (g.dh % 256 == 0) ? 256 : 128;
   P.g_nt = g.dh / P.g_bn;
   // token splits when the (z, n-block) items alone leave SMs idle (up to 8)
   const int kbs = (P.C + BK - 1) / BK;
-  P.g_splits_max = std::max(1, std::min({8, kbs / 8, (kNumSmsHint / P.g_cs) / (P.Z * P.g_nt)}));
+  P.g_splits_max = std::max(1, std::min({8, kbs / 8, (kNumSmsHint / P.g_cs) / (P.Z * P.g_nt * P.g_mg)}));
   const size_t wz = (size_t)P.Z * g.d * g.dh;
   const size_t dd = (size_t)P.Z * g.d * g.d;
   const size_t lo = P.split ? 1 : 0;  // the low halves exist only in split precision
@@ -974,7 +796,7 @@ int tc_run(const Call& c) {
   const int n_full = T / P.C;
 
   // ---- tensor maps ([0] = hi or single operand, [1] = lo; lo maps alias hi in SINGLE precision)
-  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mWh[2], mHq, mW2o, mE[2];
+  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mHq, mW2o, mE[2];
   bool ok = true;
   ok &= map3(&mQ, c.Q, d, T, BH, 64, 128);
   ok &= map3(&mK, c.K, d, T, BH, 64, 128);
@@ -1002,9 +824,6 @@ int tc_run(const Call& c) {
   }
   ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
   ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
-  ok &= map3(&mWh[0], Ms, dh, d, Z, 32, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= map3(&mWh[1], split_fwd ? Msl : Ms, dh, d, Z, 32, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-             CU_TENSOR_MAP_SWIZZLE_64B);
   ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
   ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
   ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
@@ -1029,15 +848,15 @@ int tc_run(const Call& c) {
 
   auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
     FwdMcOp::Params p{};
-    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1]; p.mWh = mWh[0]; p.mWhl = mWh[1];
+    p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
-    // pairs of consecutive token tiles share each weight slice: clusters of two
-    // fill all 148 SMs (clusters of four leave 16 idle); on CTA pairs the two
-    // tiles are one M = 256 MMA (the second may lie past the chunk's tokens)
-    p.cs = (g_fwd_pairs || p.n_tok >= 2) ? 2 : 1;
+    // pairs of consecutive token tiles share each weight slice by multicast:
+    // clusters of two fill all 148 SMs (clusters of four leave 16 idle); the
+    // build without multicast runs clusters of one
+    p.cs = (TTT_HAS_MULTICAST && p.n_tok >= 2) ? 2 : 1;
     p.groups = (p.n_tok + p.cs - 1) / p.cs;
     p.n_js = dh / 64;
     p.BH = BH;
@@ -1046,8 +865,8 @@ int tc_run(const Call& c) {
     p.w_split = split_fwd ? 1 : 0;
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
+    p.cm.stall = g_stall_next_fwd.exchange(0);
     const int n_work = BH * p.n_js * p.groups * (p.q + p.k);
-    if (g_fwd_pairs) return launch_pair<FwdPairOp>(TTT_KERNEL_FWD, p, n_work, st);
     return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st);
   };
   auto run_o = [&](int s, int valid, cudaStream_t os) -> int {
@@ -1064,7 +883,7 @@ int tc_run(const Call& c) {
   auto run_grad = [&](int ci, int s, int valid) -> int {
     const bool full = (s + P.C <= T) && ci < n_full;
     const int kbs = (valid + 31) / 32;  // 32-token k-blocks
-    const int items = Z * P.g_nt;
+    const int items = Z * P.g_nt * P.g_mg;
     auto launch = [&](auto op) -> int {
       using Op = decltype(op);
       const int max_cl = mc_max_clusters<Op>(P.g_cs);
@@ -1077,6 +896,7 @@ int tc_run(const Call& c) {
       p.G = G; p.split_out = splitbuf;
       p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
       p.nt = P.g_nt; p.splits = splits; p.kb_per_split = kb_per_split; p.e_split = split_grad ? 1 : 0; p.cm = cm;
+      p.mg = P.g_mg; p.cs = P.g_cs;
       const int r = launch_mc<Op>(TTT_KERNEL_GRAD, p, P.g_cs, items * splits, st);
       if (r != TTT_OK || splits == 1) return r;
       const size_t n = (size_t)Z * d * dh;
@@ -1201,7 +1021,7 @@ extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, i
   return go(PlainOp<false, false>{});
 }
 
-extern "C" int ttt_dbg_fwd_pairs(int on) {
-  ttt::g_fwd_pairs = on != 0;
-  return TTT_OK;
-}
+extern "C" int ttt_build_features(void) { return TTT_HAS_MULTICAST ? TTT_FEATURE_CLUSTER_MULTICAST : 0; }
+
+extern "C" void ttt_dbg_stall_next_fwd(void) { ttt::g_stall_next_fwd.store(1); }
+

@@ -56,7 +56,7 @@ class LayerSpec:
     ns_iters: int = 5
     wnorm: bool = True
     step: float = 1.0
-    update: str = "all"        # "all" | "odd" (0-based odd chunks update)
+    update: str = "all"        # "all" | "odd" (0-based odd chunks update) | "none"
     lr_kind: str = "sigmoid"   # "sigmoid" | "uniform"
     lr_a: float = 0.01         # sigmoid: scale; uniform: low
     lr_b: float = 0.0          # uniform: high
@@ -81,6 +81,8 @@ class LayerSpec:
         if self.update == "odd":
             m[:] = 0
             m[1::2] = 1
+        elif self.update == "none":
+            m[:] = 0
         return m
 
     def replace(self, **kw) -> "LayerSpec":

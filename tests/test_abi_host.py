@@ -99,3 +99,24 @@ def test_strerror_covers_every_code():
     for code in range(0, abi.TTT_ERR_SCRATCH_LIMIT - 1, -1):
         assert abi.ttt_strerror(code) != "unknown status"
     assert abi.ttt_strerror(12345) == "unknown status"
+
+
+def _static_call(c, **over):
+    p = dict(Q=_fake(1), K=_fake(2), V=_fake(3), lr=_fake(4), W1=_fake(5), W2=_fake(6),
+             W3=_fake(7), O=_fake(8), F1=_fake(9), F2=_fake(10), F3=_fake(11), st=_fake(12))
+    p.update(over)
+    return abi.lib().ttt_fwd_static_scratch(ctypes.byref(c), p["Q"], p["K"], p["V"], p["lr"], p["W1"],
+                                            p["W2"], p["W3"], p["O"], p["F1"], p["F2"], p["F3"], p["st"],
+                                            None)
+
+
+@pytest.mark.parametrize("over", [
+    dict(st=_fake(1) + 64),       # status word inside Q
+    dict(st=_fake(4)),            # status word on the learning rates
+    dict(st=_fake(6) + 128),      # status word inside W0_2
+    dict(st=_fake(9) + 4),        # status word inside an output
+    dict(st=_fake(12) + 2),       # misaligned
+])
+def test_static_scratch_rejects_a_bad_status_word_before_launch(over):
+    c = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"], impl=abi.TTT_IMPL_SIMT).cfg
+    assert _static_call(c, **over) == abi.TTT_ERR_ARG

@@ -79,3 +79,29 @@ def test_non_finite_input_is_reported_and_the_next_call_succeeds(impl, spec):
     O, Wf = abi.layer(holder, dev["Q"], dev["K"], dev["V"], dev["lr"], dev["W0"])
     torch.cuda.synchronize()
     assert torch.isfinite(O.float()).all() and all(torch.isfinite(w).all() for w in Wf)
+
+
+@pytest.mark.parametrize("where", ["pinned", "pageable"])
+def test_host_memory_is_rejected_before_any_launch(where):
+    """Every tensor must be device memory of the current device (the kernels
+    read it through TMA tensor maps): host memory passed as Q is TTT_ERR_ARG,
+    returned before anything is launched or written."""
+    import torch
+    spec = synth.LayerSpec("hostptr", B=1, H=2, T=256, d=64, dh=128, chunk=128, seed=76)
+    x = synth.layer_inputs(spec, exact=False)
+    dev = to_device(x, spec)
+    holder = abi.cfg_from_spec(spec, impl=abi.TTT_IMPL_TC)
+    cfg = holder.cfg
+    hq = dev["Q"].cpu()
+    if where == "pinned":
+        hq = hq.pin_memory()
+    O = torch.empty_like(dev["Q"])
+    Wf = [torch.empty((cfg.B, cfg.H) + s, dtype=torch.float32, device="cuda") for s in abi.weight_shapes(cfg)]
+    ws = torch.zeros(abi.ttt_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    n0 = abi.ttt_launch_count()
+    rc = abi.ttt_fwd(cfg, hq, dev["K"], dev["V"], dev["lr"], *dev["W0"], O, *Wf, ws, check=False)
+    assert rc == abi.TTT_ERR_ARG
+    torch.cuda.synchronize()
+    assert abi.ttt_launch_count() == n0
+    assert int(ws[:4].view(torch.int32).item()) == 0

@@ -31,6 +31,11 @@ CASES = {
     "long_small": BASE.replace(name="long_small", T=2048, chunk=128, seed=48),   # 16 updates
     # d and dh multiples of 256: Newton-Schulz on CTA-pair (cta_group::2) tiles
     "pair_d256": BASE.replace(name="pair_d256", B=2, H=2, d=256, dh=512, T=1024, chunk=256, seed=49),
+    # degenerate cases: no chunk updates (O is the plain SwiGLU MLP of W0, Wf = W0),
+    # and every learning rate zero (G = 0: Newton-Schulz of a zero matrix is zero)
+    "no_update": BASE.replace(name="no_update", update="none", T=640, chunk=128, seed=50),
+    "zero_lr": BASE.replace(name="zero_lr", lr_a=0.0, seed=51),
+    "zero_lr_single": BASE.replace(name="zero_lr_single", lr_a=0.0, mode="single", chunk=512, seed=52),
 }
 
 
@@ -68,28 +73,30 @@ def test_tc_full_workload_sampled_heads(wl, heads, block):
     full_workload_check(spec, heads, TOL, block=block)
 
 
+@pytest.mark.parametrize("name", ["no_update", "zero_lr"])
+def test_tc_degenerate_cases_keep_w0(name):
+    """With no update (mask all zero, or every rate zero) the final weights are
+    W0 and the output is the plain SwiGLU MLP f_W0(Q) (LaCT page §2.1 with the
+    update phase removed)."""
+    spec = CASES[name]
+    x = synth.layer_inputs(spec)
+    O, Wf = run_gpu(spec, x, impl=TC)
+    for j, w in enumerate(x["W0"]):
+        for b in range(spec.B):
+            assert np.abs(Wf[j][b] - w).max() <= 1e-6 * np.abs(w).max(), (name, j)
+    W1, W2, W3 = (w.astype(np.float64) for w in x["W0"])
+    for h in range(spec.H):
+        q = x["Q64"][0, h]
+        a, bm = q @ W1[h].T, q @ W3[h].T
+        mlp = (a / (1.0 + np.exp(-a)) * bm) @ W2[h].T
+        assert np.abs(O[0, h] - mlp).max() <= TOL * np.abs(mlp).max(), name
+
+
 def test_tc_is_deterministic():
     spec = CASES["small_odd_ragged"]
     x = synth.layer_inputs(spec)
     a = run_gpu(spec, x, impl=TC)
     b = run_gpu(spec, x, impl=TC)
-    assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
-
-
-@pytest.mark.parametrize("name", ["small_odd_ragged", "pair_d256", "d192_split_k"])
-def test_forward_on_cta_pairs_equals_multicast_clusters(name):
-    """The forward on CTA pairs (two token tiles as one M = 256 MMA, each CTA
-    holding half of the weight slice) forms every product in the same order as
-    the multicast-cluster forward, so the layer's outputs are bitwise equal."""
-    spec = CASES[name]
-    x = synth.layer_inputs(spec)
-    try:
-        abi.ttt_dbg_fwd_pairs(True)
-        a = run_gpu(spec, x, impl=TC)
-        abi.ttt_dbg_fwd_pairs(False)
-        b = run_gpu(spec, x, impl=TC)
-    finally:
-        abi.ttt_dbg_fwd_pairs(True)
     assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
 
 
@@ -108,3 +115,53 @@ def test_muon_on_cta_pairs_matches_oracle():
     finally:
         abi.ttt_dbg_ns_pairs(False)
     compare(spec, got, run_oracle(spec, x), TOL)
+
+
+@pytest.mark.parametrize("hook", ["fwd", "ns_barrier"])
+def test_bounded_wait_reports_timeout_and_the_next_call_succeeds(hook):
+    """Failure detection without a GPU fault: the tensor-core forward withholds
+    its loads (its MMA warp's mbarrier wait runs out), or one CTA of the fused
+    Muon kernel never arrives at a grid barrier (every CTA's wait runs out).
+    The status word says TTT_ERR_TIMEOUT, the context stays usable, and the
+    next call matches the oracle."""
+    import torch
+    from parity import to_device
+    spec = CASES["small_muon"]
+    x = synth.layer_inputs(spec)
+    dev = to_device(x, spec)
+    holder = abi.cfg_from_spec(spec, impl=TC, timeout_us=20000)
+    (abi.ttt_dbg_stall_next_fwd if hook == "fwd" else abi.ttt_dbg_stall_next_ns_barrier)()
+    with pytest.raises(abi.TTTError) as err:
+        abi.layer(holder, dev["Q"], dev["K"], dev["V"], dev["lr"], dev["W0"])
+    assert err.value.code == abi.TTT_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    compare(spec, run_gpu(spec, x, impl=TC), run_oracle(spec, x), TOL)
+
+
+_LOCAL_BUILD_CHECK = """
+import sys
+sys.path.insert(0, {root!r})
+sys.path.insert(0, {tests!r})
+from long_seq_models_chunked_b300 import abi, synth
+from parity import compare, run_gpu, run_oracle
+assert abi.ttt_build_features() & abi.TTT_FEATURE_CLUSTER_MULTICAST == 0
+for spec in [synth.LayerSpec("local_a", B=1, H=2, T=700, d=64, dh=128, chunk=200, update="odd", seed=61),
+             synth.LayerSpec("local_b", B=1, H=2, T=4096, d=192, dh=384, chunk=4096, mode="single",
+                             lr_a=0.005, seed=62)]:
+    x = synth.layer_inputs(spec)
+    print(spec.name, compare(spec, run_gpu(spec, x, impl=abi.TTT_IMPL_TC), run_oracle(spec, x), 2e-2))
+"""
+
+
+def test_build_without_multicast_matches_oracle():
+    """The library a multi-GPU process loads (built without cluster multicast:
+    clusters of one CTA; the gradient's row tiles become separate work items)
+    runs the same tensor-core path and matches the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = _LOCAL_BUILD_CHECK.format(root=root, tests=os.path.join(root, "tests"))
+    env = dict(os.environ, TTT_B300_LIBRARY="local")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
