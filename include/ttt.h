@@ -91,11 +91,20 @@ typedef struct ttt_cfg {
   uint32_t timeout_us;    /* limit of every device-side wait (default 2,000,000)  */
   int32_t impl;           /* TTT_IMPL_*                                           */
   int32_t precision;      /* TTT_PREC_* (tensor-core family only)                 */
+  float   momentum;       /* mu of the momentum buffer B_j of each matrix (LaCT page
+                             §2.2.1 compares Muon with a momentum optimiser):
+                             B_j <- mu B_j + G_j at every update (B_j starts at 0),
+                             then U_j = NS5(B_j) with Muon, or U_j = B_j without.
+                             0 (default) = no buffer, U_j from G_j alone        */
+  int32_t lr_per_matrix;  /* 0: lr is [B, H, T], one rate per token for every matrix;
+                             1: lr is [B, H, T, n_w], one rate per token and matrix
+                             (n_w = 3 for SwiGLU, in the order W1, W2, W3; 1 for
+                             the linear net): G_j = sum_t lr[t, j] grad_Wj l_t   */
 } ttt_cfg;
 
 /* Fills *cfg with the defaults above (B = H = T = d = dh = chunk = 0, SwiGLU,
  * inner-product loss, shifted mode, bf16, Muon with 5 iterations, weight norm
- * on, step 1, AUTO, SPLIT precision). */
+ * on, step 1, AUTO, SPLIT precision, no momentum, one rate per token). */
 TTT_API void ttt_cfg_default(ttt_cfg* cfg);
 
 /* Bytes of device workspace ttt_fwd needs for *cfg (and the path AUTO picks).
@@ -107,7 +116,8 @@ TTT_API int ttt_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
  * All tensor pointers are DEVICE pointers, 16-byte aligned, row-major,
  * contiguous, owned by the caller:
  *   Q, K, V   [B, H, T, d]     fp32 or bf16 (cfg->dtype); read only
- *   lr        [B, H, T]        fp32 per-token learning rate; read only
+ *   lr        [B, H, T]        fp32 per-token learning rate ([B, H, T, n_w] with
+ *                              lr_per_matrix); read only
  *   W0_1..3   SwiGLU: W1 [H, dh, d], W2 [H, d, dh], W3 [H, dh, d] fp32
  *             (each with a leading B when w0_per_batch); linear: W0_1 = W [H, d, d],
  *             W0_2 = W0_3 = NULL; read only

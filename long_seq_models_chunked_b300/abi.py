@@ -60,6 +60,7 @@ class ttt_cfg(ctypes.Structure):
         ("wnorm", c_int32), ("wnorm_eps", c_float), ("step", c_float),
         ("update_mask", c_void_p), ("w0_per_batch", c_int32), ("check_finite", c_int32),
         ("timeout_us", c_uint32), ("impl", c_int32), ("precision", c_int32),
+        ("momentum", c_float), ("lr_per_matrix", c_int32),
     ]
 
 
@@ -366,6 +367,8 @@ def cfg_from_spec(spec, impl: int = TTT_IMPL_AUTO, check_finite: bool = False,
     c.precision = precision
     c.check_finite = int(check_finite)
     c.timeout_us = timeout_us
+    c.momentum = float(getattr(spec, "momentum", 0.0))
+    c.lr_per_matrix = int(bool(getattr(spec, "lr_per_matrix", False)))
     n_chunks = (c.T + c.chunk - 1) // c.chunk
     mask = np.ascontiguousarray(spec.replace(T=c.T).update_mask(), dtype=np.uint8)
     assert mask.size == n_chunks

@@ -10,7 +10,7 @@
 namespace ttt {
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 constexpr int kMaxPipelineChunks = 512;  // per-chunk events of ttt_fwd_host
 
@@ -34,6 +34,8 @@ int validate_cfg(const ttt_cfg* g) {
   if (g->check_finite != 0 && g->check_finite != 1) return TTT_ERR_ARG;
   if (g->impl < TTT_IMPL_AUTO || g->impl > TTT_IMPL_LINEAR) return TTT_ERR_ARG;
   if (g->precision != TTT_PREC_SPLIT && g->precision != TTT_PREC_SINGLE) return TTT_ERR_ARG;
+  if (!std::isfinite(g->momentum)) return TTT_ERR_ARG;
+  if (g->lr_per_matrix != 0 && g->lr_per_matrix != 1) return TTT_ERR_ARG;
   const int64_t tok = (int64_t)g->B * g->H * g->T;
   if (tok * g->d > kMaxElems) return TTT_ERR_ARG;
   const int64_t wd = g->fast_net == TTT_NET_SWIGLU ? (int64_t)g->d * g->dh : (int64_t)g->d * g->d;
@@ -84,8 +86,8 @@ Sizes tensor_sizes(const ttt_cfg& g) {
   Sizes s{};
   const size_t tok = (size_t)g.B * g.H * g.T;
   s.tok_bytes = tok * g.d * elem_bytes(g.dtype);
-  s.lr_bytes = tok * sizeof(float);
   s.nw = g.fast_net == TTT_NET_SWIGLU ? 3 : 1;
+  s.lr_bytes = tok * sizeof(float) * (g.lr_per_matrix ? s.nw : 1);
   const size_t wsz = s.nw == 3 ? (size_t)g.d * g.dh : (size_t)g.d * g.d;
   for (int j = 0; j < s.nw; ++j) {
     s.w0_bytes[j] = (size_t)(g.w0_per_batch ? g.B : 1) * g.H * wsz * sizeof(float);
@@ -173,6 +175,8 @@ void ttt_cfg_default(ttt_cfg* cfg) {
   cfg->timeout_us = 2000000u;
   cfg->impl = TTT_IMPL_AUTO;
   cfg->precision = TTT_PREC_SPLIT;
+  cfg->momentum = 0.f;
+  cfg->lr_per_matrix = 0;
 }
 
 int ttt_abi_version(void) { return kAbiVersion; }

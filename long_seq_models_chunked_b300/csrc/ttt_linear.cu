@@ -344,8 +344,11 @@ constexpr size_t kLinSmem = 1024 + kLinStages * kLinStageBytes + 4 * kTileBytes 
 int g_linear_stall_next = 0;  // test hook: the next launch withholds its loads
 
 bool linear_supported(const ttt_cfg& g) {
+  // (no momentum buffer: the kernel keeps W alone in registers; with one
+  // matrix, per-matrix rates have the per-token layout)
   return g.fast_net == TTT_NET_LINEAR && g.dtype == TTT_DTYPE_BF16 && g.d == kLinD && g.muon == 0 &&
-         g.wnorm == 0 && g.mode == TTT_MODE_SHIFTED && g.chunk % kTile == 0 && g.T % 4 == 0;
+         g.wnorm == 0 && g.momentum == 0.f && g.mode == TTT_MODE_SHIFTED && g.chunk % kTile == 0 &&
+         g.T % 4 == 0;
 }
 
 size_t linear_workspace_bytes(const ttt_cfg&) { return kStatusBytes; }

@@ -62,6 +62,8 @@ struct NsParams {
   CUtensorMap sX[2][2];        // X operand [ping-pong][hi, lo]: {dh, d, Z}
   CUtensorMap sM;              // fp32 M: {dh, d, Z}, box {32, 32}, 128-byte swizzle
   float* X;         // [Z][d][dh] fp32: the gradient (read only)
+  float* mom;       // [Z][d][dh] momentum buffers, or nullptr: B <- mu B + G replaces G
+  float mu;
   void* Xop[2][2];  // operand copies of X [ping-pong][hi, lo]
   void* Rop[2];
   void* Pop[2];
@@ -346,6 +348,19 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
 #pragma unroll
         for (int u = 0; u < kStream; ++u)
           if (b + u * kNsThreads < n4) v[u] = ldcg4(g + 4 * (b + u * kNsThreads));
+        if (p.mom) {
+          // momentum: B <- mu B + G (stored; Newton-Schulz normalises B)
+          float* mb = p.mom + (g - p.X);
+#pragma unroll
+          for (int u = 0; u < kStream; ++u)
+            if (b + u * kNsThreads < n4) {
+              float4* q = reinterpret_cast<float4*>(mb + 4 * (b + u * kNsThreads));
+              const float4 o = __ldcg(q);
+              v[u] = make_float4(fmaf(p.mu, o.x, v[u].x), fmaf(p.mu, o.y, v[u].y), fmaf(p.mu, o.z, v[u].z),
+                                 fmaf(p.mu, o.w, v[u].w));
+              *q = v[u];
+            }
+        }
 #pragma unroll
         for (int u = 0; u < kStream; ++u)
           if (b + u * kNsThreads < n4) ss = sumsq4(v[u], ss);
@@ -367,7 +382,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
         float4 v[kStream];
 #pragma unroll
         for (int u = 0; u < kStream; ++u)
-          if (b + u * kNsThreads < n4) v[u] = ldcg4(p.X + base + 4 * (b + u * kNsThreads));
+          if (b + u * kNsThreads < n4) v[u] = ldcg4((p.mom ? p.mom : p.X) + base + 4 * (b + u * kNsThreads));
 #pragma unroll
         for (int u = 0; u < kStream; ++u)
           if (b + u * kNsThreads < n4) {
@@ -1034,7 +1049,7 @@ namespace {
 // buffers) launch with the same arguments.
 struct NsKey {
   const void* ptrs[16];
-  float coef[6];
+  float coef[7];
   int ints[7];
 };
 
@@ -1042,11 +1057,11 @@ NsKey ns_key(const NsFusedArgs& a) {
   NsKey k;
   std::memset(&k, 0, sizeof(k));
   const void* ps[16] = {a.X, a.Xh[0], a.Xh[1], a.Xl[0], a.Xl[1], a.Rh, a.Rl, a.Ph, a.Pl, a.M, a.Ms, a.Msl,
-                        a.n0, a.scratch, a.cm.status, nullptr};
+                        a.n0, a.scratch, a.cm.status, a.mom};
   for (int i = 0; i < 16; ++i) k.ptrs[i] = ps[i];
   const ttt_cfg& g = *a.cfg;
-  const float cf[6] = {g.ns_a, g.ns_b, g.ns_c, g.ns_eps, g.step, g.wnorm_eps};
-  for (int i = 0; i < 6; ++i) k.coef[i] = cf[i];
+  const float cf[7] = {g.ns_a, g.ns_b, g.ns_c, g.ns_eps, g.step, g.wnorm_eps, a.mu};
+  for (int i = 0; i < 7; ++i) k.coef[i] = cf[i];
   const int in[7] = {a.Z, g.d, g.dh, g.ns_iters, g.wnorm, a.split ? 1 : 0, ns_use_pairs(g) ? 1 : 0};
   for (int i = 0; i < 7; ++i) k.ints[i] = in[i];
   return k;
@@ -1121,6 +1136,8 @@ int ns_build_params(const NsFusedArgs& a, NsParams& p) {
   ok &= map3(&p.sM, a.M, dh, d, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return TTT_ERR_CUDA;
   p.X = a.X;
+  p.mom = a.mom;
+  p.mu = a.mu;
   p.M = a.M;
   p.Ms = static_cast<bf16*>(a.Ms);
   p.Msl = static_cast<bf16*>(a.Msl);

@@ -22,6 +22,8 @@ struct NsFusedArgs {
   void* Ms; void* Msl;   // bf16 shadows (hi, lo or nullptr)
   const float* n0;       // [Z][dh] reference row norms
   float* scratch;        // >= ns_fused_scratch_floats() floats (partial sums, barrier)
+  float* mom;            // [Z][d][dh] momentum buffers (B <- mu B + G), or nullptr
+  float mu;
   TcCommon cm;
 };
 

@@ -19,13 +19,13 @@ constexpr int kThreads = 256;
 constexpr int kTokenBlock = 64;
 
 struct SimtLayout {
-  size_t W[3], G[3], N0[3];
+  size_t W[3], G[3], N0[3], Mom[3];
   size_t A, Bm, Hh, Y;
   size_t X, S, P, Xn;
   size_t total;
 };
 
-__host__ __device__ inline SimtLayout simt_layout(int fast_net, int d, int dh, int tb) {
+__host__ __device__ inline SimtLayout simt_layout(int fast_net, int d, int dh, int tb, bool mom) {
   SimtLayout L{};
   size_t off = 0;
   const int nw = fast_net == TTT_NET_SWIGLU ? 3 : 1;
@@ -39,6 +39,7 @@ __host__ __device__ inline SimtLayout simt_layout(int fast_net, int d, int dh, i
   for (int j = 0; j < nw; ++j) { L.W[j] = off; off += align_up(sz[j], 64); }
   for (int j = 0; j < nw; ++j) { L.G[j] = off; off += align_up(sz[j], 64); }
   for (int j = 0; j < nw; ++j) { L.N0[j] = off; off += align_up(rows[j], 64); }
+  for (int j = 0; j < nw; ++j) { L.Mom[j] = off; off += mom ? align_up(sz[j], 64) : 0; }
   const int hid = nw == 3 ? dh : d;
   L.A = off;  off += align_up((size_t)tb * hid, 64);
   L.Bm = off; off += align_up((size_t)tb * hid, 64);
@@ -57,7 +58,9 @@ __host__ __device__ inline SimtLayout simt_layout(int fast_net, int d, int dh, i
 struct SimtArgs {
   int B, H, T, d, dh, chunk, fast_net, loss, mode, dtype, muon, ns_iters, wnorm;
   int w0_per_batch, has_mask, tb;
+  int lr_stride;   // 1: one rate per token; n_w: one per token and matrix
   float ns_a, ns_b, ns_c, ns_eps, wnorm_eps, step;
+  float momentum;  // 0: no momentum buffer
   const void* Q;
   const void* K;
   const void* V;
@@ -213,7 +216,10 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
   for (int t0 = s; t0 < e; t0 += a.tb) {
     const int nt = min(a.tb, e - t0);
     const size_t base = (head * a.T + t0) * (size_t)d;
-    const float* lr = a.lr + head * a.T + t0;
+    // rate of token t for matrix j (j = 0 when every matrix shares it)
+    const float* lr = a.lr + (head * a.T + t0) * a.lr_stride;
+    const int ls = a.lr_stride;
+    auto eta = [&](int t, int j) { return lr[(size_t)t * ls + (ls > 1 ? j : 0)]; };
     float* Y = ws + L.Y;
     if (a.fast_net == TTT_NET_SWIGLU) {
       const float* W1 = ws + L.W[0];
@@ -238,13 +244,13 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
       for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
         const int t = idx / d, i = idx % d;
         const float v = ld_val(a.V, base + idx, a.dtype);
-        float y;
+        float y;  // dl/df of token t, without its rate
         if (a.loss == TTT_LOSS_MSE) {
           float f = 0.f;
           for (int j = 0; j < dh; ++j) f = fmaf(W2[(size_t)i * dh + j], Hh[(size_t)t * dh + j], f);
-          y = lr[t] * (f - v);
+          y = f - v;
         } else {
-          y = -lr[t] * v;
+          y = -v;
         }
         Y[idx] = y;
       }
@@ -255,8 +261,8 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
         for (int i = 0; i < d; ++i) g = fmaf(Y[(size_t)t * d + i], W2[(size_t)i * dh + j], g);
         const float xa = A[idx], xb = Bm[idx];
         const float sg = sigmoidf_(xa);
-        A[idx] = g * xb * sg * (1.f + xa * (1.f - sg));   // dl/da
-        Bm[idx] = g * xa * sg;                             // dl/db
+        A[idx] = eta(t, 0) * g * xb * sg * (1.f + xa * (1.f - sg));   // lr1 * dl/da
+        Bm[idx] = eta(t, 2) * g * xa * sg;                             // lr3 * dl/db
       }
       __syncthreads();
       float* G1 = ws + L.G[0];
@@ -265,7 +271,7 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
       for (int idx = threadIdx.x; idx < d * dh; idx += blockDim.x) {
         const int i = idx / dh, j = idx % dh;
         float acc = 0.f;
-        for (int t = 0; t < nt; ++t) acc = fmaf(Y[(size_t)t * d + i], Hh[(size_t)t * dh + j], acc);
+        for (int t = 0; t < nt; ++t) acc = fmaf(eta(t, 1) * Y[(size_t)t * d + i], Hh[(size_t)t * dh + j], acc);
         G2[idx] += acc;
       }
       for (int idx = threadIdx.x; idx < dh * d; idx += blockDim.x) {
@@ -290,9 +296,9 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
           float f = 0.f;
           for (int k = 0; k < d; ++k)
             f = fmaf(W[(size_t)i * d + k], ld_val(a.K, base + (size_t)t * d + k, a.dtype), f);
-          y = lr[t] * (f - v);
+          y = eta(t, 0) * (f - v);
         } else {
-          y = -lr[t] * v;
+          y = -eta(t, 0) * v;
         }
         Y[idx] = y;
       }
@@ -311,6 +317,16 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
   for (int j = 0; j < nw; ++j) {
     float* G = ws + L.G[j];
     float* W = ws + L.W[j];
+    if (a.momentum != 0.f) {
+      // B <- mu B + G; B is what Newton-Schulz (or the plain step) receives
+      float* Mo = ws + L.Mom[j];
+      for (int idx = threadIdx.x; idx < rows[j] * cols[j]; idx += blockDim.x) {
+        const float b = fmaf(a.momentum, Mo[idx], G[idx]);
+        Mo[idx] = b;
+        G[idx] = b;
+      }
+      __syncthreads();
+    }
     if (a.muon) newton_schulz(a, G, rows[j], cols[j], ws, L, red);
     for (int idx = threadIdx.x; idx < rows[j] * cols[j]; idx += blockDim.x) W[idx] -= a.step * G[idx];
     __syncthreads();
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) simt_layer_kernel(const __grid_const
   __shared__ float red[kThreads];
   const size_t head = blockIdx.x;
   const int b = (int)(head / a.H), h = (int)(head % a.H);
-  const SimtLayout L = simt_layout(a.fast_net, a.d, a.dh, a.tb);
+  const SimtLayout L = simt_layout(a.fast_net, a.d, a.dh, a.tb, a.momentum != 0.f);
   float* ws = a.scratch + head * a.head_floats;
   const int nw = a.fast_net == TTT_NET_SWIGLU ? 3 : 1;
   const int rows[3] = {nw == 3 ? a.dh : a.d, a.d, a.dh};
@@ -337,6 +353,9 @@ __global__ void __launch_bounds__(kThreads) simt_layer_kernel(const __grid_const
   }
   __syncthreads();
   for (int j = 0; j < nw; ++j) row_norms(ws + L.W[j], rows[j], cols[j], ws + L.N0[j]);
+  if (a.momentum != 0.f)
+    for (int j = 0; j < nw; ++j)
+      for (size_t idx = threadIdx.x; idx < (size_t)rows[j] * cols[j]; idx += blockDim.x) ws[L.Mom[j] + idx] = 0.f;
   __syncthreads();
   (void)b;
   const int n_chunks = (a.T + a.chunk - 1) / a.chunk;
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kThreads) simt_layer_kernel(const __grid_const
 
 size_t simt_workspace_bytes(const ttt_cfg& cfg) {
   const int tb = cfg.chunk < kTokenBlock ? cfg.chunk : kTokenBlock;
-  const SimtLayout L = simt_layout(cfg.fast_net, cfg.d, cfg.dh, tb);
+  const SimtLayout L = simt_layout(cfg.fast_net, cfg.d, cfg.dh, tb, cfg.momentum != 0.f);
   return kStatusBytes + (size_t)cfg.B * cfg.H * L.total * sizeof(float);
 }
 
@@ -375,12 +394,14 @@ int simt_run(const Call& c) {
   a.tb = g.chunk < kTokenBlock ? g.chunk : kTokenBlock;
   a.ns_a = g.ns_a; a.ns_b = g.ns_b; a.ns_c = g.ns_c; a.ns_eps = g.ns_eps;
   a.wnorm_eps = g.wnorm_eps; a.step = g.step;
+  a.momentum = g.momentum;
+  a.lr_stride = g.lr_per_matrix ? (g.fast_net == TTT_NET_SWIGLU ? 3 : 1) : 1;
   a.Q = c.Q; a.K = c.K; a.V = c.V; a.lr = c.lr;
   for (int j = 0; j < 3; ++j) { a.W0[j] = c.W0[j]; a.Wf[j] = c.Wf[j]; }
   a.O = c.O;
   a.status = reinterpret_cast<int*>(c.ws);
   a.scratch = reinterpret_cast<float*>(c.ws + kStatusBytes);
-  a.head_floats = simt_layout(g.fast_net, g.d, g.dh, a.tb).total;
+  a.head_floats = simt_layout(g.fast_net, g.d, g.dh, a.tb, g.momentum != 0.f).total;
   a.has_mask = c.mask_all ? 0 : 1;
   if (a.has_mask)
     for (int i = 0; i < c.n_chunks; ++i)

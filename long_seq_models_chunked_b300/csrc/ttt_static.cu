@@ -59,7 +59,7 @@ extern "C" int ttt_fwd_static_scratch(const ttt_cfg* cfg, const void* Q, const v
   const int nw = g.fast_net == TTT_NET_SWIGLU ? 3 : 1;
   const size_t es = g.dtype == TTT_DTYPE_F32 ? 4 : 2;
   const size_t tok = (size_t)g.B * g.H * g.T;
-  const size_t tok_bytes = tok * g.d * es, lr_bytes = tok * sizeof(float);
+  const size_t tok_bytes = tok * g.d * es, lr_bytes = tok * sizeof(float) * (g.lr_per_matrix ? nw : 1);
   const size_t wsz = nw == 3 ? (size_t)g.d * g.dh : (size_t)g.d * g.d;
   const size_t w0_bytes = (size_t)(g.w0_per_batch ? g.B : 1) * g.H * wsz * sizeof(float);
   const size_t wf_bytes = (size_t)g.B * g.H * wsz * sizeof(float);

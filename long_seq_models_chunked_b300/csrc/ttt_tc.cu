@@ -62,6 +62,7 @@ struct FwdMcOp {
     int n_tok, groups, n_js, BH, cs;
     int q, k;                // which kinds of tiles this launch computes
     int w_split, e_split;
+    int lr_stride;           // 1: one rate per token; 3: one per token and matrix (W1, W2, W3)
     TcCommon cm;
   };
   struct Tile {
@@ -172,8 +173,15 @@ struct FwdMcOp {
         put(va, false, &p.sHq, &p.sHq, j0 + c, t.bh);
       }
     } else {
-      // rows past the chunk's tokens get lr 0, so their E rows are zero
-      const float eta = valid ? p.lr[(size_t)t.bh * p.T + p.chunk_start + tl] : 0.f;
+      // rows past the chunk's tokens get lr 0, so their E rows are zero; the
+      // rates of W1, W2, W3 (one shared rate, or one per matrix)
+      float e1 = 0.f, e2 = 0.f, e3 = 0.f;
+      if (valid) {
+        const float* lp = p.lr + ((size_t)t.bh * p.T + p.chunk_start + tl) * p.lr_stride;
+        e1 = lp[0];
+        e2 = p.lr_stride > 1 ? lp[1] : e1;
+        e3 = p.lr_stride > 1 ? lp[2] : e1;
+      }
       const bool lo = p.e_split != 0;
       float vd[32];
       for (int c = 0; c < 64; c += 32) {
@@ -184,12 +192,13 @@ struct FwdMcOp {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float a = va[i], b = vb[i];
-          const float g = -eta * vd[i];         // dl/dh = W2^T (-lr v)
+          const float g1 = -e1 * vd[i];         // lr1 * dl/dh, dl/dh = W2^T (-v)
+          const float g3 = -e3 * vd[i];         // lr3 * dl/dh
           const float sg = sigmoid_fast(a);
           const float s = a * sg;
-          oh[i] = -eta * s * b;                 // -lr * h  (G2 = V^T He)
-          va[i] = g * b * sg * (1.f + a * (1.f - sg));
-          vb[i] = g * s;
+          oh[i] = -e2 * s * b;                  // -lr2 * h  (G2 = V^T He)
+          va[i] = g1 * b * sg * (1.f + a * (1.f - sg));
+          vb[i] = g3 * s;
         }
         const int z = t.bh * 3;
         put(va, lo, &p.sE, &p.sEl, j0 + c, z);
@@ -508,8 +517,10 @@ __global__ void norms_kernel(const float* M, float* n0, int d, int dh) {
 
 // M <- M - step*U; optional weight norm back to n0 (LaCT page §2.2.1, eq. 8; the
 // rows of W1/W3 are the columns of M1/M3); refresh the bf16 shadow(s).
-__global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, const float* n0, float step,
-                              int wnorm, float floor_, int d, int dh) {
+// With a momentum buffer (mom != NULL) the step is B = mu*B + U, and B is
+// stored back.
+__global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, float* mom, float mu,
+                              const float* n0, float step, int wnorm, float floor_, int d, int dh) {
   __shared__ float red[8][33];
   const int z = blockIdx.y, j = z % 3;
   const size_t base = (size_t)z * d * dh;
@@ -517,6 +528,9 @@ __global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, con
   bf16* ms = Ms + base;
   bf16* ml = Msl ? Msl + base : nullptr;
   const float* u = U + base;
+  float* mb = mom ? mom + base : nullptr;
+  // the step of element o: the gradient, or the advanced momentum buffer
+  auto stp = [&](size_t o) { return mb ? fmaf(mu, mb[o], u[o]) : u[o]; };
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (j == 1) {
     if (blockIdx.x * 8 >= d) return;
@@ -524,15 +538,18 @@ __global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, con
     if (r >= d) return;  // warp-uniform
     float s = 0.f;
     for (int c = lane; c < dh; c += 32) {
-      const float x = m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c];
+      const float x = m[(size_t)r * dh + c] - step * stp((size_t)r * dh + c);
       s = fmaf(x, x, s);
     }
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const float sc = wnorm ? n0[(size_t)z * dh + r] / fmaxf(sqrtf(s), floor_) : 1.f;
     for (int c = lane; c < dh; c += 32) {
-      const float x = (m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c]) * sc;
-      m[(size_t)r * dh + c] = x;
-      st_shadow(ms, ml, (size_t)r * dh + c, x);
+      const size_t o = (size_t)r * dh + c;
+      const float b = stp(o);
+      const float x = (m[o] - step * b) * sc;
+      m[o] = x;
+      if (mb) mb[o] = b;
+      st_shadow(ms, ml, o, x);
     }
   } else {
     if (blockIdx.x * 32 >= dh) return;
@@ -540,7 +557,7 @@ __global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, con
     float s = 0.f;
     if (c < dh)
       for (int r = w; r < d; r += 8) {
-        const float x = m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c];
+        const float x = m[(size_t)r * dh + c] - step * stp((size_t)r * dh + c);
         s = fmaf(x, x, s);
       }
     red[w][lane] = s;
@@ -550,9 +567,12 @@ __global__ void update_kernel(float* M, bf16* Ms, bf16* Msl, const float* U, con
     const float sc = (wnorm && c < dh) ? n0[(size_t)z * dh + c] / fmaxf(sqrtf(t), floor_) : 1.f;
     if (c < dh)
       for (int r = w; r < d; r += 8) {
-        const float x = (m[(size_t)r * dh + c] - step * u[(size_t)r * dh + c]) * sc;
-        m[(size_t)r * dh + c] = x;
-        st_shadow(ms, ml, (size_t)r * dh + c, x);
+        const size_t o = (size_t)r * dh + c;
+        const float b = stp(o);
+        const float x = (m[o] - step * b) * sc;
+        m[o] = x;
+        if (mb) mb[o] = b;
+        st_shadow(ms, ml, o, x);
       }
   }
 }
@@ -692,6 +712,7 @@ struct Plan {
   int g_cs, g_mg;         // gradient: cluster size and row groups (g_cs * g_mg = ceil(d / 128) row tiles)
   int g_bn, g_nt;         //           N tile over dh, N tiles
   int g_splits_max;       // token splits the workspace has room for
+  size_t off_mom;         // momentum buffers [Z][d][dh] fp32 (momentum != 0 only)
   size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_Sh,
       off_Sl, off_Ph, off_Pl, off_split, off_nsq, total;
 };
@@ -747,6 +768,7 @@ Plan make_plan(const ttt_cfg& g) {
   P.off_Pl = take(lo * dd * 2);
   P.off_split = take(P.g_splits_max > 1 ? (size_t)P.g_splits_max * wz * 4 : 0);
   P.off_nsq = take(ns_fused_scratch_floats(g, P.Z) * 4);
+  P.off_mom = take(g.momentum != 0.f ? wz * 4 : 0);
   P.total = off;
   return P;
 }
@@ -790,6 +812,7 @@ int tc_run(const Call& c) {
   void* Ph = ws + P.off_Ph;
   void* Pl = at(P.off_Pl, split);
   float* splitbuf = reinterpret_cast<float*>(ws + P.off_split);
+  float* mom = g.momentum != 0.f ? reinterpret_cast<float*>(ws + P.off_mom) : nullptr;
   int* status = reinterpret_cast<int*>(ws);
   const TcCommon cm{status, (unsigned long long)c.cfg.timeout_us * 1000ull};
   const int d = g.d, dh = g.dh, BH = P.BH, Z = P.Z, T = g.T;
@@ -836,7 +859,8 @@ int tc_run(const Call& c) {
   if (!ok) return TTT_ERR_CUDA;
 
   int rc;
-  // ---- import W0, reference row norms
+  // ---- import W0, reference row norms; momentum buffers start at zero
+  if (mom && cudaMemsetAsync(mom, 0, (size_t)Z * d * dh * sizeof(float), st) != cudaSuccess) return TTT_ERR_CUDA;
   {
     const dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
     TTT_LAUNCH(TTT_KERNEL_AUX, st,
@@ -851,6 +875,7 @@ int tc_run(const Call& c) {
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
     p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
+    p.lr_stride = g.lr_per_matrix ? 3 : 1;
     p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
     // pairs of consecutive token tiles share each weight slice by multicast:
@@ -908,7 +933,8 @@ int tc_run(const Call& c) {
   auto run_update = [&]() -> int {
     const dim3 grid(std::max((dh + 31) / 32, (d + 7) / 8), Z);
     TTT_LAUNCH(TTT_KERNEL_UPDATE, st,
-               update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, G, n0, g.step, g.wnorm, g.wnorm_eps, d, dh));
+               update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, G, mom, g.momentum, n0, g.step, g.wnorm,
+                                                   g.wnorm_eps, d, dh));
     return TTT_OK;
   };
   NsFusedArgs nsa{};
@@ -917,6 +943,8 @@ int tc_run(const Call& c) {
   nsa.Rh = Sh; nsa.Rl = Sl; nsa.Ph = Ph; nsa.Pl = Pl;
   nsa.M = M; nsa.Ms = Ms; nsa.Msl = Msl; nsa.n0 = n0;
   nsa.scratch = reinterpret_cast<float*>(ws + P.off_nsq);
+  nsa.mom = mom;
+  nsa.mu = g.momentum;
   nsa.cm = cm;
   // update: gradient, then Muon + update + weight norm in one launch (or, without
   // Muon, the plain update + weight norm)

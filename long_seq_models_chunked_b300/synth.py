@@ -14,7 +14,8 @@ workload table below states):
   or fp32 and then bf16 (round to nearest even on the fp32 bit pattern).
   Everyone downstream (oracle and kernels) consumes the ROUNDED values.
 * Per-token learning rates: ``uniform(lo, hi)`` or ``scale * sigmoid(N(0, 1))``,
-  computed in fp64 and rounded to fp32.
+  computed in fp64 and rounded to fp32; with per-matrix rates, one such column
+  per matrix (column 0 is the shared rate's stream).
 * Initial fast weights (one set per head, shared by every batch row):
   W1, W3 ~ N(0, 1/d), W2 ~ N(0, 1/dh); linear W ~ N(0, 1/d); stored fp32.
 * Streams: numpy PCG64 seeded by ``SeedSequence(entropy=ENTROPY,
@@ -35,6 +36,7 @@ TOKEN_BLOCK = 4096
 # tensor ids inside the spawn key
 _T_Q, _T_K, _T_V, _T_LR = 0, 1, 2, 3
 _T_W = 10  # + matrix index
+_T_LR_COL = 20  # + matrix index (per-matrix rates, columns 1 and 2)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -61,6 +63,8 @@ class LayerSpec:
     lr_a: float = 0.01         # sigmoid: scale; uniform: low
     lr_b: float = 0.0          # uniform: high
     seed: int = 0
+    momentum: float = 0.0      # mu of the per-matrix momentum buffer (0 = none)
+    lr_per_matrix: bool = False  # lr [T, n_weights]: one rate per token and matrix
 
     @property
     def n_chunks(self) -> int:
@@ -162,11 +166,12 @@ def _token_draw(spec: LayerSpec, tensor: int, b: int, h: int, t0: int, t1: int,
     return out
 
 
-def _lr_draw(spec: LayerSpec, b: int, h: int, t0: int, t1: int) -> np.ndarray:
+def _lr_draw(spec: LayerSpec, b: int, h: int, t0: int, t1: int, column: int = 0) -> np.ndarray:
+    """Rates of tokens [t0, t1); column j > 0 (per-matrix rates) has its own stream."""
     out = np.empty(t1 - t0, dtype=np.float64)
     blk0, blk1 = t0 // TOKEN_BLOCK, (t1 - 1) // TOKEN_BLOCK
     for blk in range(blk0, blk1 + 1):
-        g = _rng(spec.seed, _T_LR, b, h, blk)
+        g = _rng(spec.seed, _T_LR if column == 0 else _T_LR_COL + column, b, h, blk)
         if spec.lr_kind == "uniform":
             z = g.uniform(spec.lr_a, spec.lr_b, TOKEN_BLOCK)
         else:
@@ -194,7 +199,11 @@ def head_tokens(spec: LayerSpec, b: int, h: int, t0: int = 0,
     out = {}
     for name, x in (("Q", q), ("K", k), ("V", v)):
         out[name], out[name + "64"] = to_storage(x, spec.dtype)
-    out["lr"] = round_fp32(_lr_draw(spec, b, h, t0, t1))
+    if spec.lr_per_matrix:
+        out["lr"] = round_fp32(np.stack([_lr_draw(spec, b, h, t0, t1, j) for j in range(spec.n_weights)],
+                                        axis=1))
+    else:
+        out["lr"] = round_fp32(_lr_draw(spec, b, h, t0, t1))
     return out
 
 
@@ -222,7 +231,8 @@ def layer_inputs(spec: LayerSpec, exact: bool = True) -> Dict[str, object]:
     if exact:
         for n in ("Q64", "K64", "V64"):
             res[n] = np.empty(shp, dtype=np.float64)
-    res["lr"] = np.empty((spec.B, spec.H, spec.T), dtype=np.float32)
+    res["lr"] = np.empty((spec.B, spec.H, spec.T) + ((spec.n_weights,) if spec.lr_per_matrix else ()),
+                         dtype=np.float32)
     for b in range(spec.B):
         for h in range(spec.H):
             ht = head_tokens(spec, b, h)

@@ -180,7 +180,8 @@ class OracleCfg:
         """Build from a workload description with LayerSpec-style attributes."""
         return cls(chunk=spec.chunk, fast_net=spec.fast_net, loss=spec.loss,
                    mode=spec.mode, muon=spec.muon, ns_iters=spec.ns_iters,
-                   wnorm=spec.wnorm, step=spec.step, mask=list(spec.update_mask()))
+                   wnorm=spec.wnorm, step=spec.step, mask=list(spec.update_mask()),
+                   momentum=getattr(spec, "momentum", 0.0))
 
 
 def _apply(cfg: OracleCfg, W: Weights, X: np.ndarray) -> np.ndarray:

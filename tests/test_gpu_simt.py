@@ -26,6 +26,14 @@ CASES = {
     "linear_ip_muon": synth.WORKLOADS["linear_chunk64"].replace(
         name="linear_ip_muon", B=1, H=2, T=256, d=32, dh=32, loss="ip", muon=True,
         wnorm=True, dtype="fp32", seed=37),
+    # LaCT page §2.2.1: Muon against a momentum optimiser; per-matrix rates
+    "momentum_muon": TINY.replace(name="momentum_muon", muon=True, momentum=0.9, seed=39),
+    "momentum_sgd": TINY.replace(name="momentum_sgd", momentum=0.8, seed=40),
+    "lr_per_matrix": TINY.replace(name="lr_per_matrix", muon=True, lr_per_matrix=True, seed=41),
+    "momentum_lr_mse_odd": TINY.replace(name="momentum_lr_mse_odd", loss="mse", momentum=0.5,
+                                        lr_per_matrix=True, T=230, chunk=48, update="odd", seed=42),
+    "linear_momentum": synth.WORKLOADS["linear_chunk64"].replace(
+        name="linear_momentum", B=1, H=2, T=512, dtype="fp32", momentum=0.9, lr_per_matrix=True, seed=43),
 }
 
 

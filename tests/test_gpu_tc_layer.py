@@ -36,6 +36,13 @@ CASES = {
     "no_update": BASE.replace(name="no_update", update="none", T=640, chunk=128, seed=50),
     "zero_lr": BASE.replace(name="zero_lr", lr_a=0.0, seed=51),
     "zero_lr_single": BASE.replace(name="zero_lr_single", lr_a=0.0, mode="single", chunk=512, seed=52),
+    # LaCT page §2.2.1: a momentum buffer before Newton-Schulz (or as the step
+    # without Muon), and one rate per token and matrix
+    "momentum_muon": BASE.replace(name="momentum_muon", momentum=0.9, seed=53),
+    "momentum_sgd": BASE.replace(name="momentum_sgd", muon=False, momentum=0.8, seed=54),
+    "lr_per_matrix": BASE.replace(name="lr_per_matrix", lr_per_matrix=True, seed=55),
+    "momentum_lr_odd_ragged": BASE.replace(name="momentum_lr_odd_ragged", T=700, chunk=200, update="odd",
+                                           momentum=0.5, lr_per_matrix=True, seed=56),
 }
 
 
@@ -53,11 +60,12 @@ def test_tc_single_precision_short(name):
     compare(spec, run_gpu(spec, x, impl=TC, precision=SINGLE), run_oracle(spec, x), TOL)
 
 
-@pytest.mark.parametrize("wl,T", [("lm_chunk2k", 4096), ("video_ar", 2 * 5616)])
-def test_tc_workload_shapes_short(wl, T):
+@pytest.mark.parametrize("wl,T,extra", [("lm_chunk2k", 4096, {}), ("video_ar", 2 * 5616, {}),
+                                        ("lm_chunk2k", 6144, {"momentum": 0.9, "lr_per_matrix": True})])
+def test_tc_workload_shapes_short(wl, T, extra):
     """The workloads' own d, dh, chunk and head counts over their first chunks;
     the oracle checks the first and the last (b, h) head."""
-    spec = synth.WORKLOADS[wl].replace(T=T)
+    spec = synth.WORKLOADS[wl].replace(T=T, **extra)
     full_workload_check(spec, [(0, 0), (spec.B - 1, spec.H - 1)], TOL, impl=TC)
 
 
