@@ -46,7 +46,15 @@ The readings used here:
 * shifted mode: for each chunk, apply with the current W, then (if the chunk's
   update flag is set) update; "single" mode: for each chunk, update first,
   then apply (with one chunk covering the whole sequence this is the image-set
-  layer).
+  layer);
+* "inclusive" mode (the tutorial page's per-token order, §3: update with x_t,
+  then output with the updated weights), for chunks of any size: query t of a
+  chunk sees the chunk's starting weights minus step times the summed
+  gradients of the chunk's tokens up to and including t, each taken at the
+  starting weights (mini-batch test-time training); the chunk then updates
+  with the sum over all its tokens. With chunks of one token this is exactly
+  the per-token recurrence. Plain gradient steps only (no Muon, momentum or
+  weight norm: those act on a whole chunk's update, not on a prefix of it).
 
 The sums over tokens of a whole-sequence chunk are taken over blocks of tokens
 (``block`` argument) only to bound host memory; in fp64 the grouping of the
@@ -255,9 +263,31 @@ def ttt_head(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.ndarray,
             if mask[ci]:
                 W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0, mom)
             O[s:e] = _apply_blocks(cfg, W, Q[s:e], block)
+        elif cfg.mode == "inclusive":
+            if cfg.muon or cfg.wnorm or cfg.momentum != 0.0:
+                raise ValueError("inclusive mode takes plain gradient steps only")
+            if mask[ci]:
+                O[s:e] = apply_inclusive(cfg, W, Q[s:e], K[s:e], V[s:e], lr[s:e])
+                W = update(cfg, W, chunk_grad(cfg, W, K[s:e], V[s:e], lr[s:e], block), n0, mom)
+            else:
+                O[s:e] = _apply_blocks(cfg, W, Q[s:e], block)
         else:
             raise ValueError(cfg.mode)
     return O, W
+
+
+def apply_inclusive(cfg: OracleCfg, W: Weights, Q: np.ndarray, K: np.ndarray, V: np.ndarray,
+                    eta: np.ndarray) -> np.ndarray:
+    """Outputs of one chunk in inclusive mode: for token t the weights
+    W - step * sum_{s <= t} grad_s(W), then f(q_t) (tutorial page §3)."""
+    acc = [np.zeros_like(w) for w in W]
+    out = np.empty((Q.shape[0], W[0].shape[0] if cfg.fast_net == "linear" else W[1].shape[0]))
+    for t in range(Q.shape[0]):
+        g = chunk_grad(cfg, W, K[t:t + 1], V[t:t + 1], eta[t:t + 1])
+        acc = [a + gj for a, gj in zip(acc, g)]
+        Wt = tuple(w - cfg.step * a for w, a in zip(W, acc))
+        out[t] = _apply(cfg, Wt, Q[t:t + 1])[0]
+    return out
 
 
 def _apply_blocks(cfg: OracleCfg, W: Weights, X: np.ndarray, block: int) -> np.ndarray:

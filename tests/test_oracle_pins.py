@@ -471,3 +471,102 @@ def test_a_zero_rate_leaves_its_matrix_unchanged():
     _, W = orc.ttt_head(cfg, Q, K, V, eta3, W0)
     assert np.array_equal(W[1], W0[1])
     assert np.abs(W[0] - W0[0]).max() > 1e-3 and np.abs(W[2] - W0[2]).max() > 1e-3
+
+
+# ---------------------------------------------------------------- inclusive (per-token) order
+def test_inclusive_chunk1_linear_mse_is_the_delta_rule_read_after_the_update():
+    """Tutorial page §3: theta_t = theta_{t-1} - eta grad l(theta_{t-1}; x_t), then
+    h_t = f(x_t; theta_t). Chunks of one token, linear net, MSE: the delta rule
+    with o_t read AFTER token t's own update."""
+    rng = np.random.default_rng(31)
+    d, T = 5, 21
+    W0 = rng.standard_normal((d, d)) / np.sqrt(d)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.2, T)
+    cfg = orc.OracleCfg(chunk=1, fast_net="linear", loss="mse", mode="inclusive", muon=False, wnorm=False)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    W = W0.copy()
+    Oref = np.zeros((T, d))
+    for t in range(T):
+        W = W - eta[t] * np.outer(W @ K[t] - V[t], K[t])
+        Oref[t] = W @ Q[t]
+    assert np.abs(O - Oref).max() <= 1e-12
+    assert np.abs(Wf - W).max() <= 1e-12
+
+
+@pytest.mark.parametrize("C", [1, 4, 7, 19])
+def test_inclusive_linear_ip_is_causal_linear_attention(C):
+    """Linear net, inner-product loss: the gradient does not depend on W, so for
+    every chunk size o_t = W0 q_t + step * sum_{s <= t} eta_s v_s (k_s . q_t):
+    causal (token-inclusive) linear attention."""
+    rng = np.random.default_rng(32)
+    d, T, step = 6, 19, 0.7
+    W0 = rng.standard_normal((d, d))
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.5, T)
+    cfg = orc.OracleCfg(chunk=C, fast_net="linear", loss="ip", mode="inclusive", muon=False, wnorm=False,
+                        step=step)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, eta, (W0,))
+    A = np.tril(Q @ K.T) * eta[None, :]
+    Oref = Q @ W0.T + step * A @ V
+    assert np.abs(O - Oref).max() <= 1e-12
+    assert np.abs(Wf - (W0 + step * (eta[:, None] * V).T @ K)).max() <= 1e-12
+
+
+def test_inclusive_chunk1_swiglu_is_the_per_token_recurrence():
+    """SwiGLU net, MSE, chunks of one token: update with token t, then output
+    with the updated weights, token after token."""
+    rng = np.random.default_rng(33)
+    d, dh, T = 4, 6, 9
+    W = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.3, T)
+    cfg = orc.OracleCfg(chunk=1, loss="mse", mode="inclusive", muon=False, wnorm=False)
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W)
+    Wt = tuple(w.copy() for w in W)
+    for t in range(T):
+        g = orc.swiglu_grad(Wt, K[t:t + 1], V[t:t + 1], eta[t:t + 1], "mse")
+        Wt = tuple(w - gj for w, gj in zip(Wt, g))
+        assert np.abs(O[t] - orc.swiglu_apply(Wt, Q[t:t + 1])[0]).max() <= 1e-12
+    for a, b in zip(Wf, Wt):
+        assert np.abs(a - b).max() <= 1e-12
+
+
+@pytest.mark.parametrize("loss", ["ip", "mse"])
+def test_inclusive_swiglu_chunk_equals_its_dual_form(loss):
+    """Each layer of the SwiGLU net is linear in its weights and each token's
+    gradient is an outer product, so the prefix weights never need forming:
+    A_q = Q W1^T - step tril(Q K^T) DA, B_q = Q W3^T - step tril(Q K^T) DB,
+    H_q = silu(A_q) * B_q, O = H_q W2^T - step tril(H_q H_k^T) Yh, where DA,
+    DB, H_k, Yh = eta * dl/df are the keys' quantities at the chunk's starting
+    weights."""
+    rng = np.random.default_rng(34)
+    d, dh, C, step = 5, 8, 11, 0.6
+    W1, W2, W3 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((C, d)) for _ in range(3))
+    eta = rng.uniform(0, 0.4, C)
+    cfg = orc.OracleCfg(chunk=C, loss=loss, mode="inclusive", muon=False, wnorm=False, step=step)
+    got = orc.apply_inclusive(cfg, (W1, W2, W3), Q, K, V, eta)
+    A, Bm = K @ W1.T, K @ W3.T
+    sg = 1.0 / (1.0 + np.exp(-A))
+    Hk = A * sg * Bm
+    Y = (Hk @ W2.T - V) if loss == "mse" else -V
+    Yh = eta[:, None] * Y
+    DH = Yh @ W2
+    DA = DH * Bm * sg * (1.0 + A * (1.0 - sg))
+    DB = DH * A * sg
+    L = np.tril(Q @ K.T)
+    Aq = Q @ W1.T - step * L @ DA
+    Bq = Q @ W3.T - step * L @ DB
+    Hq = Aq / (1.0 + np.exp(-Aq)) * Bq
+    Oref = Hq @ W2.T - step * np.tril(Hq @ Hk.T) @ Yh
+    assert np.abs(got - Oref).max() <= 1e-12 * max(1.0, np.abs(Oref).max())
+
+
+def test_inclusive_mode_refuses_chunk_level_optimisers():
+    cfg = orc.OracleCfg(chunk=4, mode="inclusive", muon=True, wnorm=False)
+    rng = np.random.default_rng(35)
+    W = _rand_weights("swiglu", 4, 6, rng)
+    X = rng.standard_normal((8, 4))
+    with pytest.raises(ValueError):
+        orc.ttt_head(cfg, X, X, X, np.ones(8), W)
