@@ -51,7 +51,17 @@ extern "C" {
 /* ---- enumerations -------------------------------------------------------- */
 enum { TTT_NET_SWIGLU = 0, TTT_NET_LINEAR = 1 };
 enum { TTT_LOSS_IP = 0, TTT_LOSS_MSE = 1 };
-enum { TTT_MODE_SHIFTED = 0, TTT_MODE_SINGLE = 1 };
+/* SHIFTED: chunk c is applied with the weights left by chunks 0..c-1, then
+ *          updates (LaCT page §3.2);
+ * SINGLE: every chunk updates, then applies to its own queries (§3.1);
+ * INCLUSIVE: query t of a chunk sees the chunk's starting weights minus step
+ *          times the gradients of the chunk's tokens up to and including t
+ *          (each taken at the starting weights); the chunk then updates with
+ *          all of them. With chunks of one token this is the per-token order
+ *          of the TTT tutorial page (§3: update with x_t, then output with the
+ *          updated weights). Plain gradient steps only: muon = wnorm = 0 and
+ *          momentum = 0, else TTT_ERR_ARG. */
+enum { TTT_MODE_SHIFTED = 0, TTT_MODE_SINGLE = 1, TTT_MODE_INCLUSIVE = 2 };
 enum { TTT_DTYPE_F32 = 0, TTT_DTYPE_BF16 = 1 };
 /* kernel family: AUTO picks the fastest one that covers the request */
 enum { TTT_IMPL_AUTO = 0, TTT_IMPL_SIMT = 1, TTT_IMPL_TC = 2, TTT_IMPL_LINEAR = 3 };
@@ -196,6 +206,47 @@ TTT_API int ttt_fwd_static_scratch(const ttt_cfg* cfg,
             const float* W0_1, const float* W0_2, const float* W0_3,
             void* O, float* Wf_1, float* Wf_2, float* Wf_3,
             int* status, void* stream);
+
+/* ---- context parallelism (LaCT page §2.2.2) -------------------------------
+ * The tokens of one chunk are split into shards held by different GPUs (or
+ * handled by different calls). Every shard computes its partial gradient with
+ * the same fast weights; the caller sums the partials over the shards (an
+ * all-reduce: the one exchange of the method); every shard then applies the
+ * same update to its copy of the weights, and its own queries. These calls
+ * run those steps one at a time on a state kept in the caller's workspace.
+ * They cover the tensor-core family (bf16 SwiGLU, inner-product loss).
+ *
+ * cfg: B, H, d, dh and the update hyper-parameters as for ttt_fwd; cfg->chunk
+ *      = the largest token count of one ttt_cp_grad / ttt_cp_apply call;
+ *      cfg->T >= 1, cfg->mode and cfg->update_mask are not used (the caller
+ *      orders apply, gradient and update).
+ * Tokens: Q, K, V [B, H, T_all, d] bf16 and lr [B, H, T_all(, 3)] fp32 as for
+ *      ttt_fwd, of which the call uses tokens [start, start + n) of every
+ *      (b, h); O has Q's layout and gets those tokens written.
+ * G:   per (b, h), the gradients of W1, W2, W3 as [B * H][3][d][dh] fp32, W1
+ *      and W3 transposed (d x dh), W2 as is: the partial of one shard from
+ *      ttt_cp_grad, the sum over the shards for ttt_cp_update.
+ * All pointers are device memory of the current device, 16-byte aligned; the
+ * workspace (>= ttt_cp_workspace_bytes, 256-byte aligned) holds the state from
+ * ttt_cp_begin to ttt_cp_end and the status word (read it with ttt_status).
+ * Work is enqueued on `stream`. Each call returns TTT_OK or a host-detected
+ * error (TTT_ERR_ARG, _UNSUPPORTED, _WORKSPACE, _CUDA) before any launch. */
+TTT_API int ttt_cp_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
+/* Loads W0 (layouts of ttt_fwd) into the state; clears the status word. */
+TTT_API int ttt_cp_begin(const ttt_cfg* cfg, const float* W0_1, const float* W0_2, const float* W0_3,
+                         void* workspace, size_t workspace_bytes, void* stream);
+/* The partial gradient of tokens [start, start + n) with the current weights. */
+TTT_API int ttt_cp_grad(const ttt_cfg* cfg, const void* K, const void* V, const float* lr, int T_all,
+                        int start, int n, float* G, void* workspace, size_t workspace_bytes, void* stream);
+/* One update (momentum, Muon, step, weight norm) from the summed gradient. */
+TTT_API int ttt_cp_update(const ttt_cfg* cfg, const float* G, void* workspace, size_t workspace_bytes,
+                          void* stream);
+/* O of tokens [start, start + n) with the current weights. */
+TTT_API int ttt_cp_apply(const ttt_cfg* cfg, const void* Q, int T_all, int start, int n, void* O,
+                         void* workspace, size_t workspace_bytes, void* stream);
+/* Writes the current weights to Wf_1..3 ([B, H, out, in] fp32, as ttt_fwd). */
+TTT_API int ttt_cp_end(const ttt_cfg* cfg, float* Wf_1, float* Wf_2, float* Wf_3, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* Which kernel family AUTO (or cfg->impl) resolves to for *cfg: TTT_IMPL_*,
  * or a negative status if none covers it. */

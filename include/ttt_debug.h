@@ -24,18 +24,6 @@ extern "C" {
 TTT_API int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, float* D,
                               int Z, int M, int N, int K, void* stream);
 
-/* D[z] = A[z] * B[z]^T on 256 x 256 tiles computed by CTA pairs (tcgen05
- * cta_group::2: the even CTA of a two-CTA cluster issues M = 256 MMAs over both
- * CTAs' shared memory and TMEM), with the Newton-Schulz operand layouts.
- *   A  bf16, DEVICE: [Z, M, K] (K-major)
- *   B  bf16, DEVICE: [Z, N, K] when b_mn_major == 0, else [Z, K, N]
- *   D  fp32, DEVICE: [Z, M, N], written
- * M, N positive multiples of 256, K a positive multiple of 32; pointers 16-byte
- * aligned. Synchronises `stream`; returns TTT_OK, TTT_ERR_ARG, TTT_ERR_CUDA or
- * TTT_ERR_TIMEOUT (a wait ran out). */
-TTT_API int ttt_dbg_gemm_pair_bf16(const void* A, const void* B, int b_mn_major, float* D, int Z, int M, int N,
-                                   int K, void* stream);
-
 /* CTAs of the fused Muon kernel's cooperative grid for *cfg on the current
  * device; *resident (may be NULL) receives how many of its CTAs fit at once.
  * Returns TTT_OK, TTT_ERR_ARG (cfg not on the tensor-core path) or TTT_ERR_CUDA. */
@@ -53,18 +41,27 @@ TTT_API int ttt_dbg_split_mask(int mask);
  * Returns TTT_OK or TTT_ERR_ARG. */
 TTT_API int ttt_dbg_ns_force_grid(int ctas);
 
-/* Whether the fused Muon kernel may run its GEMM phases on CTA pairs
- * (cta_group::2 tiles of 256 rows; taken when d and dh are multiples of 256).
- * Default 0 (single-CTA tiles). Process-global, for comparisons and tests. Returns TTT_OK. */
-TTT_API int ttt_dbg_ns_pairs(int on);
+/* Whether the fused Muon kernel computes the symmetric d x d products
+ * (R = X X^T + beta I and P = c R^2 + alpha I) on the tiles that meet the upper
+ * triangle only, writing the missing lower blocks as transposes: 1 always,
+ * 0 never, -1 (default) when an iteration has more than four tiles per SM.
+ * Process-global, for comparisons and tests. Returns TTT_OK. */
+TTT_API int ttt_dbg_ns_symmetric(int on);
+
+/* Column-tile widths of the fused Muon kernel's d x d products (bns) and of its
+ * X updates (bnx): 128 or 256, each dividing d (bns, or d <= bns) and dh (bnx);
+ * 0 = chosen by the shape (the default). Process-global, for tuning sweeps and
+ * tests. Returns TTT_OK or TTT_ERR_ARG. */
+TTT_API int ttt_dbg_ns_tiles(int bns, int bnx);
 
 /* Phase timeline of the fused Muon kernel. With tracing on, every later launch
  * records %globaltimer stamps (ns) into a device table: slot 0 the start,
- * slot 1 the last CTA's exit, and for grid barrier i >= 1 (the phases end at
- * barriers) slots 3i, 3i+1, 3i+2 the first and the last CTA's arrival and CTA
- * 0's departure. A traced launch synchronises its stream first. read copies
- * the first n (<= 96) slots of the last traced launch to HOST memory `out`.
- * Return TTT_OK, TTT_ERR_ARG or TTT_ERR_CUDA. */
+ * slot 1 the last CTA's exit, and for phase i of the item list (0 norm1,
+ * 1 norm2, 2 + 3 it + k the Gram / polynomial / X update of iteration it, then
+ * the weight norm) slot 2 + 2i the earliest start and slot 3 + 2i the latest
+ * finish of one of its items. A traced launch synchronises its stream first.
+ * read copies the first n (<= 96) slots of the last traced launch to HOST
+ * memory `out`. Return TTT_OK, TTT_ERR_ARG or TTT_ERR_CUDA. */
 TTT_API int ttt_dbg_ns_trace(int on);
 TTT_API int ttt_dbg_ns_trace_read(unsigned long long* out, int n);
 
@@ -82,11 +79,12 @@ TTT_API void ttt_dbg_stall_next_linear(void);
  * starts from W0 again and is unaffected. */
 TTT_API void ttt_dbg_stall_next_fwd(void);
 
-/* Failure-detection test: in the next launch of the fused Muon kernel the last
- * CTA does not arrive at the first grid barrier, so every CTA's bounded wait
- * runs out; TTT_ERR_TIMEOUT is recorded, every CTA skips the remaining work,
- * frees its TMEM and returns. Later launches are unaffected. */
-TTT_API void ttt_dbg_stall_next_ns_barrier(void);
+/* Failure-detection test: in the next launch of the fused Muon kernel CTA 0
+ * never signals the completion of its first item, so the items of that
+ * matrix's next phase wait until their bounded waits run out; TTT_ERR_TIMEOUT
+ * is recorded, every CTA skips the remaining work, drains what it has in
+ * flight, frees its TMEM and returns. Later launches are unaffected. */
+TTT_API void ttt_dbg_stall_next_ns(void);
 
 /* ---- launch accounting and per-kernel timing ------------------------------
  * Every kernel launch of the library is counted by class. With timing on, each
@@ -104,7 +102,7 @@ enum {
   TTT_KERNEL_LINEAR = 8,  /* linear small-chunk persistent kernel                            */
   TTT_KERNEL_SIMT = 9,    /* fp32 SIMT layer kernel                                          */
   TTT_KERNEL_NS = 10,     /* fused Muon step: normalise, 5 Newton-Schulz iterations, update,
-                             row weight norm (one cooperative grid over every matrix)       */
+                             row weight norm (one dataflow launch over every matrix)        */
   TTT_KERNEL_COUNT = 11
 };
 

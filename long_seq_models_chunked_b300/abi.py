@@ -31,7 +31,7 @@ TTT_ERR_SCRATCH_LIMIT = -8
 TTT_STATIC_SCRATCH_BYTES = 16 << 20
 TTT_NET_SWIGLU, TTT_NET_LINEAR = 0, 1
 TTT_LOSS_IP, TTT_LOSS_MSE = 0, 1
-TTT_MODE_SHIFTED, TTT_MODE_SINGLE = 0, 1
+TTT_MODE_SHIFTED, TTT_MODE_SINGLE, TTT_MODE_INCLUSIVE = 0, 1, 2
 TTT_DTYPE_F32, TTT_DTYPE_BF16 = 0, 1
 TTT_IMPL_AUTO, TTT_IMPL_SIMT, TTT_IMPL_TC, TTT_IMPL_LINEAR = 0, 1, 2, 3
 TTT_PREC_SPLIT, TTT_PREC_SINGLE = 0, 1
@@ -41,9 +41,10 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_abi_version", "ttt_cfg_size", "ttt_dbg_gemm_bf16", "ttt_prof_enable",
             "ttt_prof_reset", "ttt_prof_read", "ttt_launch_count", "ttt_kernel_name",
             "ttt_fwd_static_scratch", "ttt_dbg_ns_plan", "ttt_dbg_ns_force_grid",
-            "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_gemm_pair_bf16", "ttt_dbg_ns_trace",
-            "ttt_dbg_ns_trace_read", "ttt_dbg_ns_pairs",
-            "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns_barrier", "ttt_build_features")
+            "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_ns_trace",
+            "ttt_dbg_ns_trace_read", "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns", "ttt_build_features",
+            "ttt_dbg_ns_symmetric", "ttt_cp_workspace_bytes", "ttt_cp_begin", "ttt_cp_grad", "ttt_cp_update",
+            "ttt_cp_apply", "ttt_cp_end", "ttt_dbg_ns_tiles")
 TTT_FEATURE_CLUSTER_MULTICAST = 1
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
@@ -99,13 +100,22 @@ def _load():
     lib.ttt_dbg_gemm_bf16.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                       c_int, c_void_p]
     lib.ttt_dbg_gemm_bf16.restype = c_int
-    lib.ttt_dbg_gemm_pair_bf16.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
-                                           c_void_p]
-    lib.ttt_dbg_gemm_pair_bf16.restype = c_int
+    lib.ttt_cp_workspace_bytes.argtypes = [P, ctypes.POINTER(c_size_t)]
+    lib.ttt_cp_begin.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.ttt_cp_grad.argtypes = [P, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                c_size_t, c_void_p]
+    lib.ttt_cp_update.argtypes = [P, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.ttt_cp_apply.argtypes = [P, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.ttt_cp_end.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    for name in ("ttt_cp_workspace_bytes", "ttt_cp_begin", "ttt_cp_grad", "ttt_cp_update", "ttt_cp_apply",
+                 "ttt_cp_end"):
+        getattr(lib, name).restype = c_int
     lib.ttt_build_features.argtypes = []
     lib.ttt_build_features.restype = c_int
-    lib.ttt_dbg_ns_pairs.argtypes = [c_int]
-    lib.ttt_dbg_ns_pairs.restype = c_int
+    lib.ttt_dbg_ns_tiles.argtypes = [c_int, c_int]
+    lib.ttt_dbg_ns_tiles.restype = c_int
+    lib.ttt_dbg_ns_symmetric.argtypes = [c_int]
+    lib.ttt_dbg_ns_symmetric.restype = c_int
     lib.ttt_dbg_ns_trace.argtypes = [c_int]
     lib.ttt_dbg_ns_trace.restype = c_int
     lib.ttt_dbg_ns_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), c_int]
@@ -118,7 +128,7 @@ def _load():
     lib.ttt_dbg_split_mask.restype = c_int
     lib.ttt_dbg_stall_next_linear.argtypes = []
     lib.ttt_dbg_stall_next_linear.restype = None
-    for name in ("ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns_barrier"):
+    for name in ("ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns"):
         getattr(lib, name).argtypes = []
         getattr(lib, name).restype = None
     lib.ttt_prof_enable.argtypes = [c_int]
@@ -237,6 +247,47 @@ def ttt_fwd_static_scratch(cfg: ttt_cfg, Q, K, V, lr, W0_1, W0_2, W0_3, O, Wf_1,
     return rc
 
 
+# ----------------------------------------------------------------- context parallelism
+def _cp_check(rc, where):
+    if rc != TTT_OK:
+        raise TTTError(rc, where)
+
+
+def ttt_cp_workspace_bytes(cfg: ttt_cfg) -> int:
+    n = c_size_t(0)
+    _cp_check(_lib.ttt_cp_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "ttt_cp_workspace_bytes")
+    return n.value
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def ttt_cp_begin(cfg: ttt_cfg, W0_1, W0_2, W0_3, workspace, stream=None) -> None:
+    _cp_check(_lib.ttt_cp_begin(ctypes.byref(cfg), _ptr(W0_1), _ptr(W0_2), _ptr(W0_3), _ptr(workspace),
+                                _nbytes(workspace), _stream_handle(stream)), "ttt_cp_begin")
+
+
+def ttt_cp_grad(cfg: ttt_cfg, K, V, lr, T_all: int, start: int, n: int, G, workspace, stream=None) -> None:
+    _cp_check(_lib.ttt_cp_grad(ctypes.byref(cfg), _ptr(K), _ptr(V), _ptr(lr), T_all, start, n, _ptr(G),
+                               _ptr(workspace), _nbytes(workspace), _stream_handle(stream)), "ttt_cp_grad")
+
+
+def ttt_cp_update(cfg: ttt_cfg, G, workspace, stream=None) -> None:
+    _cp_check(_lib.ttt_cp_update(ctypes.byref(cfg), _ptr(G), _ptr(workspace), _nbytes(workspace),
+                                 _stream_handle(stream)), "ttt_cp_update")
+
+
+def ttt_cp_apply(cfg: ttt_cfg, Q, T_all: int, start: int, n: int, O, workspace, stream=None) -> None:
+    _cp_check(_lib.ttt_cp_apply(ctypes.byref(cfg), _ptr(Q), T_all, start, n, _ptr(O), _ptr(workspace),
+                                _nbytes(workspace), _stream_handle(stream)), "ttt_cp_apply")
+
+
+def ttt_cp_end(cfg: ttt_cfg, Wf_1, Wf_2, Wf_3, workspace, stream=None) -> None:
+    _cp_check(_lib.ttt_cp_end(ctypes.byref(cfg), _ptr(Wf_1), _ptr(Wf_2), _ptr(Wf_3), _ptr(workspace),
+                              _nbytes(workspace), _stream_handle(stream)), "ttt_cp_end")
+
+
 def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: int, N: int, K: int,
                       stream=None) -> int:
     """Test hook: D[z] = A[z] B[z]^T on the tcgen05 tile kernel (include/ttt_debug.h)."""
@@ -244,20 +295,22 @@ def ttt_dbg_gemm_bf16(A, a_mn_major: bool, B, b_mn_major: bool, D, Z: int, M: in
                                   K, _stream_handle(stream))
 
 
-def ttt_dbg_gemm_pair_bf16(A, B, b_mn_major: bool, D, Z: int, M: int, N: int, K: int, stream=None) -> int:
-    """Test hook: D[z] = A[z] B[z]^T on CTA-pair (cta_group::2) tiles (include/ttt_debug.h)."""
-    return _lib.ttt_dbg_gemm_pair_bf16(_ptr(A), _ptr(B), int(b_mn_major), _ptr(D), Z, M, N, K,
-                                       _stream_handle(stream))
-
-
 def ttt_build_features() -> int:
     """Bit flags of the loaded build (TTT_FEATURE_CLUSTER_MULTICAST)."""
     return _lib.ttt_build_features()
 
 
-def ttt_dbg_ns_pairs(on: bool) -> int:
-    """Test hook: allow CTA-pair tiles in the fused Muon kernel (include/ttt_debug.h)."""
-    return _lib.ttt_dbg_ns_pairs(int(on))
+def ttt_dbg_ns_symmetric(on: int) -> int:
+    """Test hook: symmetric (upper-triangle) tiles in the fused Muon kernel:
+    1 always, 0 never, -1 chosen by the shape (the default)."""
+    return _lib.ttt_dbg_ns_symmetric(int(on))
+
+
+def ttt_dbg_ns_tiles(bns: int, bnx: int) -> None:
+    """Test hook: column-tile widths of the fused Muon kernel (0 = by shape)."""
+    rc = _lib.ttt_dbg_ns_tiles(int(bns), int(bnx))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_ns_tiles")
 
 
 def ttt_dbg_ns_trace(on: bool) -> int:
@@ -308,9 +361,9 @@ def ttt_dbg_stall_next_fwd() -> None:
     _lib.ttt_dbg_stall_next_fwd()
 
 
-def ttt_dbg_stall_next_ns_barrier() -> None:
-    """Test hook: the next fused Muon launch loses one arrival at its first grid barrier."""
-    _lib.ttt_dbg_stall_next_ns_barrier()
+def ttt_dbg_stall_next_ns() -> None:
+    """Test hook: the next fused Muon launch loses one item's completion signal."""
+    _lib.ttt_dbg_stall_next_ns()
 
 
 def ttt_prof_enable(on: bool) -> None:
@@ -357,7 +410,7 @@ def cfg_from_spec(spec, impl: int = TTT_IMPL_AUTO, check_finite: bool = False,
     c.d, c.dh, c.chunk = spec.d, spec.dh, spec.chunk
     c.fast_net = TTT_NET_SWIGLU if spec.fast_net == "swiglu" else TTT_NET_LINEAR
     c.loss = TTT_LOSS_IP if spec.loss == "ip" else TTT_LOSS_MSE
-    c.mode = TTT_MODE_SHIFTED if spec.mode == "shifted" else TTT_MODE_SINGLE
+    c.mode = {"shifted": TTT_MODE_SHIFTED, "single": TTT_MODE_SINGLE, "inclusive": TTT_MODE_INCLUSIVE}[spec.mode]
     c.dtype = TTT_DTYPE_F32 if spec.dtype == "fp32" else TTT_DTYPE_BF16
     c.muon = int(spec.muon)
     c.ns_iters = spec.ns_iters

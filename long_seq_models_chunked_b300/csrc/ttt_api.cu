@@ -16,13 +16,16 @@ constexpr int kMaxPipelineChunks = 512;  // per-chunk events of ttt_fwd_host
 
 int elem_bytes(int dtype) { return dtype == TTT_DTYPE_F32 ? 4 : 2; }
 
+}  // namespace
+
 int validate_cfg(const ttt_cfg* g) {
   if (!g) return TTT_ERR_ARG;
   if (g->B < 1 || g->H < 1 || g->T < 1 || g->d < 1 || g->chunk < 1) return TTT_ERR_ARG;
   if (g->fast_net != TTT_NET_SWIGLU && g->fast_net != TTT_NET_LINEAR) return TTT_ERR_ARG;
   if (g->fast_net == TTT_NET_SWIGLU && g->dh < 1) return TTT_ERR_ARG;
   if (g->loss != TTT_LOSS_IP && g->loss != TTT_LOSS_MSE) return TTT_ERR_ARG;
-  if (g->mode != TTT_MODE_SHIFTED && g->mode != TTT_MODE_SINGLE) return TTT_ERR_ARG;
+  if (g->mode != TTT_MODE_SHIFTED && g->mode != TTT_MODE_SINGLE && g->mode != TTT_MODE_INCLUSIVE)
+    return TTT_ERR_ARG;
   if (g->dtype != TTT_DTYPE_F32 && g->dtype != TTT_DTYPE_BF16) return TTT_ERR_ARG;
   if ((g->muon != 0 && g->muon != 1) || (g->wnorm != 0 && g->wnorm != 1)) return TTT_ERR_ARG;
   if (g->ns_iters < 0 || g->ns_iters > 64) return TTT_ERR_ARG;
@@ -36,12 +39,16 @@ int validate_cfg(const ttt_cfg* g) {
   if (g->precision != TTT_PREC_SPLIT && g->precision != TTT_PREC_SINGLE) return TTT_ERR_ARG;
   if (!std::isfinite(g->momentum)) return TTT_ERR_ARG;
   if (g->lr_per_matrix != 0 && g->lr_per_matrix != 1) return TTT_ERR_ARG;
+  // the inclusive order takes plain gradient steps (a prefix of a chunk has no Muon, momentum or norm)
+  if (g->mode == TTT_MODE_INCLUSIVE && (g->muon || g->wnorm || g->momentum != 0.f)) return TTT_ERR_ARG;
   const int64_t tok = (int64_t)g->B * g->H * g->T;
   if (tok * g->d > kMaxElems) return TTT_ERR_ARG;
   const int64_t wd = g->fast_net == TTT_NET_SWIGLU ? (int64_t)g->d * g->dh : (int64_t)g->d * g->d;
   if ((int64_t)g->B * g->H * wd > kMaxElems) return TTT_ERR_ARG;
   return TTT_OK;
 }
+
+namespace {
 
 int select_impl(const ttt_cfg& g) {
   switch (g.impl) {

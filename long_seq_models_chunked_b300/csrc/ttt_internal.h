@@ -52,6 +52,8 @@ size_t linear_workspace_bytes(const ttt_cfg& cfg);
 int linear_run(const Call& c);
 
 // ---- misc ------------------------------------------------------------------
+// TTT_OK or TTT_ERR_ARG: field ranges and sizes of *cfg (host only).
+int validate_cfg(const ttt_cfg* cfg);
 int launch_check_finite(const Call& c);
 // TTT_OK when every non-NULL pointer is device memory of the current device,
 // else TTT_ERR_ARG (TTT_ERR_CUDA if the current device cannot be queried).

@@ -24,6 +24,12 @@ struct NsFusedArgs {
   float* scratch;        // >= ns_fused_scratch_floats() floats (partial sums, barrier)
   float* mom;            // [Z][d][dh] momentum buffers (B <- mu B + G), or nullptr
   float mu;
+  // fused normalisation: the gradient kernel wrote Xh[0] / Xl[0] from the
+  // UNSCALED gradient (momentum already advanced) and per-z partial sums of
+  // squares nsqg[z][nsq_n]; X and mom are then unused
+  bool fused;
+  const float* nsqg;
+  int nsq_n;
   TcCommon cm;
 };
 

@@ -21,6 +21,7 @@ constexpr int kTokenBlock = 64;
 struct SimtLayout {
   size_t W[3], G[3], N0[3], Mom[3];
   size_t A, Bm, Hh, Y;
+  size_t Hq, KQ;  // inclusive order: the block's query hiddens, and q.k / h_q.h_k products
   size_t X, S, P, Xn;
   size_t total;
 };
@@ -45,6 +46,8 @@ __host__ __device__ inline SimtLayout simt_layout(int fast_net, int d, int dh, i
   L.Bm = off; off += align_up((size_t)tb * hid, 64);
   L.Hh = off; off += align_up((size_t)tb * hid, 64);
   L.Y = off;  off += align_up((size_t)tb * d, 64);
+  L.Hq = off; off += align_up((size_t)tb * hid, 64);
+  L.KQ = off; off += align_up((size_t)tb * tb, 64);
   const size_t m = nw == 3 ? (d < dh ? d : dh) : d;
   const size_t n = nw == 3 ? (d < dh ? dh : d) : d;
   L.X = off;  off += align_up(m * n, 64);
@@ -204,6 +207,107 @@ __device__ void apply_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, s
   }
 }
 
+// Inclusive order (tutorial page §3: update with a token, then output with the
+// updated weights), one token block [t0, t0 + nt) of a chunk: query t sees
+// W - step (G + sum_{s <= t in the block} G_s), G the gradient summed over the
+// chunk's earlier blocks and G_s token s's gradient, all at the chunk's
+// starting weights W. Each layer is linear in its weights and every G_s is an
+// outer product, so the block's part is a causal dual form:
+//   A_q = q (W1 - step G1)^T - step sum_{s<=t} (q.k_s) DA_s   (B_q likewise with DB)
+//   o   = (W2 - step G2) h_q - step sum_{s<=t} (h_q.h_s) lr2_s y_s
+// On entry A, Bm hold the block's DA, DB (rates applied), Hh its key hiddens,
+// Y its dl/df without rates; G holds the earlier blocks' sums.
+template <class Eta>
+__device__ void inclusive_block_swiglu(const SimtArgs& a, float* ws, const SimtLayout& L, size_t head, int t0,
+                                       int nt, Eta eta) {
+  const int d = a.d, dh = a.dh;
+  const size_t base = (head * a.T + t0) * (size_t)d;
+  const float* W1 = ws + L.W[0];
+  const float* W2 = ws + L.W[1];
+  const float* W3 = ws + L.W[2];
+  const float* G1 = ws + L.G[0];
+  const float* G2 = ws + L.G[1];
+  const float* G3 = ws + L.G[2];
+  const float* DA = ws + L.A;
+  const float* DB = ws + L.Bm;
+  const float* Hk = ws + L.Hh;
+  const float* Y = ws + L.Y;
+  float* Hq = ws + L.Hq;
+  float* KQ = ws + L.KQ;
+  const float st = a.step;
+  for (int idx = threadIdx.x; idx < nt * nt; idx += blockDim.x) {
+    const int t = idx / nt, u = idx % nt;
+    float acc = 0.f;
+    if (u <= t)
+      for (int i = 0; i < d; ++i)
+        acc = fmaf(ld_val(a.Q, base + (size_t)t * d + i, a.dtype), ld_val(a.K, base + (size_t)u * d + i, a.dtype), acc);
+    KQ[idx] = acc;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+    const int t = idx / dh, j = idx % dh;
+    float xa = 0.f, xb = 0.f;
+    for (int i = 0; i < d; ++i) {
+      const float q = ld_val(a.Q, base + (size_t)t * d + i, a.dtype);
+      xa = fmaf(W1[(size_t)j * d + i] - st * G1[(size_t)j * d + i], q, xa);
+      xb = fmaf(W3[(size_t)j * d + i] - st * G3[(size_t)j * d + i], q, xb);
+    }
+    for (int u = 0; u <= t; ++u) {
+      xa = fmaf(-st * KQ[(size_t)t * nt + u], DA[(size_t)u * dh + j], xa);
+      xb = fmaf(-st * KQ[(size_t)t * nt + u], DB[(size_t)u * dh + j], xb);
+    }
+    Hq[idx] = xa * sigmoidf_(xa) * xb;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nt * nt; idx += blockDim.x) {  // KQ now holds h_q . h_k
+    const int t = idx / nt, u = idx % nt;
+    float acc = 0.f;
+    if (u <= t)
+      for (int j = 0; j < dh; ++j) acc = fmaf(Hq[(size_t)t * dh + j], Hk[(size_t)u * dh + j], acc);
+    KQ[idx] = acc;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+    const int t = idx / d, i = idx % d;
+    float o = 0.f;
+    for (int j = 0; j < dh; ++j) o = fmaf(W2[(size_t)i * dh + j] - st * G2[(size_t)i * dh + j], Hq[(size_t)t * dh + j], o);
+    for (int u = 0; u <= t; ++u) o = fmaf(-st * KQ[(size_t)t * nt + u] * eta(u, 1), Y[(size_t)u * d + i], o);
+    st_val(a.O, base + idx, a.dtype, o);
+  }
+  __syncthreads();
+}
+
+// The linear net's block: o = (W - step G) q - step sum_{s<=t} (q.k_s) y_s, with
+// Y = lr * dl/df (rates applied) on entry.
+__device__ void inclusive_block_linear(const SimtArgs& a, float* ws, const SimtLayout& L, size_t head, int t0,
+                                       int nt) {
+  const int d = a.d;
+  const size_t base = (head * a.T + t0) * (size_t)d;
+  const float* W = ws + L.W[0];
+  const float* G = ws + L.G[0];
+  const float* Y = ws + L.Y;
+  float* KQ = ws + L.KQ;
+  const float st = a.step;
+  for (int idx = threadIdx.x; idx < nt * nt; idx += blockDim.x) {
+    const int t = idx / nt, u = idx % nt;
+    float acc = 0.f;
+    if (u <= t)
+      for (int i = 0; i < d; ++i)
+        acc = fmaf(ld_val(a.Q, base + (size_t)t * d + i, a.dtype), ld_val(a.K, base + (size_t)u * d + i, a.dtype), acc);
+    KQ[idx] = acc;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+    const int t = idx / d, i = idx % d;
+    float o = 0.f;
+    for (int k = 0; k < d; ++k)
+      o = fmaf(W[(size_t)i * d + k] - st * G[(size_t)i * d + k], ld_val(a.Q, base + (size_t)t * d + k, a.dtype), o);
+    for (int u = 0; u <= t; ++u) o = fmaf(-st * KQ[(size_t)t * nt + u], Y[(size_t)u * d + i], o);
+    st_val(a.O, base + idx, a.dtype, o);
+  }
+  __syncthreads();
+}
+
 __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, size_t head,
                              int s, int e, float* red) {
   const int d = a.d, dh = a.dh;
@@ -265,6 +369,7 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
         Bm[idx] = eta(t, 2) * g * xa * sg;                             // lr3 * dl/db
       }
       __syncthreads();
+      if (a.mode == TTT_MODE_INCLUSIVE) inclusive_block_swiglu(a, ws, L, head, t0, nt, eta);
       float* G1 = ws + L.G[0];
       float* G2 = ws + L.G[1];
       float* G3 = ws + L.G[2];
@@ -303,6 +408,7 @@ __device__ void update_chunk(const SimtArgs& a, float* ws, const SimtLayout& L, 
         Y[idx] = y;
       }
       __syncthreads();
+      if (a.mode == TTT_MODE_INCLUSIVE) inclusive_block_linear(a, ws, L, head, t0, nt);
       float* G = ws + L.G[0];
       for (int idx = threadIdx.x; idx < d * d; idx += blockDim.x) {
         const int i = idx / d, k = idx % d;
@@ -365,6 +471,13 @@ __global__ void __launch_bounds__(kThreads) simt_layer_kernel(const __grid_const
     if (a.mode == TTT_MODE_SHIFTED) {
       apply_chunk(a, ws, L, head, s, e);
       if (upd) update_chunk(a, ws, L, head, s, e, red);
+    } else if (a.mode == TTT_MODE_INCLUSIVE) {
+      // the update writes the chunk's outputs on the way (each token block's
+      // queries before the block's gradient joins the sum)
+      if (upd)
+        update_chunk(a, ws, L, head, s, e, red);
+      else
+        apply_chunk(a, ws, L, head, s, e);
     } else {
       if (upd) update_chunk(a, ws, L, head, s, e, red);
       apply_chunk(a, ws, L, head, s, e);

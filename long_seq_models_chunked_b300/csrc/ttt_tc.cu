@@ -278,6 +278,15 @@ struct GradMcOp {
     float* split_out;      // [splits][Z][d][dh] fp32 (splits > 1)
     int d, dh, Z, chunk_idx, chunk_start, valid, use4d, nt, splits, kb_per_split, e_split;
     int mg, cs;            // row groups per item and CTAs per cluster (mg * cs = ceil(d / 128))
+    // Newton-Schulz input (splits == 1, Xh != NULL): instead of fp32 G the
+    // epilogue writes the gradient (or the momentum buffer B <- mu B + G, with
+    // mom != NULL) as bf16 (hi, lo) operands and, per row and column tile, the
+    // sum of squares nsq[(z d + m) nt + n0 / BN] for the Frobenius norm
+    bf16* Xh;
+    bf16* Xl;
+    float* mom;
+    float mu;
+    float* nsq;
     TcCommon cm;
   };
   struct Tile {
@@ -344,6 +353,32 @@ struct GradMcOp {
   static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&) {
     const int m = t.m0 + r;
     float v[32];
+    if (p.Xh && p.splits == 1) {
+      float ss = 0.f;
+      for (int c = 0; c < BN; c += 32) {
+        ptx::tmem_ld32(tm + c, v);
+        if (m < p.d) {
+          const size_t o = ((size_t)t.z * p.d + m) * p.dh + t.n0 + c;
+          if (p.mom) {
+            float4* mb = reinterpret_cast<float4*>(p.mom + o);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 b = mb[q];
+              v[4 * q + 0] = fmaf(p.mu, b.x, v[4 * q + 0]);
+              v[4 * q + 1] = fmaf(p.mu, b.y, v[4 * q + 1]);
+              v[4 * q + 2] = fmaf(p.mu, b.z, v[4 * q + 2]);
+              v[4 * q + 3] = fmaf(p.mu, b.w, v[4 * q + 3]);
+              mb[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+          }
+          st_bf16pair32(p.Xh + o, p.Xl + o, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+        }
+      }
+      if (m < p.d) p.nsq[((size_t)t.z * p.d + m) * p.nt + t.n0 / BN] = ss;
+      return;
+    }
     float* dst = p.splits > 1 ? p.split_out + (size_t)t.split * p.Z * p.d * p.dh : p.G;
     for (int c = 0; c < BN; c += 32) {
       ptx::tmem_ld32(tm + c, v);
@@ -590,6 +625,49 @@ __global__ void gsplit_reduce_kernel(const float* parts, float* G, int splits, s
   }
 }
 
+// The same reduction writing the Newton-Schulz input (see GradMcOp): one warp
+// per (matrix z, row m, column tile of bn) sums the partials in split order,
+// advances the momentum buffer, writes bf16 (hi, lo) operands and the tile
+// row's sum of squares nsq[(z d + m) nt + tile].
+__global__ void gsplit_reduce_ns_kernel(const float* parts, int splits, int Z, int d, int dh, int bn,
+                                        float* mom, float mu, bf16* Xh, bf16* Xl, float* nsq) {
+  const int lane = threadIdx.x & 31;
+  const int nt = dh / bn;
+  const long long n_rows = (long long)Z * d * nt;
+  const size_t n = (size_t)Z * d * dh;
+  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_rows;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int tile = (int)(w % nt);
+    const long long zm = w / nt;  // z * d + m
+    const size_t row0 = (size_t)zm * dh + (size_t)tile * bn;
+    float ss = 0.f;
+    for (int c = 4 * lane; c < bn; c += 128) {
+      const size_t e = row0 + c;
+      float4 acc = *reinterpret_cast<const float4*>(parts + e);
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 v = *reinterpret_cast<const float4*>(parts + (size_t)sp * n + e);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      if (mom) {
+        float4* mb = reinterpret_cast<float4*>(mom + e);
+        const float4 b = *mb;
+        acc = make_float4(fmaf(mu, b.x, acc.x), fmaf(mu, b.y, acc.y), fmaf(mu, b.z, acc.z), fmaf(mu, b.w, acc.w));
+        *mb = acc;
+      }
+      uint2 h, l;
+      h.x = pack_bf16(acc.x, acc.y);
+      h.y = pack_bf16(acc.z, acc.w);
+      l.x = pack_bf16(bf_rest(acc.x), bf_rest(acc.y));
+      l.y = pack_bf16(bf_rest(acc.z), bf_rest(acc.w));
+      *reinterpret_cast<uint2*>(Xh + e) = h;
+      *reinterpret_cast<uint2*>(Xl + e) = l;
+      ss = fmaf(acc.w, acc.w, fmaf(acc.z, acc.z, fmaf(acc.y, acc.y, fmaf(acc.x, acc.x, ss))));
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) nsq[(size_t)zm * nt + tile] = ss;
+  }
+}
+
 // ============================================================ host side
 
 template <class Op>
@@ -713,6 +791,7 @@ struct Plan {
   int g_bn, g_nt;         //           N tile over dh, N tiles
   int g_splits_max;       // token splits the workspace has room for
   size_t off_mom;         // momentum buffers [Z][d][dh] fp32 (momentum != 0 only)
+  size_t off_nsqg;        // per-row sums of squares of the gradient [Z][d][dh / g_bn] (Muon)
   size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_Sh,
       off_Sl, off_Ph, off_Pl, off_split, off_nsq, total;
 };
@@ -769,6 +848,7 @@ Plan make_plan(const ttt_cfg& g) {
   P.off_split = take(P.g_splits_max > 1 ? (size_t)P.g_splits_max * wz * 4 : 0);
   P.off_nsq = take(ns_fused_scratch_floats(g, P.Z) * 4);
   P.off_mom = take(g.momentum != 0.f ? wz * 4 : 0);
+  P.off_nsqg = take(g.muon ? (size_t)P.Z * g.d * P.g_nt * 4 : 0);
   P.total = off;
   return P;
 }
@@ -779,134 +859,193 @@ bool tc_supported(const ttt_cfg& g) {
   // d <= 1024: the gradient's clusters hold d / 128 <= 8 CTAs
   // (the fused Muon step completes the square of its quintic, so it needs c != 0,
   // and fuses the update into its last iteration, so it needs at least one)
-  return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU && g.loss == TTT_LOSS_IP && g.d % 64 == 0 &&
+  return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU && g.loss == TTT_LOSS_IP &&
+         g.mode != TTT_MODE_INCLUSIVE && g.d % 64 == 0 &&
          g.dh % 128 == 0 && g.d <= g.dh && g.d <= 1024 && g.dh <= 16384 &&
          (!g.muon || (g.ns_c != 0.f && g.ns_iters >= 1));
 }
 
 size_t tc_workspace_bytes(const ttt_cfg& g) { return make_plan(g).total; }
 
-int tc_run(const Call& c) {
-  const ttt_cfg& g = c.cfg;
-  const Plan P = make_plan(g);
-  const bool split = P.split != 0;
-  // which stages carry split operands (all of them unless a test hook narrowed it)
-  const bool split_fwd = split && (g_split_mask & 1);
-  const bool split_grad = split && (g_split_mask & 2);
-  const bool split_ns = split && (g_split_mask & 4);
-  const cudaStream_t st = c.stream;
-  char* ws = c.ws;
-  auto at = [&](size_t off, size_t n) -> void* { return n ? static_cast<void*>(ws + off) : nullptr; };
-  float* M = reinterpret_cast<float*>(ws + P.off_M);
-  bf16* Ms = reinterpret_cast<bf16*>(ws + P.off_Ms);
-  bf16* Msl = split ? reinterpret_cast<bf16*>(ws + P.off_Msl) : nullptr;
-  float* n0 = reinterpret_cast<float*>(ws + P.off_n0);
-  bf16* Hq = reinterpret_cast<bf16*>(ws + P.off_Hq);
-  bf16* E = reinterpret_cast<bf16*>(ws + P.off_E);
-  bf16* El = split ? reinterpret_cast<bf16*>(ws + P.off_El) : nullptr;
-  float* G = reinterpret_cast<float*>(ws + P.off_G);
-  void* Xh[2] = {ws + P.off_Xh[0], ws + P.off_Xh[1]};
-  void* Xl[2] = {at(P.off_Xl[0], split), at(P.off_Xl[1], split)};
-  void* Sh = ws + P.off_Sh;
-  void* Sl = at(P.off_Sl, split);
-  void* Ph = ws + P.off_Ph;
-  void* Pl = at(P.off_Pl, split);
-  float* splitbuf = reinterpret_cast<float*>(ws + P.off_split);
-  float* mom = g.momentum != 0.f ? reinterpret_cast<float*>(ws + P.off_mom) : nullptr;
-  int* status = reinterpret_cast<int*>(ws);
-  const TcCommon cm{status, (unsigned long long)c.cfg.timeout_us * 1000ull};
-  const int d = g.d, dh = g.dh, BH = P.BH, Z = P.Z, T = g.T;
-  const int n_full = T / P.C;
+namespace {
 
-  // ---- tensor maps ([0] = hi or single operand, [1] = lo; lo maps alias hi in SINGLE precision)
-  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4, mW[2], mHq, mW2o, mE[2];
-  bool ok = true;
-  ok &= map3(&mQ, c.Q, d, T, BH, 64, 128);
-  ok &= map3(&mK, c.K, d, T, BH, 64, 128);
-  ok &= map3(&mV, c.V, d, T, BH, 64, 128);
-  ok &= map3(&mK3, c.K, d, T, BH, 64, 32);  // gradient: 32-token boxes
-  ok &= map3(&mV3, c.V, d, T, BH, 64, 32);
-  if (n_full > 0) {
-    // 4D view {d, C, n_full, BH}: a chunk's token range ends at the chunk boundary
-    auto fn = encode_fn();
-    if (!fn) return TTT_ERR_CUDA;
-    CUtensorMap* outs[2] = {&mK4, &mV4};
-    const void* bases[2] = {c.K, c.V};
+// One call's view of the tensor-core path: the workspace plan, the pointers
+// into the workspace, the tensor maps and the launch helpers of each step of a
+// chunk. ttt_fwd drives it chunk by chunk; the context-parallel entry points
+// drive the same steps one at a time.
+class TcLayer {
+ public:
+  int init(const ttt_cfg& g, char* ws, cudaStream_t st) {
+    g_ = g;
+    P = make_plan(g);
+    st_ = st;
+    ws_ = ws;
+    const bool split = P.split != 0;
+    // which stages carry split operands (all of them unless a test hook narrowed it)
+    split_fwd = split && (g_split_mask & 1);
+    split_grad = split && (g_split_mask & 2);
+    split_ns = split && (g_split_mask & 4);
+    auto at = [&](size_t off, bool on) -> void* { return on ? static_cast<void*>(ws + off) : nullptr; };
+    M = reinterpret_cast<float*>(ws + P.off_M);
+    Ms = reinterpret_cast<bf16*>(ws + P.off_Ms);
+    Msl = split ? reinterpret_cast<bf16*>(ws + P.off_Msl) : nullptr;
+    n0 = reinterpret_cast<float*>(ws + P.off_n0);
+    Hq = reinterpret_cast<bf16*>(ws + P.off_Hq);
+    E = reinterpret_cast<bf16*>(ws + P.off_E);
+    El = split ? reinterpret_cast<bf16*>(ws + P.off_El) : nullptr;
+    G = reinterpret_cast<float*>(ws + P.off_G);
+    splitbuf = reinterpret_cast<float*>(ws + P.off_split);
+    mom = g.momentum != 0.f ? reinterpret_cast<float*>(ws + P.off_mom) : nullptr;
+    cm = TcCommon{reinterpret_cast<int*>(ws), (unsigned long long)g.timeout_us * 1000ull, 0};
+    const int d = g.d, dh = g.dh, BH = P.BH, Z = P.Z;
+    bool ok = true;
+    ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
+    ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
+    ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
+    ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
+    ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
+    ok &= map3(&mE[1], split_grad ? El : E, dh, P.Cp, Z, 64, 32);
+    ok &= map3(&sHq, Hq, dh, P.Cp, BH, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= map3(&sE[0], E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= map3(&sE[1], split_grad ? El : E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               CU_TENSOR_MAP_SWIZZLE_64B);
+    nsa = NsFusedArgs{};
+    nsa.cfg = &g_;
+    nsa.Z = Z;
+    nsa.split = split_ns;
+    nsa.X = G;
     for (int i = 0; i < 2; ++i) {
-      cuuint64_t gd[4] = {(cuuint64_t)d, (cuuint64_t)P.C, (cuuint64_t)n_full, (cuuint64_t)BH};
-      cuuint64_t gs[3] = {(cuuint64_t)d * 2, (cuuint64_t)P.C * d * 2, (cuuint64_t)T * d * 2};
-      cuuint32_t bx[4] = {64, 32, 1, 1};
-      cuuint32_t es[4] = {1, 1, 1, 1};
-      ok &= fn(outs[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]), gd, gs, bx, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      nsa.Xh[i] = ws + P.off_Xh[i];
+      nsa.Xl[i] = at(P.off_Xl[i], split);
     }
-  } else {
+    nsa.Rh = ws + P.off_Sh;
+    nsa.Rl = at(P.off_Sl, split);
+    nsa.Ph = ws + P.off_Ph;
+    nsa.Pl = at(P.off_Pl, split);
+    nsa.M = M;
+    nsa.Ms = Ms;
+    nsa.Msl = Msl;
+    nsa.n0 = n0;
+    nsa.scratch = reinterpret_cast<float*>(ws + P.off_nsq);
+    nsa.mom = mom;
+    nsa.mu = g.momentum;
+    nsa.cm = cm;
+    // Newton-Schulz in split precision takes its input straight from the
+    // gradient kernel (operands and partial norms), with no normalise pass
+    fused_ns = g.muon && split_ns;
+    nsqg = reinterpret_cast<float*>(ws + P.off_nsqg);
+    return ok ? TTT_OK : TTT_ERR_CUDA;
+  }
+
+  // Token tensors of the following steps: [B, H, T, d] (lr [B, H, T(, 3)]);
+  // any of them may be NULL when no step reads it.
+  int bind_tokens(const void* Q, const void* K, const void* V, const float* lr, void* O, int T) {
+    const int d = g_.d, BH = P.BH;
+    T_ = T;
+    lr_ = lr;
+    O_ = O;
+    n_full = P.C > 0 ? T / P.C : 0;
+    bool ok = true;
+    if (Q) ok &= map3(&mQ, Q, d, T, BH, 64, 128);
+    if (K) {
+      ok &= map3(&mK, K, d, T, BH, 64, 128);
+      ok &= map3(&mK3, K, d, T, BH, 64, 32);  // gradient: 32-token boxes
+    }
+    if (V) {
+      ok &= map3(&mV, V, d, T, BH, 64, 128);
+      ok &= map3(&mV3, V, d, T, BH, 64, 32);
+    }
     mK4 = mK3;
     mV4 = mV3;
+    if (K && V && n_full > 0) {
+      // 4D view {d, C, n_full, BH}: a chunk's token range ends at the chunk boundary
+      auto fn = encode_fn();
+      if (!fn) return TTT_ERR_CUDA;
+      CUtensorMap* outs[2] = {&mK4, &mV4};
+      const void* bases[2] = {K, V};
+      for (int i = 0; i < 2; ++i) {
+        cuuint64_t gd[4] = {(cuuint64_t)d, (cuuint64_t)P.C, (cuuint64_t)n_full, (cuuint64_t)BH};
+        cuuint64_t gs[3] = {(cuuint64_t)d * 2, (cuuint64_t)P.C * d * 2, (cuuint64_t)T * d * 2};
+        cuuint32_t bx[4] = {64, 32, 1, 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        ok &= fn(outs[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]), gd, gs, bx, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      }
+    }
+    return ok ? TTT_OK : TTT_ERR_CUDA;
   }
-  ok &= map3(&mW[0], Ms, dh, d, Z, 64, 64);
-  ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
-  ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
-  ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
-  ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
-  ok &= map3(&mE[1], split_grad ? El : E, dh, P.Cp, Z, 64, 32);
-  CUtensorMap sHq, sE[2];
-  ok &= map3(&sHq, Hq, dh, P.Cp, BH, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= map3(&sE[0], E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= map3(&sE[1], split_grad ? El : E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-             CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!ok) return TTT_ERR_CUDA;
 
-  int rc;
-  // ---- import W0, reference row norms; momentum buffers start at zero
-  if (mom && cudaMemsetAsync(mom, 0, (size_t)Z * d * dh * sizeof(float), st) != cudaSuccess) return TTT_ERR_CUDA;
-  {
+  // W0 -> master weights, bf16 shadows and reference row norms; momentum buffers start at zero.
+  int import_w0(const float* const W0[3]) {
+    const int d = g_.d, dh = g_.dh, Z = P.Z;
+    cudaStream_t st = st_;
+    if (mom && cudaMemsetAsync(mom, 0, (size_t)Z * d * dh * sizeof(float), st) != cudaSuccess) return TTT_ERR_CUDA;
     const dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
     TTT_LAUNCH(TTT_KERNEL_AUX, st,
-               import_kernel<<<grid, 256, 0, st>>>(c.W0[0], c.W0[1], c.W0[2], M, Ms, Msl, g.H, d, dh,
-                                                   g.w0_per_batch));
+               import_kernel<<<grid, 256, 0, st>>>(W0[0], W0[1], W0[2], M, Ms, Msl, g_.H, d, dh, g_.w0_per_batch));
     const dim3 gn(std::max((dh + 31) / 32, (d + 7) / 8), Z);
     TTT_LAUNCH(TTT_KERNEL_AUX, st, norms_kernel<<<gn, 256, 0, st>>>(M, n0, d, dh));
+    return TTT_OK;
   }
 
-  auto run_fwd = [&](int s, int valid, bool q, bool k) -> int {
+  int export_w(float* const Wf[3]) {
+    const int d = g_.d, dh = g_.dh;
+    cudaStream_t st = st_;
+    const dim3 grid((dh + 31) / 32, (d + 31) / 32, P.Z);
+    TTT_LAUNCH(TTT_KERNEL_AUX, st, export_kernel<<<grid, 256, 0, st>>>(M, Wf[0], Wf[1], Wf[2], d, dh));
+    return TTT_OK;
+  }
+
+  // Forward of tokens [s, s + valid): query tiles (H_q) and/or key tiles (E).
+  int fwd(int s, int valid, bool q, bool k) {
     FwdMcOp::Params p{};
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
-    p.lr = c.lr; p.Hq = Hq; p.E = E; p.El = El;
-    p.lr_stride = g.lr_per_matrix ? 3 : 1;
-    p.d = d; p.dh = dh; p.T = T; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
+    p.lr = lr_; p.Hq = Hq; p.E = E; p.El = El;
+    p.lr_stride = g_.lr_per_matrix ? 3 : 1;
+    p.d = g_.d; p.dh = g_.dh; p.T = T_; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
     p.n_tok = (valid + BM - 1) / BM;
     // pairs of consecutive token tiles share each weight slice by multicast:
     // clusters of two fill all 148 SMs (clusters of four leave 16 idle); the
     // build without multicast runs clusters of one
     p.cs = (TTT_HAS_MULTICAST && p.n_tok >= 2) ? 2 : 1;
     p.groups = (p.n_tok + p.cs - 1) / p.cs;
-    p.n_js = dh / 64;
-    p.BH = BH;
+    p.n_js = g_.dh / 64;
+    p.BH = P.BH;
     p.q = q ? 1 : 0;
     p.k = k ? 1 : 0;
     p.w_split = split_fwd ? 1 : 0;
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
     p.cm.stall = g_stall_next_fwd.exchange(0);
-    const int n_work = BH * p.n_js * p.groups * (p.q + p.k);
-    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st);
-  };
-  auto run_o = [&](int s, int valid, cudaStream_t os) -> int {
+    const int n_work = P.BH * p.n_js * p.groups * (p.q + p.k);
+    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
+  }
+
+  // O[s, s + valid) = H_q W2^T on stream `os`.
+  int apply(int s, int valid, cudaStream_t os) {
+    const int d = g_.d;
     const int mt = (valid + BM - 1) / BM, nt = (d + P.bn_o - 1) / P.bn_o;
     auto fill = [&](auto& p) {
-      p.mH = mHq; p.mW2 = mW2o; p.O = static_cast<bf16*>(c.O);
-      p.d = d; p.dh = dh; p.T = T; p.chunk_start = s; p.valid = valid; p.m_tiles = mt; p.n_tiles = nt; p.cm = cm;
+      p.mH = mHq; p.mW2 = mW2o; p.O = static_cast<bf16*>(O_);
+      p.d = d; p.dh = g_.dh; p.T = T_; p.chunk_start = s; p.valid = valid; p.m_tiles = mt; p.n_tiles = nt;
+      p.cm = cm;
     };
-    const dim3 grid(mt * nt, BH);
+    const dim3 grid(mt * nt, P.BH);
     if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(TTT_KERNEL_APPLY, p, grid, os); }
     if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, os); }
     typename OOp<128>::Params p{}; fill(p); return launch_op<OOp<128>>(TTT_KERNEL_APPLY, p, grid, os);
-  };
-  auto run_grad = [&](int ci, int s, int valid) -> int {
-    const bool full = (s + P.C <= T) && ci < n_full;
+  }
+
+  // Chunk gradient of tokens [s, s + valid) (chunk ci) from E into `out`
+  // ([Z][d][dh] fp32), or, when out is NULL: into the workspace's G, or (fused
+  // Newton-Schulz) straight into the Muon step's input operands.
+  int grad(int ci, int s, int valid, float* out = nullptr) {
+    const int d = g_.d, dh = g_.dh, Z = P.Z;
+    float* dst = out ? out : G;
+    const bool to_ns = !out && fused_ns;
+    const bool full = n_full > 0 && (s + P.C <= T_) && ci < n_full && s == ci * P.C;
     const int kbs = (valid + 31) / 32;  // 32-token k-blocks
     const int items = Z * P.g_nt * P.g_mg;
     auto launch = [&](auto op) -> int {
@@ -918,41 +1057,89 @@ int tc_run(const Call& c) {
       splits = (kbs + kb_per_split - 1) / kb_per_split;
       typename Op::Params p{};
       p.mK4 = mK4; p.mV4 = mV4; p.mK3 = mK3; p.mV3 = mV3; p.mE = mE[0]; p.mEl = mE[1];
-      p.G = G; p.split_out = splitbuf;
+      p.G = dst; p.split_out = splitbuf;
       p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
       p.nt = P.g_nt; p.splits = splits; p.kb_per_split = kb_per_split; p.e_split = split_grad ? 1 : 0; p.cm = cm;
       p.mg = P.g_mg; p.cs = P.g_cs;
-      const int r = launch_mc<Op>(TTT_KERNEL_GRAD, p, P.g_cs, items * splits, st);
+      if (to_ns) {
+        p.Xh = static_cast<bf16*>(nsa.Xh[0]);
+        p.Xl = static_cast<bf16*>(nsa.Xl[0]);
+        p.mom = mom;
+        p.mu = g_.momentum;
+        p.nsq = nsqg;
+      }
+      const int r = launch_mc<Op>(TTT_KERNEL_GRAD, p, P.g_cs, items * splits, st_);
       if (r != TTT_OK || splits == 1) return r;
       const size_t n = (size_t)Z * d * dh;
-      TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, G, splits, n));
+      cudaStream_t st = st_;
+      if (to_ns) {
+        TTT_LAUNCH(TTT_KERNEL_GRAD, st,
+                   gsplit_reduce_ns_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(
+                       splitbuf, splits, Z, d, dh, P.g_bn, mom, g_.momentum, static_cast<bf16*>(nsa.Xh[0]),
+                       static_cast<bf16*>(nsa.Xl[0]), nsqg));
+        return TTT_OK;
+      }
+      TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, dst, splits, n));
       return TTT_OK;
     };
     return P.g_bn == 256 ? launch(GradMcOp<256>{}) : launch(GradMcOp<128>{});
-  };
-  auto run_update = [&]() -> int {
-    const dim3 grid(std::max((dh + 31) / 32, (d + 7) / 8), Z);
+  }
+
+  // The update from the gradient `u` ([Z][d][dh] fp32; the workspace's G when
+  // NULL): Muon + update + weight norm in one launch, or without Muon the
+  // plain update + weight norm.
+  int step(const float* u = nullptr) {
+    const int d = g_.d, dh = g_.dh;
+    const float* src = u ? u : G;
+    if (g_.muon) {
+      NsFusedArgs a = nsa;
+      a.X = const_cast<float*>(src);
+      if (!u && fused_ns) {
+        // the gradient kernel wrote the operands and advanced the momentum
+        a.fused = true;
+        a.nsqg = nsqg;
+        a.nsq_n = g_.d * P.g_nt;
+        a.mom = nullptr;
+      }
+      return ns_fused_run(a, st_);
+    }
+    cudaStream_t st = st_;
+    const dim3 grid(std::max((dh + 31) / 32, (d + 7) / 8), P.Z);
     TTT_LAUNCH(TTT_KERNEL_UPDATE, st,
-               update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, G, mom, g.momentum, n0, g.step, g.wnorm,
-                                                   g.wnorm_eps, d, dh));
+               update_kernel<<<grid, 256, 0, st>>>(M, Ms, Msl, src, mom, g_.momentum, n0, g_.step, g_.wnorm,
+                                                   g_.wnorm_eps, d, dh));
     return TTT_OK;
-  };
-  NsFusedArgs nsa{};
-  nsa.cfg = &c.cfg; nsa.Z = Z; nsa.split = split_ns; nsa.X = G;
-  for (int i = 0; i < 2; ++i) { nsa.Xh[i] = Xh[i]; nsa.Xl[i] = Xl[i]; }
-  nsa.Rh = Sh; nsa.Rl = Sl; nsa.Ph = Ph; nsa.Pl = Pl;
-  nsa.M = M; nsa.Ms = Ms; nsa.Msl = Msl; nsa.n0 = n0;
-  nsa.scratch = reinterpret_cast<float*>(ws + P.off_nsq);
-  nsa.mom = mom;
-  nsa.mu = g.momentum;
-  nsa.cm = cm;
-  // update: gradient, then Muon + update + weight norm in one launch (or, without
-  // Muon, the plain update + weight norm)
-  auto do_update = [&](int ci, int s, int valid) -> int {
-    const int r = run_grad(ci, s, valid);
-    if (r != TTT_OK) return r;
-    return g.muon ? ns_fused_run(nsa, st) : run_update();
-  };
+  }
+
+  Plan P;
+
+ private:
+  ttt_cfg g_;
+  cudaStream_t st_;
+  char* ws_;
+  bool split_fwd, split_grad, split_ns, fused_ns;
+  float *M, *n0, *G, *splitbuf, *mom, *nsqg;
+  bf16 *Ms, *Msl, *Hq, *E, *El;
+  TcCommon cm;
+  NsFusedArgs nsa;
+  CUtensorMap mW[2], mHq, mW2o, mE[2], sHq, sE[2];
+  CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4;
+  const float* lr_ = nullptr;
+  void* O_ = nullptr;
+  int T_ = 0, n_full = 0;
+};
+
+}  // namespace
+
+int tc_run(const Call& c) {
+  const ttt_cfg& g = c.cfg;
+  TcLayer L;
+  int rc = L.init(g, c.ws, c.stream);
+  if (rc == TTT_OK) rc = L.bind_tokens(c.Q, c.K, c.V, c.lr, c.O, g.T);
+  if (rc == TTT_OK) rc = L.import_w0(c.W0);
+  if (rc != TTT_OK) return rc;
+  const cudaStream_t st = c.stream;
+  const int T = g.T;
 
   // In shifted mode the apply of a chunk (O = H_q W2^T) and its gradient are
   // independent: the apply runs on a side stream between the forward and the
@@ -964,42 +1151,141 @@ int tc_run(const Call& c) {
     const bool upd = call_updates(c, ci);
     if (c.chunk_ready && cudaStreamWaitEvent(st, c.chunk_ready[ci], 0) != cudaSuccess) return TTT_ERR_CUDA;
     if (g.mode == TTT_MODE_SHIFTED) {
-      rc = run_fwd(s, valid, true, upd);
+      rc = L.fwd(s, valid, true, upd);
       if (rc == TTT_OK && upd && side) {
         cudaStream_t os = side->stream;
         if (cudaEventRecord(side->fwd_done, st) != cudaSuccess || cudaStreamWaitEvent(os, side->fwd_done, 0) != cudaSuccess)
           return TTT_ERR_CUDA;
-        rc = run_o(s, valid, os);
+        rc = L.apply(s, valid, os);
         if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], os) != cudaSuccess) rc = TTT_ERR_CUDA;
         if (rc == TTT_OK && cudaEventRecord(side->apply_done, os) != cudaSuccess) rc = TTT_ERR_CUDA;
-        if (rc == TTT_OK) rc = run_grad(ci, s, valid);
+        if (rc == TTT_OK) rc = L.grad(ci, s, valid);
         if (rc == TTT_OK && cudaStreamWaitEvent(st, side->apply_done, 0) != cudaSuccess) rc = TTT_ERR_CUDA;
-        if (rc == TTT_OK) rc = g.muon ? ns_fused_run(nsa, st) : run_update();
+        if (rc == TTT_OK) rc = L.step();
       } else {
-        if (rc == TTT_OK) rc = run_o(s, valid, st);
+        if (rc == TTT_OK) rc = L.apply(s, valid, st);
         if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], st) != cudaSuccess) rc = TTT_ERR_CUDA;
-        if (rc == TTT_OK && upd) rc = do_update(ci, s, valid);
+        if (rc == TTT_OK && upd) rc = L.grad(ci, s, valid);
+        if (rc == TTT_OK && upd) rc = L.step();
       }
     } else {
       rc = TTT_OK;
       if (upd) {
-        rc = run_fwd(s, valid, false, true);
-        if (rc == TTT_OK) rc = do_update(ci, s, valid);
+        rc = L.fwd(s, valid, false, true);
+        if (rc == TTT_OK) rc = L.grad(ci, s, valid);
+        if (rc == TTT_OK) rc = L.step();
       }
-      if (rc == TTT_OK) rc = run_fwd(s, valid, true, false);
-      if (rc == TTT_OK) rc = run_o(s, valid, st);
+      if (rc == TTT_OK) rc = L.fwd(s, valid, true, false);
+      if (rc == TTT_OK) rc = L.apply(s, valid, st);
       if (rc == TTT_OK && c.chunk_done && cudaEventRecord(c.chunk_done[ci], st) != cudaSuccess) rc = TTT_ERR_CUDA;
     }
     if (rc != TTT_OK) return rc;
   }
-  {
-    const dim3 grid((dh + 31) / 32, (d + 31) / 32, Z);
-    TTT_LAUNCH(TTT_KERNEL_AUX, st, export_kernel<<<grid, 256, 0, st>>>(M, c.Wf[0], c.Wf[1], c.Wf[2], d, dh));
-  }
+  return L.export_w(c.Wf);
+}
+
+// ============================================================ context parallelism
+namespace {
+
+bool cp_aligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by the context-parallel calls; on success `L` is ready on the workspace.
+int cp_open(const ttt_cfg* cfg, void* ws, size_t ws_bytes, void* stream, TcLayer& L) {
+  int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  if (cfg->impl != TTT_IMPL_AUTO && cfg->impl != TTT_IMPL_TC) return TTT_ERR_UNSUPPORTED;
+  if (!tc_supported(*cfg)) return TTT_ERR_UNSUPPORTED;
+  if (cfg->T < cfg->chunk) return TTT_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < tc_workspace_bytes(*cfg)) return TTT_ERR_WORKSPACE;
+  const void* p[1] = {ws};
+  v = check_device_ptrs(p, 1);
+  if (v != TTT_OK) return v;
+  ttt_cfg g = *cfg;
+  if (g.timeout_us == 0) g.timeout_us = 2000000u;
+  return L.init(g, static_cast<char*>(ws), static_cast<cudaStream_t>(stream));
+}
+
+int cp_range_ok(const ttt_cfg* cfg, int T_all, int start, int n) {
+  return (start >= 0 && n >= 1 && n <= cfg->chunk && T_all >= 1 && (int64_t)start + n <= T_all) ? TTT_OK : TTT_ERR_ARG;
+}
+
+}  // namespace
+}  // namespace ttt
+
+using namespace ttt;
+
+extern "C" int ttt_cp_workspace_bytes(const ttt_cfg* cfg, size_t* bytes) {
+  if (!bytes || validate_cfg(cfg) != TTT_OK) return TTT_ERR_ARG;
+  if ((cfg->impl != TTT_IMPL_AUTO && cfg->impl != TTT_IMPL_TC) || !tc_supported(*cfg)) return TTT_ERR_UNSUPPORTED;
+  if (cfg->T < cfg->chunk) return TTT_ERR_ARG;
+  *bytes = tc_workspace_bytes(*cfg);
   return TTT_OK;
 }
 
-}  // namespace ttt
+extern "C" int ttt_cp_begin(const ttt_cfg* cfg, const float* W0_1, const float* W0_2, const float* W0_3,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  TcLayer L;
+  if (!cp_aligned(W0_1) || !cp_aligned(W0_2) || !cp_aligned(W0_3)) return TTT_ERR_ARG;
+  int rc = cp_open(cfg, workspace, workspace_bytes, stream, L);
+  if (rc != TTT_OK) return rc;
+  const void* p[3] = {W0_1, W0_2, W0_3};
+  rc = check_device_ptrs(p, 3);
+  if (rc != TTT_OK) return rc;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTT_ERR_CUDA;
+  const float* w0[3] = {W0_1, W0_2, W0_3};
+  return L.import_w0(w0);
+}
+
+extern "C" int ttt_cp_grad(const ttt_cfg* cfg, const void* K, const void* V, const float* lr, int T_all, int start,
+                           int n, float* G, void* workspace, size_t workspace_bytes, void* stream) {
+  TcLayer L;
+  if (!cp_aligned(K) || !cp_aligned(V) || !cp_aligned(lr) || !cp_aligned(G)) return TTT_ERR_ARG;
+  int rc = cp_open(cfg, workspace, workspace_bytes, stream, L);
+  if (rc != TTT_OK) return rc;
+  if ((rc = cp_range_ok(cfg, T_all, start, n)) != TTT_OK) return rc;
+  const void* p[4] = {K, V, lr, G};
+  if ((rc = check_device_ptrs(p, 4)) != TTT_OK) return rc;
+  if ((rc = L.bind_tokens(nullptr, K, V, lr, nullptr, T_all)) != TTT_OK) return rc;
+  if ((rc = L.fwd(start, n, false, true)) != TTT_OK) return rc;
+  return L.grad(start == 0 ? 0 : -1, start, n, G);
+}
+
+extern "C" int ttt_cp_update(const ttt_cfg* cfg, const float* G, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  TcLayer L;
+  if (!cp_aligned(G)) return TTT_ERR_ARG;
+  int rc = cp_open(cfg, workspace, workspace_bytes, stream, L);
+  if (rc != TTT_OK) return rc;
+  const void* p[1] = {G};
+  if ((rc = check_device_ptrs(p, 1)) != TTT_OK) return rc;
+  return L.step(G);
+}
+
+extern "C" int ttt_cp_apply(const ttt_cfg* cfg, const void* Q, int T_all, int start, int n, void* O,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  TcLayer L;
+  if (!cp_aligned(Q) || !cp_aligned(O)) return TTT_ERR_ARG;
+  int rc = cp_open(cfg, workspace, workspace_bytes, stream, L);
+  if (rc != TTT_OK) return rc;
+  if ((rc = cp_range_ok(cfg, T_all, start, n)) != TTT_OK) return rc;
+  const void* p[2] = {Q, O};
+  if ((rc = check_device_ptrs(p, 2)) != TTT_OK) return rc;
+  if ((rc = L.bind_tokens(Q, nullptr, nullptr, nullptr, O, T_all)) != TTT_OK) return rc;
+  if ((rc = L.fwd(start, n, true, false)) != TTT_OK) return rc;
+  return L.apply(start, n, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ttt_cp_end(const ttt_cfg* cfg, float* Wf_1, float* Wf_2, float* Wf_3, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  TcLayer L;
+  if (!cp_aligned(Wf_1) || !cp_aligned(Wf_2) || !cp_aligned(Wf_3)) return TTT_ERR_ARG;
+  int rc = cp_open(cfg, workspace, workspace_bytes, stream, L);
+  if (rc != TTT_OK) return rc;
+  const void* p[3] = {Wf_1, Wf_2, Wf_3};
+  if ((rc = check_device_ptrs(p, 3)) != TTT_OK) return rc;
+  float* wf[3] = {Wf_1, Wf_2, Wf_3};
+  return L.export_w(wf);
+}
 
 // ============================================================ test hooks
 extern "C" int ttt_dbg_ns_plan(const ttt_cfg* cfg, int* grid, int* resident) {

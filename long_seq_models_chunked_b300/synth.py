@@ -52,7 +52,7 @@ class LayerSpec:
     chunk: int
     fast_net: str = "swiglu"   # "swiglu" | "linear"
     loss: str = "ip"           # "ip" (-f(k).v) | "mse" (1/2 ||f(k)-v||^2)
-    mode: str = "shifted"      # "shifted" | "single" (update-then-apply per chunk)
+    mode: str = "shifted"      # "shifted" | "single" (update-then-apply per chunk) | "inclusive"
     dtype: str = "bf16"        # storage type of Q, K, V, O: "bf16" | "fp32"
     muon: bool = True
     ns_iters: int = 5

@@ -34,6 +34,16 @@ CASES = {
                                         lr_per_matrix=True, T=230, chunk=48, update="odd", seed=42),
     "linear_momentum": synth.WORKLOADS["linear_chunk64"].replace(
         name="linear_momentum", B=1, H=2, T=512, dtype="fp32", momentum=0.9, lr_per_matrix=True, seed=43),
+    # inclusive order (tutorial page §3): each query sees its own token's update
+    "inclusive_mse": TINY.replace(name="inclusive_mse", mode="inclusive", loss="mse", wnorm=False, seed=44),
+    "inclusive_ip_rates": TINY.replace(name="inclusive_ip_rates", mode="inclusive", wnorm=False,
+                                       lr_per_matrix=True, T=230, chunk=48, update="odd", seed=45),
+    "inclusive_chunk1": TINY.replace(name="inclusive_chunk1", mode="inclusive", wnorm=False, loss="mse",
+                                     T=40, chunk=1, seed=46),
+    "inclusive_block_tail": TINY.replace(name="inclusive_block_tail", mode="inclusive", wnorm=False, T=300,
+                                         chunk=150, step=0.5, seed=47),   # blocks of 64 inside a chunk
+    "inclusive_linear": synth.WORKLOADS["linear_chunk64"].replace(
+        name="inclusive_linear", B=2, H=2, T=512, dtype="fp32", mode="inclusive", seed=48),
 }
 
 
@@ -42,6 +52,14 @@ def test_simt_fp32_matches_oracle(name):
     spec = CASES[name]
     x = synth.layer_inputs(spec)
     compare(spec, run_gpu(spec, x, impl=SIMT), run_oracle(spec, x), 1e-4)
+
+
+def test_simt_inclusive_bf16_linear_workload_heads():
+    """The small-chunk linear workload's shape (64 x 64 weights, chunks of 64,
+    MSE) in the inclusive order, bf16 storage, sampled heads against the oracle."""
+    from parity import full_workload_check
+    spec = synth.WORKLOADS["linear_chunk64"].replace(name="inclusive_lin_wl", B=2, H=4, T=2048, mode="inclusive")
+    full_workload_check(spec, [(0, 0), (1, 3)], 2e-2, impl=SIMT)
 
 
 def test_simt_bf16_storage_matches_oracle():

@@ -1,7 +1,6 @@
-"""The tcgen05/TMEM/TMA tile kernels in isolation: the one-CTA tile kernel (test
-hook ttt_dbg_gemm_bf16) in every operand orientation, and the CTA-pair
-(cta_group::2) tiles of ttt_dbg_gemm_pair_bf16 with the Newton-Schulz operand
-layouts, each against an fp64 product of the same bf16 values."""
+"""The tcgen05/TMEM/TMA tile kernel in isolation: the one-CTA tile kernel (test
+hook ttt_dbg_gemm_bf16) in every operand orientation, against an fp64 product
+of the same bf16 values."""
 import pytest
 import torch
 
@@ -22,21 +21,5 @@ def test_tile_kernel_matches_fp64(a_mn, b_mn, Z, M, N, K):
     D = torch.full((Z, M, N), float("nan"), dtype=torch.float32, device="cuda")
     assert abi.ttt_dbg_gemm_bf16(Ad, a_mn, Bd, b_mn, D, Z, M, N, K) == 0
     torch.cuda.synchronize()
-    err = (D.double().cpu() - ref).abs().max().item() / ref.abs().max().item()
-    assert err < 1e-5, err
-
-
-@pytest.mark.parametrize("b_mn", [False, True])
-@pytest.mark.parametrize("Z,M,N,K", [(1, 256, 256, 32), (2, 512, 768, 320), (5, 256, 512, 1024)])
-def test_pair_tiles_match_fp64(b_mn, Z, M, N, K):
-    from long_seq_models_chunked_b300 import abi
-    g = torch.Generator(device="cpu").manual_seed(M * 5 + N * 3 + K + 7 * b_mn)
-    A = torch.randn(Z, M, K, generator=g).to(torch.bfloat16)
-    B = torch.randn(Z, N, K, generator=g).to(torch.bfloat16)
-    ref = torch.bmm(A.double(), B.double().transpose(1, 2))
-    Ad = A.contiguous().cuda()
-    Bd = (B.transpose(1, 2) if b_mn else B).contiguous().cuda()
-    D = torch.full((Z, M, N), float("nan"), dtype=torch.float32, device="cuda")
-    assert abi.ttt_dbg_gemm_pair_bf16(Ad, Bd, b_mn, D, Z, M, N, K) == 0
     err = (D.double().cpu() - ref).abs().max().item() / ref.abs().max().item()
     assert err < 1e-5, err

@@ -29,7 +29,7 @@ CASES = {
                                  lr_a=0.005, seed=45),
     "multi_head_batch": BASE.replace(name="multi_head_batch", B=2, H=3, d=128, dh=256, T=384, seed=46),
     "long_small": BASE.replace(name="long_small", T=2048, chunk=128, seed=48),   # 16 updates
-    # d and dh multiples of 256: Newton-Schulz on CTA-pair (cta_group::2) tiles
+    # d and dh multiples of 256: 256-wide Newton-Schulz tiles
     "pair_d256": BASE.replace(name="pair_d256", B=2, H=2, d=256, dh=512, T=1024, chunk=256, seed=49),
     # degenerate cases: no chunk updates (O is the plain SwiGLU MLP of W0, Wf = W0),
     # and every learning rate zero (G = 0: Newton-Schulz of a zero matrix is zero)
@@ -108,28 +108,59 @@ def test_tc_is_deterministic():
     assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
 
 
-def test_muon_on_cta_pairs_matches_oracle():
-    """The Muon step's GEMM phases on CTA-pair tiles (cta_group::2, off by
-    default; taken when d and dh are multiples of 256), with the update fused
-    into the last X update: parity with the oracle, on a small case and on the
-    lm workload's shapes."""
+@pytest.mark.parametrize("ctas", [5, 37])
+def test_muon_on_a_small_grid_matches_oracle(ctas):
+    """The fused Muon kernel's item list on a grid far smaller than its items
+    (each CTA walks many items of every phase, waiting on other CTAs' matrix
+    counters): parity with the oracle on a small case and on the lm workload's
+    shapes."""
     spec = CASES["pair_d256"]
     x = synth.layer_inputs(spec)
     lm = synth.WORKLOADS["lm_chunk2k"].replace(T=4096)
     try:
-        abi.ttt_dbg_ns_pairs(True)
+        abi.ttt_dbg_ns_force_grid(ctas)
         got = run_gpu(spec, x, impl=TC)
         full_workload_check(lm, [(0, 0), (lm.B - 1, lm.H - 1)], TOL, impl=TC)
     finally:
-        abi.ttt_dbg_ns_pairs(False)
+        abi.ttt_dbg_ns_force_grid(0)
     compare(spec, got, run_oracle(spec, x), TOL)
 
 
-@pytest.mark.parametrize("hook", ["fwd", "ns_barrier"])
+@pytest.mark.parametrize("sym", [0, 1])
+@pytest.mark.parametrize("name", ["small_muon", "d192_split_k", "pair_d256", "small_odd_ragged", "momentum_muon"])
+def test_muon_tile_sets_match_oracle(name, sym):
+    """The fused Muon kernel with every tile of R = X X^T + beta I and
+    P = c R^2 + alpha I computed (0), or only the tiles that meet the upper
+    triangle, the missing lower blocks written as transposes (1); the default
+    picks one by the shape."""
+    spec = CASES[name]
+    x = synth.layer_inputs(spec)
+    try:
+        abi.ttt_dbg_ns_symmetric(sym)
+        got = run_gpu(spec, x, impl=TC)
+    finally:
+        abi.ttt_dbg_ns_symmetric(-1)
+    compare(spec, got, run_oracle(spec, x), TOL)
+
+
+def test_muon_split_mask_without_fused_normalisation():
+    """With Newton-Schulz on single fp16 operands (precision-study hook), the
+    Muon kernel normalises the fp32 gradient itself (its normalise phases);
+    the short lm shape stays within the tolerance."""
+    lm = synth.WORKLOADS["lm_chunk2k"].replace(T=4096)
+    try:
+        abi.ttt_dbg_split_mask(3)
+        full_workload_check(lm, [(0, 0)], TOL, impl=TC)
+    finally:
+        abi.ttt_dbg_split_mask(7)
+
+
+@pytest.mark.parametrize("hook", ["fwd", "ns"])
 def test_bounded_wait_reports_timeout_and_the_next_call_succeeds(hook):
     """Failure detection without a GPU fault: the tensor-core forward withholds
     its loads (its MMA warp's mbarrier wait runs out), or one CTA of the fused
-    Muon kernel never arrives at a grid barrier (every CTA's wait runs out).
+    Muon kernel never signals an item's completion (the waits of the items that
+    need it run out).
     The status word says TTT_ERR_TIMEOUT, the context stays usable, and the
     next call matches the oracle."""
     import torch
@@ -138,7 +169,7 @@ def test_bounded_wait_reports_timeout_and_the_next_call_succeeds(hook):
     x = synth.layer_inputs(spec)
     dev = to_device(x, spec)
     holder = abi.cfg_from_spec(spec, impl=TC, timeout_us=20000)
-    (abi.ttt_dbg_stall_next_fwd if hook == "fwd" else abi.ttt_dbg_stall_next_ns_barrier)()
+    (abi.ttt_dbg_stall_next_fwd if hook == "fwd" else abi.ttt_dbg_stall_next_ns)()
     with pytest.raises(abi.TTTError) as err:
         abi.layer(holder, dev["Q"], dev["K"], dev["V"], dev["lr"], dev["W0"])
     assert err.value.code == abi.TTT_ERR_TIMEOUT
