@@ -323,3 +323,59 @@ def ttt_layer(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.ndarray,
     Wf = [np.stack([np.stack([out[(b, h)][1][j] for h in range(Hn)]) for b in range(Bn)])
           for j in range(len(W0))]
     return O, Wf
+
+
+# ------------------------------------------------------------------ backward (outer loop)
+def linear_head_backward(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.ndarray, lr: np.ndarray,
+                         W0: np.ndarray, dO: np.ndarray, dWf: np.ndarray):
+    """Gradients of a scalar loss L through the layer on one head, given
+    dL/dO (dO) and dL/dW_final (dWf): returns (dQ, dK, dV, dlr, dW0).
+
+    The outer loop of the TTT-E2E news page (§2.2: the model's loss is
+    differentiated through the inner updates), for the linear net with plain
+    gradient steps in shifted mode (the small-chunk regime). Per chunk c of
+    tokens t: o_t = W_c q_t; y_t = W_c k_t - v_t (MSE) or -v_t (inner product);
+    W_{c+1} = W_c - step * sum_t lr_t y_t k_t^T. Reverse mode, chunk by chunk
+    from the last, with L_c = dL/dW_c:
+      L_c = L_{c+1} + sum_t dO_t q_t^T + [MSE] sum_t e_t k_t^T,
+      with a_t = -step L_{c+1} k_t (the cotangent of lr_t y_t) and e_t = lr_t a_t;
+      dq_t = W_c^T dO_t;  dlr_t = y_t . a_t;  dv_t = -e_t;
+      dk_t = -step L_{c+1}^T (lr_t y_t) + [MSE] W_c^T e_t.
+    """
+    if cfg.fast_net != "linear" or cfg.muon or cfg.wnorm or cfg.momentum != 0.0 or cfg.mode != "shifted":
+        raise ValueError("the backward covers the linear net, plain steps, shifted mode")
+    T = Q.shape[0]
+    C = cfg.chunk
+    n = (T + C - 1) // C
+    mask = cfg.mask if cfg.mask is not None else [1] * n
+    lr = np.asarray(lr, dtype=np.float64)
+    # forward, keeping every chunk's starting weights
+    Ws = [np.asarray(W0, dtype=np.float64)]
+    for ci in range(n):
+        s, e = ci * C, min(T, (ci + 1) * C)
+        W = Ws[-1]
+        if mask[ci]:
+            Y = (K[s:e] @ W.T - V[s:e]) if cfg.loss == "mse" else -V[s:e]
+            W = W - cfg.step * (lr[s:e, None] * Y).T @ K[s:e]
+        Ws.append(W)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dlr = np.zeros(T)
+    Lnext = np.asarray(dWf, dtype=np.float64).copy()   # dL/dW_{c+1}
+    for ci in reversed(range(n)):
+        s, e = ci * C, min(T, (ci + 1) * C)
+        W = Ws[ci]
+        Lc = Lnext.copy()
+        dQ[s:e] = dO[s:e] @ W
+        Lc += dO[s:e].T @ Q[s:e]
+        if mask[ci]:
+            Y = (K[s:e] @ W.T - V[s:e]) if cfg.loss == "mse" else -V[s:e]
+            A = -cfg.step * K[s:e] @ Lnext.T                  # rows a_t = -step L_{c+1} k_t
+            dlr[s:e] = (Y * A).sum(axis=1)
+            E = lr[s:e, None] * A                             # rows e_t: cotangents of y_t
+            dV[s:e] = -E
+            dK[s:e] = -cfg.step * (lr[s:e, None] * Y) @ Lnext
+            if cfg.loss == "mse":
+                dK[s:e] += E @ W
+                Lc += E.T @ K[s:e]
+        Lnext = Lc
+    return dQ, dK, dV, dlr, Lnext

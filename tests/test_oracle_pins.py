@@ -570,3 +570,64 @@ def test_inclusive_mode_refuses_chunk_level_optimisers():
     X = rng.standard_normal((8, 4))
     with pytest.raises(ValueError):
         orc.ttt_head(cfg, X, X, X, np.ones(8), W)
+
+
+def test_zero_rate_target_views_never_change_the_weights():
+    """Novel-view synthesis (LaCT page §3.1): one chunk over a set of views in
+    which the target views only query. Their tokens carry rate 0, so whatever
+    their keys and values, the weights (and so every output) are those of the
+    input views alone."""
+    rng = np.random.default_rng(36)
+    d, dh, T = 5, 8, 48
+    W = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    target = (np.arange(T) // 6) % 4 == 3           # every fourth view of 6 tokens
+    eta = np.where(target, 0.0, rng.uniform(0, 0.3, T))
+    cfg = orc.OracleCfg(chunk=T, mode="single", muon=True, wnorm=True)
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W)
+    K2, V2 = K.copy(), V.copy()
+    K2[target] = rng.standard_normal((int(target.sum()), d))
+    V2[target] = rng.standard_normal((int(target.sum()), d))
+    O2, Wf2 = orc.ttt_head(cfg, Q, K2, V2, eta, W)
+    assert np.array_equal(O, O2)
+    assert all(np.array_equal(a, b) for a, b in zip(Wf, Wf2))
+    # and the input views alone give the same update
+    keep = ~target
+    cfg_in = orc.OracleCfg(chunk=int(keep.sum()), mode="single", muon=True, wnorm=True)
+    _, Wf3 = orc.ttt_head(cfg_in, Q[keep], K[keep], V[keep], eta[keep], W)
+    for a, b in zip(Wf, Wf3):
+        assert np.abs(a - b).max() <= 1e-12
+
+
+# ---------------------------------------------------------------- backward (outer loop)
+@pytest.mark.parametrize("loss", ["mse", "ip"])
+@pytest.mark.parametrize("C,mask", [(1, None), (4, None), (5, [1, 0, 1, 1])])
+def test_linear_backward_matches_central_differences(loss, C, mask):
+    """Every gradient of L = sum dO.O + sum dWf.Wf against central finite
+    differences of the forward oracle (h = 1e-6), on a tiny head with a ragged
+    last chunk."""
+    rng = np.random.default_rng(41)
+    d, T, step = 3, 17, 0.8
+    W0 = rng.standard_normal((d, d)) / np.sqrt(d)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    lr = rng.uniform(0.05, 0.3, T)
+    dO = rng.standard_normal((T, d))
+    dWf = rng.standard_normal((d, d))
+    cfg = orc.OracleCfg(chunk=C, fast_net="linear", loss=loss, muon=False, wnorm=False, step=step, mask=mask)
+
+    def L(Q_, K_, V_, lr_, W_):
+        O, (Wf,) = orc.ttt_head(cfg, Q_, K_, V_, lr_, (W_,))
+        return float((dO * O).sum() + (dWf * Wf).sum())
+
+    got = orc.linear_head_backward(cfg, Q, K, V, lr, W0, dO, dWf)
+    args = [Q, K, V, lr, W0]
+    h = 1e-6
+    for i, g in enumerate(got):
+        num = np.zeros_like(g)
+        for idx in np.ndindex(*g.shape):
+            up = [a.copy() for a in args]
+            dn = [a.copy() for a in args]
+            up[i][idx] += h
+            dn[i][idx] -= h
+            num[idx] = (L(*up) - L(*dn)) / (2 * h)
+        assert np.abs(g - num).max() <= 1e-6 * max(1.0, np.abs(num).max()), (i, np.abs(g - num).max())
