@@ -207,6 +207,22 @@ TTT_API int ttt_fwd_static_scratch(const ttt_cfg* cfg,
             void* O, float* Wf_1, float* Wf_2, float* Wf_3,
             int* status, void* stream);
 
+/* ---- outer-loop backward ---------------------------------------------------
+ * Gradients of a scalar loss L through the layer (the outer loop that trains
+ * the model around it differentiates through the inner updates: TTT-E2E news
+ * page §2.2), for the linear fast net with plain gradient steps (muon = wnorm =
+ * 0, momentum = 0) in shifted mode, inner-product or MSE loss: given
+ * dO = dL/dO ([B, H, T, d], cfg->dtype) and dWf = dL/dW_final ([B, H, d, d]
+ * fp32), writes dQ, dK, dV ([B, H, T, d], cfg->dtype), dlr ([B, H, T] fp32)
+ * and dW0 (fp32, W0's layout: summed over the batch unless w0_per_batch).
+ * Other configurations return TTT_ERR_UNSUPPORTED. Pointers, alignment,
+ * device memory, workspace (>= ttt_bwd_workspace_bytes, 256-byte aligned) and
+ * errors as for ttt_fwd; outputs overlap nothing. Enqueued on `stream`. */
+TTT_API int ttt_bwd_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
+TTT_API int ttt_bwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+                    const float* W0, const void* dO, const float* dWf, void* dQ, void* dK, void* dV,
+                    float* dlr, float* dW0, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- context parallelism (LaCT page §2.2.2) -------------------------------
  * The tokens of one chunk are split into shards held by different GPUs (or
  * handled by different calls). Every shard computes its partial gradient with

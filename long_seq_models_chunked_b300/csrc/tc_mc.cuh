@@ -32,8 +32,11 @@
 //   static __device__ void consume(const Params&, const Tile&, int kb, uint32_t stage_addr, uint32_t tmem)
 //   static constexpr uint32_t kEpiBytes   shared memory for the epilogue (a multiple of 4 KB
 //                                         per epilogue warp, or 0)
+//   struct Pre; static __device__ Pre pre(const Params&, const Tile&, int row)
+//        values the epilogue needs from global memory, loaded before the
+//        accumulator wait (so their latency hides under the tile's MMAs)
 //   static __device__ void epilogue(const Params&, const Tile&, uint32_t tmem_lane_base, int row,
-//                                   uint8_t* epi, uint32_t& es)
+//                                   uint8_t* epi, uint32_t& es, const Pre&)
 //        warp-uniform control flow around tcgen05.ld is required; epi = this warp's
 //        kEpiBytes / 4 of staging, es = a per-warp counter the epilogue may use for
 //        its buffers; TMA stores it issues (lane 0, bulk groups) complete before
@@ -162,12 +165,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
       typename Op::Tile t;
       Op::tile_of(p, w, rank, t);
       const uint32_t acc = et & 1u;
+      // global loads the epilogue needs, issued while the tile's MMAs run
+      const typename Op::Pre pre = Op::pre(p, t, 32 * g + lane);
       int ok = 0;
       if (lane == 0) ok = tc_wait(&accf[acc], (et >> 1) & 1u, p.cm, abort_flag) && !*abort_flag;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane, epi_w, es);
+      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane, epi_w, es, pre);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acce[acc]);

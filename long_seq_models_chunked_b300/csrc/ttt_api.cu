@@ -449,6 +449,51 @@ int ttt_fwd_host(const ttt_cfg* cfg, const void* Q, const void* K, const void* V
   return rc != TTT_OK ? rc : status;
 }
 
+int ttt_bwd_workspace_bytes(const ttt_cfg* cfg, size_t* bytes) {
+  if (!bytes) return TTT_ERR_ARG;
+  const int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  if (!bwd_supported(*cfg)) return TTT_ERR_UNSUPPORTED;
+  *bytes = bwd_workspace_bytes(*cfg);
+  return TTT_OK;
+}
+
+int ttt_bwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr, const float* W0,
+            const void* dO, const float* dWf, void* dQ, void* dK, void* dV, float* dlr, float* dW0,
+            void* workspace, size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  int v = ttt_bwd_workspace_bytes(cfg, &need);
+  if (v != TTT_OK) return v;
+  const ttt_cfg& g = *cfg;
+  const Sizes s = tensor_sizes(g);
+  const void* in[7] = {Q, K, V, lr, W0, dO, dWf};
+  void* out[5] = {dQ, dK, dV, dlr, dW0};
+  for (const void* p : in)
+    if (!p || !aligned16(p)) return TTT_ERR_ARG;
+  for (const void* p : out)
+    if (!p || !aligned16(p)) return TTT_ERR_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return TTT_ERR_WORKSPACE;
+  // outputs may not overlap the inputs, the workspace or each other
+  const size_t in_n[7] = {s.tok_bytes, s.tok_bytes, s.tok_bytes, s.lr_bytes, s.w0_bytes[0], s.tok_bytes,
+                          s.wf_bytes[0]};
+  const size_t out_n[5] = {s.tok_bytes, s.tok_bytes, s.tok_bytes, s.lr_bytes, s.w0_bytes[0]};
+  for (int i = 0; i < 5; ++i) {
+    const Range o{(const char*)out[i], out_n[i]};
+    for (int k = 0; k < 7; ++k)
+      if (overlap(o, Range{(const char*)in[k], in_n[k]})) return TTT_ERR_ARG;
+    if (overlap(o, Range{(const char*)workspace, need})) return TTT_ERR_ARG;
+    for (int k = i + 1; k < 5; ++k)
+      if (overlap(o, Range{(const char*)out[k], out_n[k]})) return TTT_ERR_ARG;
+  }
+  const void* ptrs[13] = {Q, K, V, lr, W0, dO, dWf, dQ, dK, dV, dlr, dW0, workspace};
+  v = check_device_ptrs(ptrs, 13);
+  if (v != TTT_OK) return v;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return TTT_ERR_CUDA;
+  return bwd_run(g, Q, K, V, lr, W0, dO, dWf, dQ, dK, dV, dlr, dW0, static_cast<char*>(workspace), st);
+}
+
 const char* ttt_strerror(int status) {
   switch (status) {
     case TTT_OK: return "ok";

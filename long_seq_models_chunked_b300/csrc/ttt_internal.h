@@ -51,6 +51,13 @@ bool linear_supported(const ttt_cfg& cfg);
 size_t linear_workspace_bytes(const ttt_cfg& cfg);
 int linear_run(const Call& c);
 
+// ---- outer-loop backward (linear net, plain steps, shifted mode) -----------
+bool bwd_supported(const ttt_cfg& cfg);
+size_t bwd_workspace_bytes(const ttt_cfg& cfg);
+int bwd_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const float* lr, const float* W0,
+            const void* dO, const float* dWf, void* dQ, void* dK, void* dV, float* dlr, float* dW0, char* ws,
+            cudaStream_t st);
+
 // ---- misc ------------------------------------------------------------------
 // TTT_OK or TTT_ERR_ARG: field ranges and sizes of *cfg (host only).
 int validate_cfg(const ttt_cfg* cfg);

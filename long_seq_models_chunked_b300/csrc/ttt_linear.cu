@@ -54,6 +54,7 @@ struct LinParams {
   int has_mask;
   int stall;               // test hook: never start the loads, so the first wait runs out
   int split;               // W and eta*R carried as bf16 hi + lo (TTT_PREC_SPLIT)
+  int inclusive;           // inclusive order (chunks of one 64-token tile): O -= step tril(Q K^T) (eta R)
   TcCommon cm;
 };
 
@@ -240,15 +241,17 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
           }
         }
       }
-      // O rows: token t_base + row, bf16
+      // O rows: token t_base + row, bf16 (inclusive order: after the correction below)
+      if (!(p.inclusive && upd)) {
 #pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
-        const int row = r0 + g + 8 * hq;
-        if (t_base + row < p.T) {
-          __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
+        for (int hq = 0; hq < 2; ++hq) {
+          const int row = r0 + g + 8 * hq;
+          if (t_base + row < p.T) {
+            __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
 #pragma unroll
-          for (int ln = 0; ln < kNT; ++ln)
-            *reinterpret_cast<uint32_t*>(dst + (kNT * nh + ln) * 8 + 2 * c4) = bf2(ao[ln][2 * hq], ao[ln][2 * hq + 1]);
+            for (int ln = 0; ln < kNT; ++ln)
+              *reinterpret_cast<uint32_t*>(dst + (kNT * nh + ln) * 8 + 2 * c4) = bf2(ao[ln][2 * hq], ao[ln][2 * hq + 1]);
+          }
         }
       }
       if (upd) {
@@ -271,6 +274,109 @@ __global__ void __launch_bounds__(kLinThreads, 2) linear_chunk_kernel(const __gr
       }
     }
     __syncthreads();
+
+    // ---- inclusive order (tutorial page §3: each query sees its own token's
+    // update): with one tile per chunk, o_t = W q_t - step sum_{u <= t} (q_t.k_u) eta_u r_u,
+    // i.e. O -= step S (eta R) with S = tril(Q K^T). S goes to the W-lo buffer,
+    // idle until the chunk-end refresh of the operands.
+    if (p.inclusive && upd) {
+      const int r0 = 16 * mr;
+      float as[kNT][4];
+#pragma unroll
+      for (int ln = 0; ln < kNT; ++ln)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) as[ln][q] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // over d
+        const int arow = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int acol = 16 * ks + 8 * (lane >> 4);
+        uint32_t aq[4];
+        ldsm_x4(sq + swz(arow, acol), aq[0], aq[1], aq[2], aq[3]);
+#pragma unroll
+        for (int lp = 0; lp < kNT / 2; ++lp) {
+          const int nrow = 16 * (kNT / 2 * nh + lp) + (lane & 7) + 8 * (lane >> 4);  // key token u
+          const int kcol = 16 * ks + 8 * ((lane >> 3) & 1);
+          uint32_t b[4];
+          ldsm_x4(sk + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
+          mma16816(as[2 * lp], aq, b[0], b[1]);
+          mma16816(as[2 * lp + 1], aq, b[2], b[3]);
+        }
+      }
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        const int t = r0 + g + 8 * hq;
+#pragma unroll
+        for (int ln = 0; ln < kNT; ++ln) {
+          const int u = (kNT * nh + ln) * 8 + 2 * c4;
+          const float x = u <= t ? as[ln][2 * hq] : 0.f;
+          const float y = u + 1 <= t ? as[ln][2 * hq + 1] : 0.f;
+          *reinterpret_cast<uint32_t*>(wl + swz(t, u)) = bf2(x, y);
+        }
+      }
+      __syncthreads();
+      float ac[kNT][4];
+#pragma unroll
+      for (int ln = 0; ln < kNT; ++ln)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ac[ln][q] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // over key tokens u
+        const int arow = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int acol = 16 * ks + 8 * (lane >> 4);
+        uint32_t a[4];
+        ldsm_x4(wl_a + swz(arow, acol), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int lp = 0; lp < kNT / 2; ++lp) {
+          // B = eta R: rows u (k), cols i (n), stored [u][i] -> transposed loads
+          const int kt = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int ic = 16 * (kNT / 2 * nh + lp) + 8 * (lane >> 4);
+          uint32_t b[4];
+          ldsm_x4_t(rh_a + swz(kt, ic), b[0], b[1], b[2], b[3]);
+          mma16816(ac[2 * lp], a, b[0], b[1]);
+          mma16816(ac[2 * lp + 1], a, b[2], b[3]);
+          if (p.split) {
+            ldsm_x4_t(rl_a + swz(kt, ic), b[0], b[1], b[2], b[3]);
+            mma16816(ac[2 * lp], a, b[0], b[1]);
+            mma16816(ac[2 * lp + 1], a, b[2], b[3]);
+          }
+        }
+      }
+      // O = Q W^T - step S (eta R): the first product again (phase 1's values
+      // are gone), then the correction, stored as bf16
+      float ao[kNT][4];
+#pragma unroll
+      for (int ln = 0; ln < kNT; ++ln)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ao[ln][q] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int arow = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int acol = 16 * ks + 8 * (lane >> 4);
+        uint32_t aq[4];
+        ldsm_x4(sq + swz(arow, acol), aq[0], aq[1], aq[2], aq[3]);
+#pragma unroll
+        for (int lp = 0; lp < kNT / 2; ++lp) {
+          const int nrow = 16 * (kNT / 2 * nh + lp) + (lane & 7) + 8 * (lane >> 4);
+          const int kcol = 16 * ks + 8 * ((lane >> 3) & 1);
+          uint32_t b[4];
+          ldsm_x4(wh_a + swz(nrow, kcol), b[0], b[1], b[2], b[3]);
+          mma16816(ao[2 * lp], aq, b[0], b[1]);
+          mma16816(ao[2 * lp + 1], aq, b[2], b[3]);
+        }
+      }
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        const int row = r0 + g + 8 * hq;
+        if (t_base + row < p.T) {
+          __nv_bfloat16* dst = p.O + ((size_t)bh * p.T + t_base + row) * kLinD;
+#pragma unroll
+          for (int ln = 0; ln < kNT; ++ln)
+            *reinterpret_cast<uint32_t*>(dst + (kNT * nh + ln) * 8 + 2 * c4) =
+                bf2(ao[ln][2 * hq] - p.step * ac[ln][2 * hq], ao[ln][2 * hq + 1] - p.step * ac[ln][2 * hq + 1]);
+        }
+      }
+      __syncthreads();  // S in the W-lo buffer is read; the chunk end may refresh it
+    }
 
     // ---- phase 2: G += (eta R)^T K, warp (mr, nh): rows i in [16 mr, +16),
     // columns j in its column group
@@ -346,9 +452,10 @@ int g_linear_stall_next = 0;  // test hook: the next launch withholds its loads
 bool linear_supported(const ttt_cfg& g) {
   // (no momentum buffer: the kernel keeps W alone in registers; with one
   // matrix, per-matrix rates have the per-token layout)
+  // (the inclusive order's dual form is built for chunks of one 64-token tile)
   return g.fast_net == TTT_NET_LINEAR && g.dtype == TTT_DTYPE_BF16 && g.d == kLinD && g.muon == 0 &&
-         g.wnorm == 0 && g.momentum == 0.f && g.mode == TTT_MODE_SHIFTED && g.chunk % kTile == 0 &&
-         g.T % 4 == 0;
+         g.wnorm == 0 && g.momentum == 0.f && g.chunk % kTile == 0 && g.T % 4 == 0 &&
+         (g.mode == TTT_MODE_SHIFTED || (g.mode == TTT_MODE_INCLUSIVE && g.chunk == kTile));
 }
 
 size_t linear_workspace_bytes(const ttt_cfg&) { return kStatusBytes; }
@@ -387,6 +494,7 @@ int linear_run(const Call& c) {
   p.has_mask = c.mask_all ? 0 : 1;
   p.stall = g_linear_stall_next ? 1 : 0;
   p.split = g.precision == TTT_PREC_SPLIT ? 1 : 0;
+  p.inclusive = g.mode == TTT_MODE_INCLUSIVE ? 1 : 0;
   g_linear_stall_next = 0;
   if (p.has_mask)
     for (int i = 0; i < c.n_chunks; ++i)

@@ -60,10 +60,9 @@ using namespace tcu;
 constexpr int kNsThreads = 192;
 constexpr int kEpiThreads = 128;  // warps 2..5
 constexpr int kAccCols = 256;     // columns of one TMEM accumulator buffer
-constexpr int kMaxGroup = 16;     // items that share one matrix in the SIMT phases
 constexpr unsigned kArrivals = 4; // completion-counter arrivals per finished item
 
-enum { K_NORM1 = 0, K_NORM2 = 1, K_GRAM = 2, K_POLY = 3, K_XUPD = 4 };
+enum { K_GRAM = 0, K_POLY = 1, K_XUPD = 2 };
 
 struct NsParams {
   CUtensorMap mXa[2][2];  // X operand [ping-pong][hi, lo]: {dh, d, Z}, box {32, 128}, 64-byte swizzle
@@ -77,29 +76,25 @@ struct NsParams {
   CUtensorMap sP[2];      // P [hi, lo]
   CUtensorMap sX[2][2];   // X operand [ping-pong][hi, lo]: {dh, d, Z}
   CUtensorMap sM;         // fp32 M: {dh, d, Z}, box {32, 32}, 128-byte swizzle
-  float* X;         // [Z][d][dh] fp32: the gradient (read only)
-  float* mom;       // [Z][d][dh] momentum buffers, or nullptr: B <- mu B + G replaces G
-  float mu;
   void* Xop[2][2];  // operand copies of X [ping-pong][hi, lo]
   float* M;         // [Z][d][dh] fp32 master weights (M1 = W1^T, M2 = W2, M3 = W3^T)
   bf16* Ms;         // bf16 shadow (hi)
   bf16* Msl;        // bf16 shadow (lo) or nullptr
   const float* n0;  // [Z][dh] reference row norms (W2: the first d entries)
-  float* nsq;       // [Z][gs] partial sums of squares of the gradient
   float* rowpart;   // [Z][dh / BNX][d] partial sums of squares of the rows of M2, one per column tile
   float* colpart;   // [Z][d / 32][dh] partial sums of squares of the columns of M1 / M3, one per 32 rows
   unsigned* cnt;    // [Z] completion counters (zeroed before the launch)
-  // fused: the gradient kernel already wrote X0's operands UNSCALED (G, or the
-  // momentum buffer) and per-z partial sums of squares nsqg[z][nsq_n]; there are
-  // no normalise phases, and the first Gram and X update scale their results by
-  // 1 / (||G||_F + eps)^2 and 1 / (||G||_F + eps)
+  // X0's operands are written before the launch. fused: UNSCALED (G, or the
+  // momentum buffer), with per-z partial sums of squares nsqg[z][nsq_n]; the
+  // first Gram and X update scale their results by 1 / (||G||_F + eps)^2 and
+  // 1 / (||G||_F + eps). Otherwise X0 = G / (||G||_F + eps) already.
   int fused;
   const float* nsqg;
   int nsq_n;
   int trace;        // test hook: record per-phase timestamps in g_ns_trace
   int stall;        // test hook: CTA 0 withholds the completion of its first item
   float alpha, beta, c, eps, step, wnorm_eps;
-  int Z, d, dh, iters, gs, wnorm;
+  int Z, d, dh, iters, wnorm;
   int mt, ntS, ntX;  // tiles: 128-row blocks; column tiles of the d x d and d x dh products
   int sym;           // 1: the d x d products compute only tiles that meet the upper triangle
   int nS;            // tiles of one d x d product per matrix
@@ -144,25 +139,6 @@ __device__ __forceinline__ float sumsq4(float4 v, float acc) {
   return fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, acc))));
 }
 
-// Four consecutive values as operands: bf16 (hi, lo) pairs (SPLIT) or fp16.
-template <bool SPLIT>
-__device__ __forceinline__ void st_op4(void* hi, void* lo, size_t o, float4 v) {
-  if (SPLIT) {
-    uint2 h, l;
-    h.x = pack_bf16(v.x, v.y);
-    h.y = pack_bf16(v.z, v.w);
-    l.x = pack_bf16(bf_rest(v.x), bf_rest(v.y));
-    l.y = pack_bf16(bf_rest(v.z), bf_rest(v.w));
-    *reinterpret_cast<uint2*>(static_cast<bf16*>(hi) + o) = h;
-    *reinterpret_cast<uint2*>(static_cast<bf16*>(lo) + o) = l;
-  } else {
-    uint2 h;
-    h.x = pack_f16(v.x, v.y);
-    h.y = pack_f16(v.z, v.w);
-    *reinterpret_cast<uint2*>(static_cast<f16*>(hi) + o) = h;
-  }
-}
-
 // The transpose of a warp's 32 x 32 block as operands, staged for a TMA store
 // in the 64-byte swizzle: lane l holds row l (v[i] = element (l, i)), which is
 // column l of the transpose, so it writes element (i, l) of the staged block
@@ -183,8 +159,6 @@ __device__ __forceinline__ void stage_op32_t(uint8_t* buf, int lane, const float
     }
   }
 }
-
-constexpr int kStream = 8;  // independent 16-byte loads in flight per thread in the SIMT items (16 spills)
 
 __device__ __forceinline__ void stage_f32x32(uint8_t* buf, int lane, const float* v) {
 #pragma unroll
@@ -209,40 +183,6 @@ __device__ __forceinline__ void warp_column_sums(float* a, int lane) {
   }
 }
 
-// ---- the epilogue warps' own barrier (named barrier 1, 128 threads) --------
-__device__ __forceinline__ void epi_sync() {
-  __syncwarp();
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// Barrier of the epilogue warps that also ORs a predicate over them: every
-// epilogue thread gets the same answer, so the four warps always take the same
-// branch (a warp that left the item loop alone would leave the others waiting
-// at a named barrier).
-__device__ __forceinline__ bool epi_sync_or(bool v) {
-  __syncwarp();
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
-
-// Deterministic sum over the 128 epilogue threads (warp butterflies, then the
-// four warp totals in warp order); every epilogue thread gets the result.
-__device__ __forceinline__ float epi_sum(float v, float* red, int ew) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  epi_sync();
-  if ((threadIdx.x & 31) == 0) red[ew] = v;
-  epi_sync();
-  return red[0] + red[1] + red[2] + red[3];
-}
-
 // Per-phase timeline of the last traced launch (test hook): for phase i (in
 // list order) slot 3i holds the earliest start of one of its items and slot
 // 3i+1 the latest finish (%globaltimer, ns); slot 2 the kernel's start.
@@ -261,12 +201,11 @@ struct Item {
   unsigned need;  // arrivals on cnt[z] before the item may start
 };
 
-__device__ __forceinline__ int n_phases(const NsParams& p) { return 2 + 3 * p.iters; }
+__device__ __forceinline__ int n_phases(const NsParams& p) { return 3 * p.iters; }
 
-// Items of one matrix in phase P.
+// Items of one matrix in phase P (3 it + k: Gram, polynomial, X update of iteration it).
 __device__ __forceinline__ int phase_items(const NsParams& p, int P) {
-  if (P < 2) return p.fused ? 0 : p.gs;
-  return ((P - 2) % 3 == 2) ? p.mt * p.ntX : p.nS;
+  return (P % 3 == 2) ? p.mt * p.ntX : p.nS;
 }
 
 // Item t of matrix z in phase P; `need` = the arrivals of every item of z in
@@ -277,17 +216,10 @@ __device__ __forceinline__ Item make_item(const NsParams& p, int P, int z, int t
   x.z = z;
   x.t = t;
   const int nS = p.nS, nX = p.mt * p.ntX;
-  const int ng = p.fused ? 0 : p.gs;  // items of each normalise phase
-  if (P < 2) {
-    x.kind = P == 0 ? K_NORM1 : K_NORM2;
-    x.need = P == 0 ? 0 : ng;
-  } else {
-    x.it = (P - 2) / 3;
-    const int k = (P - 2) % 3;
-    x.kind = K_GRAM + k;
-    x.need = 2 * ng + x.it * (2 * nS + nX) + (k >= 1 ? nS : 0) + (k == 2 ? nS : 0);
-  }
-  x.need *= kArrivals;
+  x.it = P / 3;
+  const int k = P % 3;
+  x.kind = K_GRAM + k;
+  x.need = (unsigned)(x.it * (2 * nS + nX) + (k >= 1 ? nS : 0) + (k == 2 ? nS : 0)) * kArrivals;
   return x;
 }
 
@@ -366,72 +298,6 @@ __device__ __forceinline__ void arrive_count(const NsParams& p, int z, bool tma_
   atomicAdd(p.cnt + z, 1u);
 }
 
-// ---- SIMT items, run by the 128 epilogue threads (et = 0..127, ew = et / 32) ----
-
-// Rows [r0, r1) of matrix z handled by SIMT item t of gs.
-__device__ __forceinline__ void item_rows(const NsParams& p, int t, int& r0, int& r1) {
-  const int rows_per = (p.d + p.gs - 1) / p.gs;
-  r0 = min(p.d, t * rows_per);
-  r1 = min(p.d, r0 + rows_per);
-}
-
-// norm1: the sum of squares of the item's rows of G; with a momentum buffer,
-// B <- mu B + G is formed and stored first and its squares are summed.
-__device__ __forceinline__ void item_norm1(const NsParams& p, const Item& x, int et, int ew, float* red) {
-  int r0, r1;
-  item_rows(p, x.t, r0, r1);
-  const size_t base = ((size_t)x.z * p.d + r0) * p.dh;
-  const float* g = p.X + base;
-  float* mb = p.mom ? p.mom + base : nullptr;
-  const int n4 = (r1 - r0) * p.dh / 4;
-  float ss = 0.f;
-  for (int b = et; b < n4; b += kEpiThreads * kStream) {
-    float4 v[kStream];
-#pragma unroll
-    for (int u = 0; u < kStream; ++u)
-      if (b + u * kEpiThreads < n4) v[u] = ldcg4(g + 4 * (b + u * kEpiThreads));
-    if (mb) {
-#pragma unroll
-      for (int u = 0; u < kStream; ++u)
-        if (b + u * kEpiThreads < n4) {
-          float* q = mb + 4 * (b + u * kEpiThreads);
-          const float4 o = ldcg4(q);
-          v[u] = make_float4(fmaf(p.mu, o.x, v[u].x), fmaf(p.mu, o.y, v[u].y), fmaf(p.mu, o.z, v[u].z),
-                             fmaf(p.mu, o.w, v[u].w));
-          *reinterpret_cast<float4*>(q) = v[u];
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < kStream; ++u)
-      if (b + u * kEpiThreads < n4) ss = sumsq4(v[u], ss);
-  }
-  ss = epi_sum(ss, red, ew);
-  if (et == 0) p.nsq[(size_t)x.z * p.gs + x.t] = ss;
-}
-
-// norm2: X0 = G / (||G||_F + eps) (or B / ...) for the item's rows, as operands.
-template <bool SPLIT>
-__device__ __forceinline__ void item_norm2(const NsParams& p, const Item& x, int et) {
-  int r0, r1;
-  item_rows(p, x.t, r0, r1);
-  const size_t base = ((size_t)x.z * p.d + r0) * p.dh;
-  const float* src = (p.mom ? p.mom : p.X) + base;
-  const int n4 = (r1 - r0) * p.dh / 4;
-  float tot = 0.f;
-  for (int q = 0; q < p.gs; ++q) tot += ldcg(p.nsq + (size_t)x.z * p.gs + q);
-  const float inv = 1.f / (sqrtf(tot) + p.eps);
-  for (int b = et; b < n4; b += kEpiThreads * kStream) {
-    float4 v[kStream];
-#pragma unroll
-    for (int u = 0; u < kStream; ++u)
-      if (b + u * kEpiThreads < n4) v[u] = ldcg4(src + 4 * (b + u * kEpiThreads));
-#pragma unroll
-    for (int u = 0; u < kStream; ++u)
-      if (b + u * kEpiThreads < n4)
-        st_op4<SPLIT>(p.Xop[0][0], p.Xop[0][1], base + 4 * (size_t)(b + u * kEpiThreads), scale4(v[u], inv));
-  }
-}
-
 __device__ __forceinline__ void trace_min(const NsParams& p, int slot) {
   if (p.trace && slot < kTraceSlots) atomicMin(&g_ns_trace[slot], globaltimer_ns());
 }
@@ -453,7 +319,6 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
   uint64_t* drainb = acce + 2;  // MMAs in flight at an abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drainb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  float* red = reinterpret_cast<float*>(tslot + 4);  // 4 floats
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = p.d, dh = p.dh;
@@ -578,40 +443,17 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue and SIMT items
-    const int ew = warp - 2;          // epilogue warp 0..3
-    const int et = threadIdx.x - 64;  // epilogue thread 0..127
+    // ------------------------------------------------------------ epilogue
     const int gq = warp & 3;          // TMEM lane group this warp may access
     const int r = 32 * gq + lane;     // accumulator row of this thread
     uint32_t et_n = 0;                // GEMM tiles drained
     uint32_t es = 0;                  // staging buffers used (this warp)
     bool first = true;
     for (int g = blockIdx.x; g < total; g += G) {
-      // the four warps take every branch together
-      if (epi_sync_or(*abort_flag != 0)) break;
+      if (*abort_flag) break;  // uniform within the warp (read after a wait)
       const Item x = decode(p, g);
       const bool withhold = p.stall && first && blockIdx.x == 0;  // test hook
       first = false;
-      if (x.kind == K_NORM1 || x.kind == K_NORM2) {
-        bool bad = false;
-        if (et == 0) {
-          bad = !wait_count(p, x.z, x.need);
-          if (bad) *abort_flag = 1;
-        }
-        if (epi_sync_or(bad)) break;
-        if (et == 0) trace_min(p, 2 + 2 * x.phase);
-        if (x.kind == K_NORM1)
-          item_norm1(p, x, et, ew, red);
-        else
-          item_norm2<SPLIT>(p, x, et);
-        // every lane's writes are ordered before the later TMA reads of them,
-        // then one lane per warp publishes the warp's part
-        ptx::fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0 && !withhold) arrive_count(p, x.z, false);
-        if (lane == 0) trace_max(p, 3 + 2 * x.phase);
-        continue;
-      }
       const bool xu = x.kind == K_XUPD;
       const bool last = xu && x.it + 1 == p.iters;
       const int bn = xu ? BNX : BNS;
@@ -871,6 +713,76 @@ __global__ void __launch_bounds__(kWnThreads) ns_wnorm_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------------------------- input
+// Newton-Schulz's input from fp32 gradients: one warp per (matrix z, row m,
+// column tile of bn) sums `splits` partials in split order, advances the
+// momentum buffer (B <- mu B + G), writes bf16 (hi, lo) operands (unless Xh is
+// NULL) and the tile row's sum of squares nsq[(z d + m) nt + tile].
+__global__ void ns_input_kernel(const float* parts, int splits, int Z, int d, int dh, int bn, float* mom, float mu,
+                                bf16* Xh, bf16* Xl, float* nsq) {
+  const int lane = threadIdx.x & 31;
+  const int nt = dh / bn;
+  const long long n_rows = (long long)Z * d * nt;
+  const size_t n = (size_t)Z * d * dh;
+  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_rows;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int tile = (int)(w % nt);
+    const long long zm = w / nt;  // z * d + m
+    const size_t row0 = (size_t)zm * dh + (size_t)tile * bn;
+    float ss = 0.f;
+    for (int c = 4 * lane; c < bn; c += 128) {
+      const size_t e = row0 + c;
+      float4 acc = *reinterpret_cast<const float4*>(parts + e);
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 v = *reinterpret_cast<const float4*>(parts + (size_t)sp * n + e);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      if (mom) {
+        float4* mb = reinterpret_cast<float4*>(mom + e);
+        const float4 b = *mb;
+        acc = make_float4(fmaf(mu, b.x, acc.x), fmaf(mu, b.y, acc.y), fmaf(mu, b.z, acc.z), fmaf(mu, b.w, acc.w));
+        *mb = acc;
+      }
+      if (Xh) {
+        uint2 h, l;
+        h.x = pack_bf16(acc.x, acc.y);
+        h.y = pack_bf16(acc.z, acc.w);
+        l.x = pack_bf16(bf_rest(acc.x), bf_rest(acc.y));
+        l.y = pack_bf16(bf_rest(acc.z), bf_rest(acc.w));
+        *reinterpret_cast<uint2*>(Xh + e) = h;
+        *reinterpret_cast<uint2*>(Xl + e) = l;
+      }
+      ss = fmaf(acc.w, acc.w, fmaf(acc.z, acc.z, fmaf(acc.y, acc.y, fmaf(acc.x, acc.x, ss))));
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) nsq[(size_t)zm * nt + tile] = ss;
+  }
+}
+
+// X0 = B / (||B||_F + eps) as fp16 operands (single precision), one CTA per
+// (matrix z, 32 rows); ||B||^2 from the partial sums, in order.
+__global__ void ns_scale_f16_kernel(const float* src, const float* nsq, int nsq_n, float eps, f16* X0, int d,
+                                    int dh) {
+  __shared__ float inv;
+  const int z = blockIdx.y;
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < nsq_n; ++k) t += nsq[(size_t)z * nsq_n + k];
+    inv = 1.f / (sqrtf(t) + eps);
+  }
+  __syncthreads();
+  const int r0 = blockIdx.x * 32, r1 = min(d, r0 + 32);
+  const size_t e0 = ((size_t)z * d + r0) * dh;
+  const int n4 = (r1 - r0) * dh / 4;
+  for (int b = threadIdx.x; b < n4; b += blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(src + e0)[b];
+    uint2 h;
+    h.x = pack_f16(v.x * inv, v.y * inv);
+    h.y = pack_f16(v.z * inv, v.w * inv);
+    reinterpret_cast<uint2*>(X0 + e0)[b] = h;
+  }
+}
+
 // Grid of the launch: every CTA resident at once (one per SM at this
 // shared-memory size), so that no dependency waits on a CTA that is not
 // running (the cooperative-launch occupancy).
@@ -905,7 +817,6 @@ int launch_ns(NsParams& p, cudaStream_t st) {
   int G = grid_size<BNS, BNX, SPLIT>(nullptr);
   if (G <= 0) return TTT_ERR_CUDA;
   if (g_forced_grid > 0 && g_forced_grid < G) G = g_forced_grid;
-  p.gs = std::max(1, std::min(kMaxGroup, G / p.Z));
   if (cudaMemsetAsync(p.cnt, 0, sizeof(unsigned) * (size_t)p.Z, st) != cudaSuccess) return TTT_ERR_CUDA;
   p.trace = g_trace ? 1 : 0;
   p.stall = g_stall_next.exchange(0);
@@ -945,7 +856,11 @@ int launch_ns(NsParams& p, cudaStream_t st) {
 }
 
 int g_tile_s = 0, g_tile_x = 0;  // test hook: forced column-tile widths (0 = by shape)
-int pick_bns(int d) { return g_tile_s ? g_tile_s : (d % 256 == 0) ? 256 : 128; }
+// 256-wide tiles of the d x d products from d = 512 on, even when d is not a
+// multiple (the padding rows load as zeros): M = 128, N = 128 MMAs run well
+// below the rate of N = 256 ones (measured: video d = 640, 724 against
+// 784 us per launch); below 512, 128-wide tiles waste less on padding
+int pick_bns(int d) { return g_tile_s ? g_tile_s : (d % 256 == 0 || d >= 512) ? 256 : 128; }
 int pick_bnx(int dh) { return (g_tile_x && dh % g_tile_x == 0) ? g_tile_x : (dh % 256 == 0) ? 256 : 128; }
 
 }  // namespace
@@ -953,6 +868,15 @@ int pick_bnx(int dh) { return (g_tile_x && dh % g_tile_x == 0) ? g_tile_x : (dh 
 bool ns_fused_supported(const ttt_cfg& g) { return g.d % 64 == 0 && g.dh % 128 == 0 && g.d <= g.dh; }
 
 void ns_force_grid(int ctas) { g_forced_grid = ctas; }
+
+int ns_input_launch(const float* parts, int splits, int Z, int d, int dh, int bn, float* mom, float mu, void* Xh,
+                    void* Xl, float* nsq, cudaStream_t st) {
+  prof_before(TTT_KERNEL_AUX, st);
+  ns_input_kernel<<<4 * 148, 256, 0, st>>>(parts, splits, Z, d, dh, bn, mom, mu, static_cast<bf16*>(Xh),
+                                           static_cast<bf16*>(Xl), nsq);
+  prof_after(TTT_KERNEL_AUX, st);
+  return cudaGetLastError() == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
 
 int ns_build_params(const NsFusedArgs& a, NsParams& p);
 
@@ -988,8 +912,27 @@ thread_local bool t_have = false;
 
 }  // namespace
 
-int ns_fused_run(const NsFusedArgs& a, cudaStream_t st) {
+int ns_fused_run(const NsFusedArgs& in, cudaStream_t st) {
+  NsFusedArgs a = in;
   const ttt_cfg& g = *a.cfg;
+  if (!a.fused) {
+    // X0 from the fp32 gradient: split precision writes the unscaled operands
+    // and partial norms (the kernel scales); single precision normalises first
+    const int nsq_bn = 128;
+    const int rc = ns_input_launch(a.X, 1, a.Z, g.d, g.dh, nsq_bn, a.mom, a.mu, a.split ? a.Xh[0] : nullptr,
+                                   a.split ? a.Xl[0] : nullptr, const_cast<float*>(a.nsqg), st);
+    if (rc != TTT_OK) return rc;
+    a.nsq_n = g.d * (g.dh / nsq_bn);
+    if (a.split) {
+      a.fused = true;
+    } else {
+      prof_before(TTT_KERNEL_AUX, st);
+      ns_scale_f16_kernel<<<dim3((g.d + 31) / 32, a.Z), 256, 0, st>>>(a.mom ? a.mom : a.X, a.nsqg, a.nsq_n, g.ns_eps,
+                                                                      static_cast<f16*>(a.Xh[0]), g.d, g.dh);
+      prof_after(TTT_KERNEL_AUX, st);
+      if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+    }
+  }
   const int bns = pick_bns(g.d), bnx = pick_bnx(g.dh);
   const bool split = a.split;
   const NsKey key = ns_key(a);
@@ -1040,15 +983,11 @@ int ns_build_params(const NsFusedArgs& a, NsParams& p) {
   }
   ok &= map3(&p.sM, a.M, dh, d, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return TTT_ERR_CUDA;
-  p.X = a.X;
-  p.mom = a.mom;
-  p.mu = a.mu;
   p.M = a.M;
   p.Ms = static_cast<bf16*>(a.Ms);
   p.Msl = static_cast<bf16*>(a.Msl);
   p.n0 = a.n0;
-  p.nsq = a.scratch;
-  p.rowpart = p.nsq + (size_t)Z * kMaxGroup;
+  p.rowpart = a.scratch;
   p.colpart = p.rowpart + (size_t)Z * (dh / 128) * d;
   p.cnt = reinterpret_cast<unsigned*>(p.colpart + (size_t)Z * (d / 32) * dh);
   // a + b s + c s^2 = c (s + beta)^2 + alpha
@@ -1099,10 +1038,10 @@ int ns_fused_plan(const ttt_cfg& g, int* resident) {
 }
 
 size_t ns_fused_scratch_floats(const ttt_cfg& g, int Z) {
-  // partial sums: of the gradient's squares per item, of the rows of M2 per
+  // partial sums: of the rows of M2 per
   // column tile (at most dh / 128 tiles), of the columns of M1 / M3 per 32 rows;
   // then the per-matrix completion counters
-  return (size_t)Z * (kMaxGroup + (size_t)(g.dh / 128) * g.d + (size_t)(g.d / 32) * g.dh) + (size_t)Z + 64;
+  return (size_t)Z * ((size_t)(g.dh / 128) * g.d + (size_t)(g.d / 32) * g.dh) + (size_t)Z + 64;
 }
 
 }  // namespace ttt

@@ -26,7 +26,9 @@ struct NsFusedArgs {
   float mu;
   // fused normalisation: the gradient kernel wrote Xh[0] / Xl[0] from the
   // UNSCALED gradient (momentum already advanced) and per-z partial sums of
-  // squares nsqg[z][nsq_n]; X and mom are then unused
+  // squares nsqg[z][nsq_n]; X and mom are then unused. Otherwise the call
+  // prepares X0 from X (and mom) itself, with nsqg as scratch of
+  // Z * d * (dh / 128) floats.
   bool fused;
   const float* nsqg;
   int nsq_n;
@@ -41,5 +43,11 @@ int ns_fused_plan(const ttt_cfg& g, int* resident);
 // Test hook: cap the grid at `ctas` CTAs (0 = every SM).
 void ns_force_grid(int ctas);
 int ns_fused_run(const NsFusedArgs& a, cudaStream_t st);
+// Newton-Schulz's input from fp32 gradients: sums `splits` partials
+// [splits][Z][d][dh] in order, advances the momentum buffer (mom != NULL:
+// B <- mu B + G), writes bf16 (hi, lo) operands (none when Xh is NULL) and the
+// sums of squares nsq[(z d + m) (dh / bn) + tile] of bn-wide row tiles.
+int ns_input_launch(const float* parts, int splits, int Z, int d, int dh, int bn, float* mom, float mu, void* Xh,
+                    void* Xl, float* nsq, cudaStream_t st);
 
 }  // namespace ttt

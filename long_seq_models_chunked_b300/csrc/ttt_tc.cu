@@ -45,8 +45,11 @@ std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch wit
 // share that slice's weights by TMA multicast (each CTA loads a share of the
 // weight boxes); the token rows are each CTA's own.
 //   query tile: [A|B] = Q [W1;W3]^T -> H_q = silu(A) * B                 (apply-1)
-//   key tile:   [A|B] = K [W1;W3]^T, Dm = V W2 -> DA, He, DB (SwiGLU backward,
-//               scaled by -lr per token), the gradient kernel's E operand
+//   key tile:   [A|B] = K [W1;W3]^T, Dm = Y W2 -> DA, He, DB (SwiGLU backward,
+//               scaled by each token's rates), the gradient kernel's E operand;
+//               Y = dl/df = -V for the inner-product loss, f(k) - V for MSE
+//   key-hidden tile (MSE): [A|B] = K [W1;W3]^T -> H_k = silu(A) * B as split
+//               operands, from which the next kernel forms Y = H_k W2^T - V
 // TMEM: [A|B] in columns 0-127, Dm in 128-191 of one 256-column accumulator.
 struct FwdMcOp {
   struct Params {
@@ -60,13 +63,16 @@ struct FwdMcOp {
     bf16* El;                // low halves of E (split precision)
     int d, dh, T, Cp, chunk_start, valid;
     int n_tok, groups, n_js, BH, cs;
-    int q, k;                // which kinds of tiles this launch computes
+    int q, k, h;             // which kinds of tiles this launch computes (query, key, key-hidden)
     int w_split, e_split;
     int lr_stride;           // 1: one rate per token; 3: one per token and matrix (W1, W2, W3)
+    int mse;                 // key tiles: Dm = Y W2 with Y (hi, lo) from mY / mYl (MSE loss)
+    CUtensorMap mY, mYl;     // Y (hi, lo) {d, Cp, BH}, box {64, 128, 1}: tokens relative to the chunk
+    CUtensorMap sHk, sHkl;   // stores: H_k (hi, lo) {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
     TcCommon cm;
   };
   struct Tile {
-    int bh, js, tok;
+    int bh, js, tok, kind;   // kind: 0 query, 1 key, 2 key-hidden
     bool is_k, real;
   };
   static constexpr int kStages = 4;
@@ -74,12 +80,18 @@ struct FwdMcOp {
   static constexpr int kAccCols = 256;
   static constexpr uint32_t kEpiBytes = 4 * 2 * 4096;  // two 4 KB staging buffers per epilogue warp
 
-  static __device__ int num_work(const Params& p) { return p.BH * p.n_js * p.groups * (p.q + p.k); }
+  static __device__ int num_work(const Params& p) { return p.BH * p.n_js * p.groups * (p.q + p.k + p.h); }
   static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
-    const int kinds = p.q + p.k;
+    const int kinds = p.q + p.k + p.h;
     const int kind = w % kinds;
     w /= kinds;
-    t.is_k = p.q ? kind == 1 : true;
+    // the kind-th enabled kind, in the order query, key, key-hidden
+    int c = 0;
+    t.kind = 0;
+    if (p.q) { if (c == kind) t.kind = 0; ++c; }
+    if (p.k) { if (c == kind) t.kind = 1; ++c; }
+    if (p.h) { if (c == kind) t.kind = 2; ++c; }
+    t.is_k = t.kind == 1;
     const int g = w % p.groups;
     w /= p.groups;
     t.js = w % p.n_js;
@@ -88,28 +100,36 @@ struct FwdMcOp {
     t.real = t.tok < p.n_tok;
   }
   static __device__ int num_kblocks(const Params& p, const Tile& t) { return (t.is_k ? 2 : 1) * (p.d / BK); }
-  // weight boxes of k-block kb: queries [W1, W3] (hi); keys segment 0
-  // [W1 hi, W3 hi, W1 lo, W3 lo], segment 1 [W2 hi, W2 lo]
+  // weight boxes of k-block kb: queries [W1, W3] (hi); keys and key hiddens,
+  // segment 0 [W1 hi, W3 hi, W1 lo, W3 lo]; keys, segment 1 [W2 hi, W2 lo]
   static __device__ int n_boxes(const Params& p, const Tile& t, int kb) {
-    if (!t.is_k) return 2;
+    if (t.kind == 0) return 2;
     return (kb < p.d / BK ? 2 : 1) * (p.w_split ? 2 : 1);
   }
+  static __device__ bool y_seg(const Params& p, const Tile& t, int kb) { return p.mse && t.is_k && kb >= p.d / BK; }
   static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int kb) {
-    return kABytes + (uint32_t)n_boxes(p, t, kb) * kBox;
+    return kABytes * (y_seg(p, t, kb) ? 2u : 1u) + (uint32_t)n_boxes(p, t, kb) * kBox;
   }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar, int rank,
                                  int cs, uint16_t mask) {
     const int nk = p.d / BK;
     const bool seg1 = t.is_k && kb >= nk;
     const int k = (seg1 ? kb - nk : kb) * BK;
-    const CUtensorMap* x = seg1 ? &p.mV : (t.is_k ? &p.mK : &p.mQ);
-    ptx::tma_load_3d(st, x, bar, k, p.chunk_start + t.tok * BM, t.bh);
+    // the Y segment (MSE) keeps its rows hi at 0 and lo at kABytes, its W2 boxes two slots on
+    const int wslot = y_seg(p, t, kb) ? 2 : 0;
+    if (y_seg(p, t, kb)) {
+      ptx::tma_load_3d(st, &p.mY, bar, k, t.tok * BM, t.bh);
+      ptx::tma_load_3d(st + kABytes, &p.mYl, bar, k, t.tok * BM, t.bh);
+    } else {
+      const CUtensorMap* x = seg1 ? &p.mV : (t.kind == 0 ? &p.mQ : &p.mK);
+      ptx::tma_load_3d(st, x, bar, k, p.chunk_start + t.tok * BM, t.bh);
+    }
     const int z = t.bh * 3;
     const int nb = n_boxes(p, t, kb);
     for (int b = rank; b < nb; b += cs) {
       const bool lo = seg1 ? b == 1 : b >= 2;
       const int zz = seg1 ? z + 1 : z + ((b & 1) ? 2 : 0);
-      ptx::tma_load_3d_shared(st + kABytes + b * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
+      ptx::tma_load_3d_shared(st + kABytes + (b + wslot) * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
     }
   }
   static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
@@ -117,11 +137,22 @@ struct FwdMcOp {
     const uint32_t a = st, b = st + kABytes;
     if (!t.is_k || kb < nk) {
       constexpr uint32_t id = ptx::idesc_bf16(128, 128, false, true);
-      const bool two = t.is_k && p.w_split;
+      const bool two = t.kind != 0 && p.w_split;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
         if (two) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b + 2 * kBox, kk), id, 1u);
+      }
+    } else if (p.mse) {
+      // Dm = Y W2 with both split: Yh W2h + Yh W2l + Yl W2h
+      const int k2 = kb - nk;
+      constexpr uint32_t id = ptx::idesc_bf16(128, 64, false, true);
+      const uint32_t yl = st + kABytes, wh = st + kABytes + 2 * kBox, wl = wh + kBox;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(wh, kk), id, (k2 | kk) != 0);
+        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(wl, kk), id, 1u);
+        ptx::mma_bf16(tmem + 128, kdesc(yl, kk), mdesc(wh, kk), id, 1u);
       }
     } else {
       const int k2 = kb - nk;
@@ -137,8 +168,24 @@ struct FwdMcOp {
   // 32 x 32 blocks (64-byte swizzle) in one of its two buffers and writes them
   // with TMA stores, hi and lo halves alike. Rows past the chunk's tokens get
   // lr 0 (zero E rows) and zero H_q rows.
+  // the key rows' rates (W1, W2, W3), loaded before the accumulator wait;
+  // rows past the chunk's tokens get rate 0, so their E rows are zero
+  struct Pre {
+    float e1, e2, e3;
+  };
+  static __device__ Pre pre(const Params& p, const Tile& t, int r) {
+    Pre x{0.f, 0.f, 0.f};
+    const int tl = t.tok * BM + r;
+    if (t.is_k && t.real && tl < p.valid) {
+      const float* lp = p.lr + ((size_t)t.bh * p.T + p.chunk_start + tl) * p.lr_stride;
+      x.e1 = lp[0];
+      x.e2 = p.lr_stride > 1 ? lp[1] : x.e1;
+      x.e3 = p.lr_stride > 1 ? lp[2] : x.e1;
+    }
+    return x;
+  }
   static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t* epi,
-                                  uint32_t& es) {
+                                  uint32_t& es, const Pre& pr) {
     if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
     const int lane = r & 31;
     const int tl = t.tok * BM + r;        // token index inside the chunk
@@ -165,23 +212,20 @@ struct FwdMcOp {
     };
     float va[32], vb[32];
     if (!t.is_k) {
+      const bool hk = t.kind == 2;  // key hiddens: split operands of the MSE's Y = H_k W2^T - V
       for (int c = 0; c < 64; c += 32) {
         ptx::tmem_ld32(tm + c, va);
         ptx::tmem_ld32(tm + 64 + c, vb);
 #pragma unroll
         for (int i = 0; i < 32; ++i) va[i] = valid ? va[i] * sigmoid_fast(va[i]) * vb[i] : 0.f;
-        put(va, false, &p.sHq, &p.sHq, j0 + c, t.bh);
+        if (hk)
+          put(va, true, &p.sHk, &p.sHkl, j0 + c, t.bh);
+        else
+          put(va, false, &p.sHq, &p.sHq, j0 + c, t.bh);
       }
     } else {
-      // rows past the chunk's tokens get lr 0, so their E rows are zero; the
-      // rates of W1, W2, W3 (one shared rate, or one per matrix)
-      float e1 = 0.f, e2 = 0.f, e3 = 0.f;
-      if (valid) {
-        const float* lp = p.lr + ((size_t)t.bh * p.T + p.chunk_start + tl) * p.lr_stride;
-        e1 = lp[0];
-        e2 = p.lr_stride > 1 ? lp[1] : e1;
-        e3 = p.lr_stride > 1 ? lp[2] : e1;
-      }
+      // the rates of W1, W2, W3 (one shared rate, or one per matrix; 0 past the chunk)
+      const float e1 = pr.e1, e2 = pr.e2, e3 = pr.e3;
       const bool lo = p.e_split != 0;
       float vd[32];
       for (int c = 0; c < 64; c += 32) {
@@ -189,14 +233,18 @@ struct FwdMcOp {
         ptx::tmem_ld32(tm + 64 + c, vb);
         ptx::tmem_ld32(tm + 128 + c, vd);
         float oh[32];
+        // inner product: Dm = V W2 and dl/dh = -Dm, G2 = V^T (-lr2 H);
+        // MSE: Dm = Y W2 = dl/dh, G2 = Y^T (lr2 H)
+        const float sgn = p.mse ? 1.f : -1.f;
+        const float s1 = sgn * e1, s2 = sgn * e2, s3 = sgn * e3;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float a = va[i], b = vb[i];
-          const float g1 = -e1 * vd[i];         // lr1 * dl/dh, dl/dh = W2^T (-v)
-          const float g3 = -e3 * vd[i];         // lr3 * dl/dh
+          const float g1 = s1 * vd[i];          // lr1 * dl/dh
+          const float g3 = s3 * vd[i];          // lr3 * dl/dh
           const float sg = sigmoid_fast(a);
           const float s = a * sg;
-          oh[i] = -e2 * s * b;                  // -lr2 * h  (G2 = V^T He)
+          oh[i] = s2 * s * b;                   // the G2 operand He
           va[i] = g1 * b * sg * (1.f + a * (1.f - sg));
           vb[i] = g3 * s;
         }
@@ -258,6 +306,87 @@ struct OOp {
   }
 };
 
+// ============================================================ MSE: Y = H_k W2^T - V
+// The keys' output error of the MSE loss (tutorial page §3: l = 1/2 ||f(k) - v||^2,
+// dl/df = f(k) - v) for the key rows of a chunk, as bf16 (hi, lo) operands
+// [BH][Cp][d] (tokens relative to the chunk; rows past its tokens are zero).
+// H_k and W2 are both split: every product is Hh Wh + Hh Wl + Hl Wh.
+struct YOp {
+  struct Params {
+    CUtensorMap mH, mHl;    // H_k (hi, lo) {dh, Cp, BH}, box {64, 128, 1}
+    CUtensorMap mW2, mW2l;  // shadows (hi, lo) {dh, d, 3BH}, box {64, 128, 1}
+    const bf16* V;          // [BH][T][d]
+    bf16* Y;                // [BH][Cp][d]
+    bf16* Yl;
+    int d, dh, T, Cp, chunk_start, valid, m_tiles, n_tiles;
+    TcCommon cm;
+  };
+  struct Tile {
+    int bh, row0, n0;
+  };
+  static constexpr int BN = 128;
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = 4 * kABytes;  // [H hi | H lo | W2 hi | W2 lo], 128 x 64 each
+  static constexpr int kTmemCols = 128;
+
+  static __device__ bool tile_of(const Params& p, Tile& t) {
+    const int nt = blockIdx.x % p.n_tiles, mt = blockIdx.x / p.n_tiles;
+    if (mt >= p.m_tiles) return false;
+    t.row0 = mt * BM;
+    t.n0 = nt * BN;
+    t.bh = blockIdx.y;
+    return true;
+  }
+  static __device__ int num_kblocks(const Params& p, const Tile&) { return p.dh / BK; }
+  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return kStageBytes; }
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar) {
+    ptx::tma_load_3d(st, &p.mH, bar, kb * BK, t.row0, t.bh);
+    ptx::tma_load_3d(st + kABytes, &p.mHl, bar, kb * BK, t.row0, t.bh);
+    ptx::tma_load_3d(st + 2 * kABytes, &p.mW2, bar, kb * BK, t.n0, t.bh * 3 + 1);
+    ptx::tma_load_3d(st + 3 * kABytes, &p.mW2l, bar, kb * BK, t.n0, t.bh * 3 + 1);
+  }
+  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
+    constexpr uint32_t id = ptx::idesc_bf16(128, BN, false, false);
+    const uint32_t hh = st, hl = st + kABytes, wh = st + 2 * kABytes, wl = st + 3 * kABytes;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      ptx::mma_bf16(tmem, kdesc(hh, kk), kdesc(wh, kk), id, (kb | kk) != 0);
+      ptx::mma_bf16(tmem, kdesc(hh, kk), kdesc(wl, kk), id, 1u);
+      ptx::mma_bf16(tmem, kdesc(hl, kk), kdesc(wh, kk), id, 1u);
+    }
+  }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, float*, bool ok) {
+    if (!ok) return;
+    const int tl = t.row0 + r;  // token index inside the chunk
+    const bool valid = tl < p.valid;
+    const bf16* vrow = p.V + ((size_t)t.bh * p.T + p.chunk_start + tl) * p.d;
+    const size_t o = ((size_t)t.bh * p.Cp + tl) * p.d;
+    float v[32];
+    for (int c = 0; c < BN; c += 32) {
+      const int n = t.n0 + c;
+      if (n >= p.d) break;
+      ptx::tmem_ld32(tm + c, v);
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(vrow + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = src[q];
+          const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[8 * q + 2 * e] -= __uint_as_float(u[e] << 16);
+            v[8 * q + 2 * e + 1] -= __uint_as_float(u[e] & 0xffff0000u);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+      st_bf16pair32(p.Y + o + n, p.Yl + o + n, v);
+    }
+  }
+};
+
 // ============================================================ chunk gradients, multicast
 // Cluster of cs CTAs per work item (z, n-block, token split, row group): CTA
 // `rank` computes rows [128 (g cs + rank), +128) of G_z^T (d x dh) over the
@@ -268,12 +397,13 @@ struct OOp {
 //   z = bh*3 + j:  j=0  G1^T = K^T DA;  j=1  G2 = V^T He;  j=2  G3^T = K^T DB
 // With split E (hi + lo) both halves sit in one stage and every A tile feeds
 // two MMAs.
-template <int BN>
+template <int BN, bool MSE = false>
 struct GradMcOp {
   struct Params {
     CUtensorMap mK4, mV4;  // 4D {d, C, n_full, BH}, box {64, 32, 1, 1}  (full chunks)
     CUtensorMap mK3, mV3;  // 3D {d, T, BH}, box {64, 32, 1}            (ragged last chunk)
     CUtensorMap mE, mEl;   // 3D {dh, Cp, 3BH}, box {64, 32, 1}
+    CUtensorMap mY, mYl;   // MSE: Y (hi, lo) {d, Cp, BH}, box {64, 32, 1}, G2's operand instead of V
     float* G;              // [Z][d][dh] fp32 (splits == 1)
     float* split_out;      // [splits][Z][d][dh] fp32 (splits > 1)
     int d, dh, Z, chunk_idx, chunk_start, valid, use4d, nt, splits, kb_per_split, e_split;
@@ -297,8 +427,9 @@ struct GradMcOp {
   static constexpr uint32_t kBoxG = 64 * kTok * 2;       // one 64 x 32 box
   static constexpr uint32_t kAB = 2 * kBoxG;              // A: 128 rows of d
   static constexpr uint32_t kEB = (BN / 64) * kBoxG;      // one half of E
-  static constexpr int kStages = 5;
-  static constexpr int kStageBytes = kAB + 2 * kEB;
+  // MSE: the stage also holds the low half of Y (G2's A operand, computed)
+  static constexpr int kStages = MSE ? 4 : 5;
+  static constexpr int kStageBytes = kAB + 2 * kEB + (MSE ? kAB : 0);
   static constexpr int kAccCols = BN;
   static constexpr uint32_t kEpiBytes = 0;
 
@@ -319,12 +450,19 @@ struct GradMcOp {
     t.nkb = max(0, min(total, t.kb0 + p.kb_per_split) - t.kb0);
   }
   static __device__ int num_kblocks(const Params&, const Tile& t) { return t.nkb; }
-  static __device__ uint32_t stage_tx(const Params& p, const Tile&, int) {
-    return kAB + (p.e_split ? 2u : 1u) * kEB;
+  static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int) {
+    return kAB + (p.e_split ? 2u : 1u) * kEB + ((MSE && t.j == 1) ? kAB : 0u);
   }
   static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint64_t* bar, int rank,
                                  int cs, uint16_t mask) {
     const int tok = (t.kb0 + kb) * kTok;
+    if (MSE && t.j == 1) {
+      // G2 = Y^T He: Y (hi, lo) of the chunk's tokens, relative to its start
+      for (int g = 0; g < 2; ++g) {
+        ptx::tma_load_3d(st + g * kBoxG, &p.mY, bar, t.m0 + g * 64, tok, t.bh);
+        ptx::tma_load_3d(st + kAB + 2 * kEB + g * kBoxG, &p.mYl, bar, t.m0 + g * 64, tok, t.bh);
+      }
+    } else
     for (int g = 0; g < 2; ++g) {
       if (p.use4d)
         ptx::tma_load_4d(st + g * kBoxG, t.j == 1 ? &p.mV4 : &p.mK4, bar, t.m0 + g * 64, tok, p.chunk_idx, t.bh);
@@ -339,18 +477,26 @@ struct GradMcOp {
                           t.z, mask);
     }
   }
-  static __device__ void consume(const Params& p, const Tile&, int kb, uint32_t st, uint32_t tmem) {
+  static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
     constexpr uint32_t id = ptx::idesc_bf16(128, BN, true, true);
     const uint32_t eh = st + kAB, el = eh + kEB;
+    const bool ylo = MSE && t.j == 1;  // a computed A operand: three products
     // MN-major operands of 64-wide groups kBoxG apart, 16 tokens per MMA
 #pragma unroll
     for (int kk = 0; kk < kTok / 16; ++kk) {
       const uint64_t a = ptx::sdesc(st + kk * 2048, kBoxG, 1024);
       ptx::mma_bf16(tmem, a, ptx::sdesc(eh + kk * 2048, kBoxG, 1024), id, (kb | kk) != 0);
       if (p.e_split) ptx::mma_bf16(tmem, a, ptx::sdesc(el + kk * 2048, kBoxG, 1024), id, 1u);
+      if (ylo) {
+        const uint64_t al = ptx::sdesc(st + kAB + 2 * kEB + kk * 2048, kBoxG, 1024);
+        ptx::mma_bf16(tmem, al, ptx::sdesc(eh + kk * 2048, kBoxG, 1024), id, 1u);
+      }
     }
   }
-  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&) {
+  struct Pre {};
+  static __device__ Pre pre(const Params&, const Tile&, int) { return {}; }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&,
+                                  const Pre&) {
     const int m = t.m0 + r;
     float v[32];
     if (p.Xh && p.splits == 1) {
@@ -625,49 +771,6 @@ __global__ void gsplit_reduce_kernel(const float* parts, float* G, int splits, s
   }
 }
 
-// The same reduction writing the Newton-Schulz input (see GradMcOp): one warp
-// per (matrix z, row m, column tile of bn) sums the partials in split order,
-// advances the momentum buffer, writes bf16 (hi, lo) operands and the tile
-// row's sum of squares nsq[(z d + m) nt + tile].
-__global__ void gsplit_reduce_ns_kernel(const float* parts, int splits, int Z, int d, int dh, int bn,
-                                        float* mom, float mu, bf16* Xh, bf16* Xl, float* nsq) {
-  const int lane = threadIdx.x & 31;
-  const int nt = dh / bn;
-  const long long n_rows = (long long)Z * d * nt;
-  const size_t n = (size_t)Z * d * dh;
-  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_rows;
-       w += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int tile = (int)(w % nt);
-    const long long zm = w / nt;  // z * d + m
-    const size_t row0 = (size_t)zm * dh + (size_t)tile * bn;
-    float ss = 0.f;
-    for (int c = 4 * lane; c < bn; c += 128) {
-      const size_t e = row0 + c;
-      float4 acc = *reinterpret_cast<const float4*>(parts + e);
-      for (int sp = 1; sp < splits; ++sp) {
-        const float4 v = *reinterpret_cast<const float4*>(parts + (size_t)sp * n + e);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      if (mom) {
-        float4* mb = reinterpret_cast<float4*>(mom + e);
-        const float4 b = *mb;
-        acc = make_float4(fmaf(mu, b.x, acc.x), fmaf(mu, b.y, acc.y), fmaf(mu, b.z, acc.z), fmaf(mu, b.w, acc.w));
-        *mb = acc;
-      }
-      uint2 h, l;
-      h.x = pack_bf16(acc.x, acc.y);
-      h.y = pack_bf16(acc.z, acc.w);
-      l.x = pack_bf16(bf_rest(acc.x), bf_rest(acc.y));
-      l.y = pack_bf16(bf_rest(acc.z), bf_rest(acc.w));
-      *reinterpret_cast<uint2*>(Xh + e) = h;
-      *reinterpret_cast<uint2*>(Xl + e) = l;
-      ss = fmaf(acc.w, acc.w, fmaf(acc.z, acc.z, fmaf(acc.y, acc.y, fmaf(acc.x, acc.x, ss))));
-    }
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) nsq[(size_t)zm * nt + tile] = ss;
-  }
-}
-
 // ============================================================ host side
 
 template <class Op>
@@ -792,6 +895,7 @@ struct Plan {
   int g_splits_max;       // token splits the workspace has room for
   size_t off_mom;         // momentum buffers [Z][d][dh] fp32 (momentum != 0 only)
   size_t off_nsqg;        // per-row sums of squares of the gradient [Z][d][dh / g_bn] (Muon)
+  size_t off_Hk[2], off_Y[2];  // MSE: key hiddens (hi, lo) [BH][Cp][dh]; Y (hi, lo) [BH][Cp][d]
   size_t off_M, off_Ms, off_Msl, off_n0, off_Hq, off_E, off_El, off_G, off_Xh[2], off_Xl[2], off_Sh,
       off_Sl, off_Ph, off_Pl, off_split, off_nsq, total;
 };
@@ -848,7 +952,12 @@ Plan make_plan(const ttt_cfg& g) {
   P.off_split = take(P.g_splits_max > 1 ? (size_t)P.g_splits_max * wz * 4 : 0);
   P.off_nsq = take(ns_fused_scratch_floats(g, P.Z) * 4);
   P.off_mom = take(g.momentum != 0.f ? wz * 4 : 0);
-  P.off_nsqg = take(g.muon ? (size_t)P.Z * g.d * P.g_nt * 4 : 0);
+  P.off_nsqg = take(g.muon ? (size_t)P.Z * g.d * (g.dh / 128) * 4 : 0);
+  const size_t mse = g.loss == TTT_LOSS_MSE ? 1 : 0;
+  for (int i = 0; i < 2; ++i) {
+    P.off_Hk[i] = take(mse * P.BH * P.Cp * g.dh * 2);
+    P.off_Y[i] = take(mse * P.BH * P.Cp * g.d * 2);
+  }
   P.total = off;
   return P;
 }
@@ -859,8 +968,9 @@ bool tc_supported(const ttt_cfg& g) {
   // d <= 1024: the gradient's clusters hold d / 128 <= 8 CTAs
   // (the fused Muon step completes the square of its quintic, so it needs c != 0,
   // and fuses the update into its last iteration, so it needs at least one)
-  return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU && g.loss == TTT_LOSS_IP &&
-         g.mode != TTT_MODE_INCLUSIVE && g.d % 64 == 0 &&
+  // (the MSE loss adds computed operands, H_k and Y, that need split precision)
+  return g.dtype == TTT_DTYPE_BF16 && g.fast_net == TTT_NET_SWIGLU &&
+         (g.loss == TTT_LOSS_IP || g.precision == TTT_PREC_SPLIT) && g.mode != TTT_MODE_INCLUSIVE && g.d % 64 == 0 &&
          g.dh % 128 == 0 && g.d <= g.dh && g.d <= 1024 && g.dh <= 16384 &&
          (!g.muon || (g.ns_c != 0.f && g.ns_iters >= 1));
 }
@@ -881,9 +991,11 @@ class TcLayer {
     st_ = st;
     ws_ = ws;
     const bool split = P.split != 0;
-    // which stages carry split operands (all of them unless a test hook narrowed it)
-    split_fwd = split && (g_split_mask & 1);
-    split_grad = split && (g_split_mask & 2);
+    mse = g.loss == TTT_LOSS_MSE;
+    // which stages carry split operands (all of them unless a test hook
+    // narrowed it; the MSE path keeps its forward and gradient split)
+    split_fwd = split && ((g_split_mask & 1) || mse);
+    split_grad = split && ((g_split_mask & 2) || mse);
     split_ns = split && (g_split_mask & 4);
     auto at = [&](size_t off, bool on) -> void* { return on ? static_cast<void*>(ws + off) : nullptr; };
     M = reinterpret_cast<float*>(ws + P.off_M);
@@ -909,6 +1021,18 @@ class TcLayer {
     ok &= map3(&sE[0], E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
     ok &= map3(&sE[1], split_grad ? El : E, dh, P.Cp, Z, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                CU_TENSOR_MAP_SWIZZLE_64B);
+    if (mse) {
+      for (int i = 0; i < 2; ++i) {
+        Hk[i] = reinterpret_cast<bf16*>(ws + P.off_Hk[i]);
+        Y[i] = reinterpret_cast<bf16*>(ws + P.off_Y[i]);
+        ok &= map3(&mHk[i], Hk[i], dh, P.Cp, BH, 64, 128);
+        ok &= map3(&sHk[i], Hk[i], dh, P.Cp, BH, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
+        ok &= map3(&mYf[i], Y[i], d, P.Cp, BH, 64, 128);
+        ok &= map3(&mYg[i], Y[i], d, P.Cp, BH, 64, 32);
+      }
+      ok &= map3(&mW2y[0], Ms, dh, d, Z, 64, 128);
+      ok &= map3(&mW2y[1], Msl, dh, d, Z, 64, 128);
+    }
     nsa = NsFusedArgs{};
     nsa.cfg = &g_;
     nsa.Z = Z;
@@ -934,6 +1058,7 @@ class TcLayer {
     // gradient kernel (operands and partial norms), with no normalise pass
     fused_ns = g.muon && split_ns;
     nsqg = reinterpret_cast<float*>(ws + P.off_nsqg);
+    nsa.nsqg = nsqg;
     return ok ? TTT_OK : TTT_ERR_CUDA;
   }
 
@@ -942,6 +1067,7 @@ class TcLayer {
   int bind_tokens(const void* Q, const void* K, const void* V, const float* lr, void* O, int T) {
     const int d = g_.d, BH = P.BH;
     T_ = T;
+    V_ = static_cast<const bf16*>(V);
     lr_ = lr;
     O_ = O;
     n_full = P.C > 0 ? T / P.C : 0;
@@ -998,7 +1124,31 @@ class TcLayer {
   }
 
   // Forward of tokens [s, s + valid): query tiles (H_q) and/or key tiles (E).
+  // With the MSE loss the key tiles need Y = f(k) - v first: one launch for
+  // the queries and the key hiddens H_k, one for Y = H_k W2^T - V, then the key
+  // tiles with Dm = Y W2.
   int fwd(int s, int valid, bool q, bool k) {
+    if (k && mse) {
+      int rc = fwd_launch(s, valid, q, false, true);
+      if (rc == TTT_OK) rc = y_launch(s, valid);
+      if (rc == TTT_OK) rc = fwd_launch(s, valid, false, true, false);
+      return rc;
+    }
+    return fwd_launch(s, valid, q, k, false);
+  }
+
+  int y_launch(int s, int valid) {
+    YOp::Params p{};
+    p.mH = mHk[0]; p.mHl = mHk[1]; p.mW2 = mW2y[0]; p.mW2l = mW2y[1];
+    p.V = V_; p.Y = Y[0]; p.Yl = Y[1];
+    p.d = g_.d; p.dh = g_.dh; p.T = T_; p.Cp = P.Cp; p.chunk_start = s; p.valid = valid;
+    p.m_tiles = (valid + BM - 1) / BM;
+    p.n_tiles = (g_.d + YOp::BN - 1) / YOp::BN;
+    p.cm = cm;
+    return launch_op<YOp>(TTT_KERNEL_FWD, p, dim3(p.m_tiles * p.n_tiles, P.BH), st_);
+  }
+
+  int fwd_launch(int s, int valid, bool q, bool k, bool h) {
     FwdMcOp::Params p{};
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
@@ -1015,11 +1165,16 @@ class TcLayer {
     p.BH = P.BH;
     p.q = q ? 1 : 0;
     p.k = k ? 1 : 0;
+    p.h = h ? 1 : 0;
+    p.mse = mse ? 1 : 0;
+    if (mse) {
+      p.mY = mYf[0]; p.mYl = mYf[1]; p.sHk = sHk[0]; p.sHkl = sHk[1];
+    }
     p.w_split = split_fwd ? 1 : 0;
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
     p.cm.stall = g_stall_next_fwd.exchange(0);
-    const int n_work = P.BH * p.n_js * p.groups * (p.q + p.k);
+    const int n_work = P.BH * p.n_js * p.groups * (p.q + p.k + p.h);
     return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
   }
 
@@ -1061,6 +1216,10 @@ class TcLayer {
       p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
       p.nt = P.g_nt; p.splits = splits; p.kb_per_split = kb_per_split; p.e_split = split_grad ? 1 : 0; p.cm = cm;
       p.mg = P.g_mg; p.cs = P.g_cs;
+      if (mse) {
+        p.mY = mYg[0];
+        p.mYl = mYg[1];
+      }
       if (to_ns) {
         p.Xh = static_cast<bf16*>(nsa.Xh[0]);
         p.Xl = static_cast<bf16*>(nsa.Xl[0]);
@@ -1072,16 +1231,12 @@ class TcLayer {
       if (r != TTT_OK || splits == 1) return r;
       const size_t n = (size_t)Z * d * dh;
       cudaStream_t st = st_;
-      if (to_ns) {
-        TTT_LAUNCH(TTT_KERNEL_GRAD, st,
-                   gsplit_reduce_ns_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(
-                       splitbuf, splits, Z, d, dh, P.g_bn, mom, g_.momentum, static_cast<bf16*>(nsa.Xh[0]),
-                       static_cast<bf16*>(nsa.Xl[0]), nsqg));
-        return TTT_OK;
-      }
+      if (to_ns)
+        return ns_input_launch(splitbuf, splits, Z, d, dh, P.g_bn, mom, g_.momentum, nsa.Xh[0], nsa.Xl[0], nsqg, st);
       TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, dst, splits, n));
       return TTT_OK;
     };
+    if (mse) return P.g_bn == 256 ? launch(GradMcOp<256, true>{}) : launch(GradMcOp<128, true>{});
     return P.g_bn == 256 ? launch(GradMcOp<256>{}) : launch(GradMcOp<128>{});
   }
 
@@ -1117,7 +1272,11 @@ class TcLayer {
   ttt_cfg g_;
   cudaStream_t st_;
   char* ws_;
-  bool split_fwd, split_grad, split_ns, fused_ns;
+  bool split_fwd, split_grad, split_ns, fused_ns, mse = false;
+  bf16* Hk[2] = {nullptr, nullptr};
+  bf16* Y[2] = {nullptr, nullptr};
+  CUtensorMap mHk[2], sHk[2], mYf[2], mYg[2], mW2y[2];
+  const bf16* V_ = nullptr;
   float *M, *n0, *G, *splitbuf, *mom, *nsqg;
   bf16 *Ms, *Msl, *Hq, *E, *El;
   TcCommon cm;

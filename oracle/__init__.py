@@ -23,7 +23,14 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
                                 the full SwiGLU + Muon + weight-norm chain has no
                                 printed values to check against: parity unpinned
                                 beyond those compositions.
+  apply_inclusive (inclusive  - pinned (chunk-1 linear MSE = the delta rule read after
+  order)                        the update; linear inner product = causal linear
+                                attention for every chunk size; chunk-1 SwiGLU = the
+                                per-token recurrence; the SwiGLU matrix dual form)
+  linear_head_backward        - pinned (central finite differences of the forward
+                                oracle, every input, inner product and MSE, masks and
+                                ragged chunks)
 """
-from .ttt_oracle import (OracleCfg, chunk_grad, linear_apply, linear_grad,  # noqa: F401
-                         newton_schulz, row_norms, sigmoid, swiglu_apply, swiglu_grad,
-                         ttt_head, ttt_layer, update, weight_norm)
+from .ttt_oracle import (OracleCfg, apply_inclusive, chunk_grad, linear_apply,  # noqa: F401
+                         linear_grad, linear_head_backward, newton_schulz, row_norms, sigmoid,
+                         swiglu_apply, swiglu_grad, ttt_head, ttt_layer, update, weight_norm)

@@ -120,3 +120,13 @@ def _static_call(c, **over):
 def test_static_scratch_rejects_a_bad_status_word_before_launch(over):
     c = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"], impl=abi.TTT_IMPL_SIMT).cfg
     assert _static_call(c, **over) == abi.TTT_ERR_ARG
+
+
+def test_backward_covers_the_linear_net_with_plain_steps():
+    lin = abi.cfg_from_spec(synth.WORKLOADS["linear_chunk64"]).cfg
+    assert abi.ttt_bwd_workspace_bytes(lin) > 0
+    for spec in (synth.WORKLOADS["lm_chunk2k"], synth.WORKLOADS["linear_chunk64"].replace(mode="single")):
+        c = abi.cfg_from_spec(spec).cfg
+        with pytest.raises(abi.TTTError) as err:
+            abi.ttt_bwd_workspace_bytes(c)
+        assert err.value.code == abi.TTT_ERR_UNSUPPORTED

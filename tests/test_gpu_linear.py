@@ -22,6 +22,10 @@ CASES = {
     "odd_chunks": BASE.replace(name="lin_odd", update="odd", seed=65),
     "step_half": BASE.replace(name="lin_step", step=0.5, seed=66),
     "one_tile": BASE.replace(name="lin_one", T=64, seed=67),
+    # inclusive order (tutorial page §3): each query sees its own token's update
+    "inclusive_mse": BASE.replace(name="lin_incl_mse", mode="inclusive", seed=68),
+    "inclusive_ip_ragged": BASE.replace(name="lin_incl_ip", mode="inclusive", loss="ip", T=700, seed=69),
+    "inclusive_odd_step": BASE.replace(name="lin_incl_odd", mode="inclusive", update="odd", step=0.5, seed=70),
 }
 
 
@@ -30,6 +34,13 @@ def test_linear_matches_oracle(name):
     spec = CASES[name]
     x = synth.layer_inputs(spec)
     compare(spec, run_gpu(spec, x, impl=LIN), run_oracle(spec, x), TOL)
+
+
+def test_linear_inclusive_full_workload_sampled_heads():
+    """The full 256-head linear workload in the inclusive order on the linear
+    kernel; three heads against the oracle."""
+    spec = synth.WORKLOADS["linear_chunk64"].replace(mode="inclusive")
+    full_workload_check(spec, [(0, 0), (7, 9), (15, 15)], TOL, impl=LIN)
 
 
 def test_linear_is_selected_and_deterministic():

@@ -43,13 +43,38 @@ CASES = {
     "lr_per_matrix": BASE.replace(name="lr_per_matrix", lr_per_matrix=True, seed=55),
     "momentum_lr_odd_ragged": BASE.replace(name="momentum_lr_odd_ragged", T=700, chunk=200, update="odd",
                                            momentum=0.5, lr_per_matrix=True, seed=56),
+    # MSE loss (tutorial page §3; the modular-TTT abstract's loss choice) on the
+    # tensor-core path: Y = f(k) - v feeds the SwiGLU backward and G2
+    "mse": BASE.replace(name="mse", loss="mse", seed=57),
+    "mse_single_ragged": BASE.replace(name="mse_single_ragged", loss="mse", mode="single", T=700, chunk=700,
+                                      seed=58),
+    "mse_odd_momentum_rates": BASE.replace(name="mse_odd_momentum_rates", loss="mse", T=700, chunk=200,
+                                           update="odd", momentum=0.9, lr_per_matrix=True, seed=59),
+    "mse_d192_split_k": BASE.replace(name="mse_d192_split_k", loss="mse", d=192, dh=384, T=8192, chunk=8192,
+                                     mode="single", lr_a=0.005, seed=60),
+    "mse_sgd": BASE.replace(name="mse_sgd", loss="mse", muon=False, seed=61),
+    # novel-view synthesis (LaCT page §3.1, fig. 3d): one chunk over a set of
+    # views in which every fourth view is a target: its tokens only query
+    # (rate 0), the input views' tokens update
+    "nvs_strided": BASE.replace(name="nvs_strided", d=128, dh=256, T=4096, chunk=4096, mode="single",
+                                lr_a=0.005, seed=62),
 }
+
+# token rate masks of the cases above (1 = the token updates)
+RATE_MASKS = {"nvs_strided": lambda T: (np.arange(T) // 256) % 4 != 3}
+
+
+def _inputs(name):
+    spec = CASES[name]
+    x = synth.layer_inputs(spec)
+    if name in RATE_MASKS:
+        x["lr"] = x["lr"] * RATE_MASKS[name](spec.T).astype(np.float32)
+    return spec, x
 
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_tc_matches_oracle(name):
-    spec = CASES[name]
-    x = synth.layer_inputs(spec)
+    spec, x = _inputs(name)
     compare(spec, run_gpu(spec, x, impl=TC), run_oracle(spec, x), TOL)
 
 
@@ -61,7 +86,8 @@ def test_tc_single_precision_short(name):
 
 
 @pytest.mark.parametrize("wl,T,extra", [("lm_chunk2k", 4096, {}), ("video_ar", 2 * 5616, {}),
-                                        ("lm_chunk2k", 6144, {"momentum": 0.9, "lr_per_matrix": True})])
+                                        ("lm_chunk2k", 6144, {"momentum": 0.9, "lr_per_matrix": True}),
+                                        ("lm_chunk2k", 4096, {"loss": "mse"})])
 def test_tc_workload_shapes_short(wl, T, extra):
     """The workloads' own d, dh, chunk and head counts over their first chunks;
     the oracle checks the first and the last (b, h) head."""
