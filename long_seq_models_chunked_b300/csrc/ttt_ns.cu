@@ -37,8 +37,8 @@
 //   warp 0 (one lane)  TMA producer over a shared-memory ring (waits on the
 //                      completion counters before an item's loads);
 //   warp 1 (one lane)  tcgen05.mma issuer into one of two TMEM accumulators;
-//   warps 2..5         epilogue (TMEM -> registers -> fused math -> TMA stores)
-//                      and the SIMT items.
+//   warps 2..9         epilogue (TMEM -> registers -> fused math -> TMA stores),
+//                      two warps per TMEM lane quarter, each half of the columns
 // Operand precision: SPLIT carries X, R and P as bf16 (hi, lo) pairs and forms
 // each product from three MMAs (hi*hi + hi*lo + lo*hi); SINGLE uses one fp16
 // operand. Every wait is bounded (timeout -> status word, no trap); after an
@@ -57,10 +57,20 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kNsThreads = 192;
-constexpr int kEpiThreads = 128;  // warps 2..5
+// Eight epilogue warps, two per TMEM lane quarter: the first four take the
+// left half of a tile's columns, the other four the right half.
+constexpr int kEpiWarps = 8;
+constexpr int kColHalves = kEpiWarps / 4;
+constexpr int kNsThreads = 64 + 32 * kEpiWarps;
 constexpr int kAccCols = 256;     // columns of one TMEM accumulator buffer
-constexpr unsigned kArrivals = 4; // completion-counter arrivals per finished item
+constexpr unsigned kArrivals = kEpiWarps;  // completion-counter arrivals per finished item
+#ifndef TTT_NS_EPI_BUFS
+#define TTT_NS_EPI_BUFS 1
+#endif
+#ifndef TTT_NS_SPLIT_STAGES
+#define TTT_NS_SPLIT_STAGES 4
+#endif
+constexpr int kEpiBufs = TTT_NS_EPI_BUFS;  // 4 KB staging buffers per epilogue warp
 
 enum { K_GRAM = 0, K_POLY = 1, K_XUPD = 2 };
 
@@ -81,7 +91,7 @@ struct NsParams {
   bf16* Ms;         // bf16 shadow (hi)
   bf16* Msl;        // bf16 shadow (lo) or nullptr
   const float* n0;  // [Z][dh] reference row norms (W2: the first d entries)
-  float* rowpart;   // [Z][dh / BNX][d] partial sums of squares of the rows of M2, one per column tile
+  float* rowpart;   // [Z][dh / (BNX / 2)][d] partial sums of squares of the rows of M2, one per half column tile
   float* colpart;   // [Z][d / 32][dh] partial sums of squares of the columns of M1 / M3, one per 32 rows
   unsigned* cnt;    // [Z] completion counters (zeroed before the launch)
   // X0's operands are written before the launch. fused: UNSCALED (G, or the
@@ -118,10 +128,10 @@ struct NsGeom {
   static constexpr int kBmax = BNS > BNX ? BNS : BNX;
   static constexpr uint32_t kBBytes = (uint32_t)kBmax * kNsBK * 2;
   static constexpr uint32_t kStageBytes = kOps * (kNsABytes + kBBytes);
-  static constexpr int kStages = SPLIT ? 4 : 8;
-  // epilogue staging: two 4 KB buffers per epilogue warp (a 32 x 32 block as a
-  // bf16 pair, one fp16 operand, or fp32)
-  static constexpr uint32_t kEpiBytes = 4 * 2 * 4096;
+  static constexpr int kStages = SPLIT ? TTT_NS_SPLIT_STAGES : 8;
+  // epilogue staging: kEpiBufs 4 KB buffers per epilogue warp (a 32 x 32 block
+  // as a bf16 pair, one fp16 operand, or fp32)
+  static constexpr uint32_t kEpiBytes = kEpiWarps * kEpiBufs * 4096;
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kEpiBytes + 1024 + 512;
 };
 
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&accf[s], 1);
-      ptx::mbar_init(&acce[s], 4);  // one arrival per epilogue warp
+      ptx::mbar_init(&acce[s], kEpiWarps);  // one arrival per epilogue warp
     }
     ptx::mbar_init(drainb, 1);
     *abort_flag = 0;
@@ -444,8 +454,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;          // epilogue warp 0..7
     const int gq = warp & 3;          // TMEM lane group this warp may access
     const int r = 32 * gq + lane;     // accumulator row of this thread
+    const int eh = ew >> 2;           // which half of a tile's columns it takes
+    uint8_t* const ebuf = epi + (size_t)ew * kEpiBufs * 4096;
     uint32_t et_n = 0;                // GEMM tiles drained
     uint32_t es = 0;                  // staging buffers used (this warp)
     bool first = true;
@@ -493,7 +506,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
         float4 mA[8], mB[8];  // last X update: M of an even block and of the next one, loaded together
         // each 32 x 32 block of the warp goes through its staging buffer and
         // one TMA store per operand half; warp-uniform control flow
-        for (int c = 0; c < bn; c += 32) {
+        const int hw = bn / kColHalves;  // columns per half (a multiple of 64)
+        for (int c = eh * hw; c < (eh + 1) * hw; c += 32) {
           const int n = n0 + c;
           if (m_warp >= d || (!xu && n >= d)) continue;  // block outside the matrix
           ptx::tmem_ld32(ta + c, v);
@@ -501,8 +515,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= gscale;
           }
-          uint8_t* buf = epi + (size_t)(2 * gq + (es & 1u)) * 4096;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the store that used this buffer has read it
+          uint8_t* buf = ebuf + (size_t)(es % kEpiBufs) * 4096;
+          if (lane == 0) ptx::bulk_wait_read<kEpiBufs - 1>();  // the store that used this buffer has read it
           __syncwarp();
           const CUtensorMap* mh;
           const CUtensorMap* ml = nullptr;
@@ -530,7 +544,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
                 const float* mrow = p.M + (size_t)z * d * dh + (size_t)m * dh + n;
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) mA[q4] = ldcg4(mrow + 4 * q4);
-                if (c + 32 < bn) {
+                if (c + 32 < (eh + 1) * hw) {
 #pragma unroll
                   for (int q4 = 0; q4 < 8; ++q4) mB[q4] = ldcg4(mrow + 32 + 4 * q4);
                 }
@@ -567,8 +581,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
           // no computed tile is also written transposed, at (n, m_warp)
           if (!xu && p.sym && n > m_warp &&
               !sym_tile_needed(n / BM, m_warp / BNS, BNS)) {
-            uint8_t* tb = epi + (size_t)(2 * gq + (es & 1u)) * 4096;
-            if (lane == 0) ptx::bulk_wait_read<1>();
+            uint8_t* tb = ebuf + (size_t)(es % kEpiBufs) * 4096;
+            if (lane == 0) ptx::bulk_wait_read<kEpiBufs - 1>();
             __syncwarp();
             stage_op32_t<SPLIT>(tb, lane, v);
             ptx::fence_proxy_async_smem();
@@ -602,7 +616,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_fused_kernel(const __grid_co
             }
           }
         }
-        if (last && p.wnorm && j == 1 && row_ok) p.rowpart[((size_t)z * (dh / BNX) + n0 / BNX) * d + m] = rs;
+        if (last && p.wnorm && j == 1 && row_ok)
+          p.rowpart[((size_t)z * (dh / hw) + n0 / hw + eh) * d + m] = rs;
         ptx::tc_fence_before();
         ptx::fence_proxy_async_global();
         __syncwarp();
@@ -844,7 +859,7 @@ int launch_ns(NsParams& p, cudaStream_t st) {
   if (!p.wnorm) return TTT_OK;
   WnormParams w{};
   w.M = p.M; w.Ms = p.Ms; w.Msl = p.Msl; w.n0 = p.n0; w.rowpart = p.rowpart; w.colpart = p.colpart;
-  w.d = p.d; w.dh = p.dh; w.bnx = BNX; w.eps = p.wnorm_eps;
+  w.d = p.d; w.dh = p.dh; w.bnx = BNX / kColHalves; w.eps = p.wnorm_eps;
   const size_t wsm = (size_t)std::max(32, p.dh) * sizeof(float);
   if (wsm > 48 * 1024 &&
       cudaFuncSetAttribute(ns_wnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm) != cudaSuccess)
@@ -988,7 +1003,7 @@ int ns_build_params(const NsFusedArgs& a, NsParams& p) {
   p.Msl = static_cast<bf16*>(a.Msl);
   p.n0 = a.n0;
   p.rowpart = a.scratch;
-  p.colpart = p.rowpart + (size_t)Z * (dh / 128) * d;
+  p.colpart = p.rowpart + (size_t)Z * (dh / 64) * d;
   p.cnt = reinterpret_cast<unsigned*>(p.colpart + (size_t)Z * (d / 32) * dh);
   // a + b s + c s^2 = c (s + beta)^2 + alpha
   p.c = g.ns_c;
@@ -1039,9 +1054,9 @@ int ns_fused_plan(const ttt_cfg& g, int* resident) {
 
 size_t ns_fused_scratch_floats(const ttt_cfg& g, int Z) {
   // partial sums: of the rows of M2 per
-  // column tile (at most dh / 128 tiles), of the columns of M1 / M3 per 32 rows;
-  // then the per-matrix completion counters
-  return (size_t)Z * ((size_t)(g.dh / 128) * g.d + (size_t)(g.d / 32) * g.dh) + (size_t)Z + 64;
+  // half column tile (at most dh / 64 of them), of the columns of M1 / M3 per
+  // 32 rows; then the per-matrix completion counters
+  return (size_t)Z * ((size_t)(g.dh / 64) * g.d + (size_t)(g.d / 32) * g.dh) + (size_t)Z + 64;
 }
 
 }  // namespace ttt

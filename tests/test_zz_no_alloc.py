@@ -87,7 +87,7 @@ def test_static_scratch_matches_oracle():
     from parity import compare, run_oracle, to_f64
     for spec in SPECS:
         holder = abi.cfg_from_spec(spec, impl=abi.TTT_IMPL_SIMT)
-        host = synth.layer_inputs(spec, exact=False)
+        host = synth.layer_inputs(spec)
         O_s, Wf_s = _static_call(holder, _inputs(spec))
         gpu = (to_f64(O_s, spec), [w.double().cpu().numpy() for w in Wf_s])
         compare(spec, gpu, run_oracle(spec, host), TOL)
