@@ -40,17 +40,22 @@ std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch wit
 
 
 // ============================================================ forward, multicast
-// Forward of the fast net on 128-token x 64-hidden tiles (LaCT page §2.1): the
-// clusters' CTAs take consecutive token tiles of one (b, h, hidden slice) and
-// share that slice's weights by TMA multicast (each CTA loads a share of the
-// weight boxes); the token rows are each CTA's own.
-//   query tile: [A|B] = Q [W1;W3]^T -> H_q = silu(A) * B                 (apply-1)
-//   key tile:   [A|B] = K [W1;W3]^T, Dm = Y W2 -> DA, He, DB (SwiGLU backward,
-//               scaled by each token's rates), the gradient kernel's E operand;
-//               Y = dl/df = -V for the inner-product loss, f(k) - V for MSE
-//   key-hidden tile (MSE): [A|B] = K [W1;W3]^T -> H_k = silu(A) * B as split
-//               operands, from which the next kernel forms Y = H_k W2^T - V
-// TMEM: [A|B] in columns 0-127, Dm in 128-191 of one 256-column accumulator.
+// Forward of the fast net on 128-token tiles (LaCT page §2.1): the clusters'
+// CTAs take consecutive token tiles of one (b, h, hidden slice) and share that
+// slice's weights by TMA multicast (each CTA loads a share of the weight
+// boxes); the token rows are each CTA's own.
+//   query tile (128 hidden): [A|B] = Q [W1;W3]^T -> H_q = silu(A) * B    (apply-1)
+//   key tile (64 hidden):    [A|B] = K [W1;W3]^T, Dm = Y W2 -> DA, He, DB (SwiGLU
+//               backward, scaled by each token's rates), the gradient kernel's E
+//               operand; Y = dl/df = -V for the inner-product loss, f(k) - V for MSE
+//   key-hidden tile (64 hidden, MSE): [A|B] = K [W1;W3]^T -> H_k = silu(A) * B as
+//               split operands, from which the next kernel forms Y = H_k W2^T - V
+// Every MMA of a query tile is N = 256 and the split weight halves of the Dm
+// product share one N = 128 MMA (W2 hi | W2 lo side by side): one thread issues
+// the MMAs, and products narrower than that leave the tensor pipe waiting on
+// the issuing thread between k-blocks.
+// TMEM of one 256-column accumulator: query [A|B] in columns 0-255; key and
+// key-hidden [A|B] in 0-127, Dm (hi part, lo part) in 128-191 and 192-255.
 struct FwdMcOp {
   struct Params {
     CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
@@ -62,7 +67,7 @@ struct FwdMcOp {
     bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
     bf16* El;                // low halves of E (split precision)
     int d, dh, T, Cp, chunk_start, valid;
-    int n_tok, groups, n_js, BH, cs;
+    int n_tok, groups, n_jq, BH, cs;  // n_jq: 128-wide hidden slices
     int q, k, h;             // which kinds of tiles this launch computes (query, key, key-hidden)
     int w_split, e_split;
     int lr_stride;           // 1: one rate per token; 3: one per token and matrix (W1, W2, W3)
@@ -72,7 +77,7 @@ struct FwdMcOp {
     TcCommon cm;
   };
   struct Tile {
-    int bh, js, tok, kind;   // kind: 0 query, 1 key, 2 key-hidden
+    int bh, hid0, tok, kind;  // kind: 0 query (128 hidden), 1 key, 2 key-hidden (64 hidden)
     bool is_k, real;
   };
   static constexpr int kStages = 4;
@@ -80,30 +85,36 @@ struct FwdMcOp {
   static constexpr int kAccCols = 256;
   static constexpr uint32_t kEpiBytes = 4 * 2 * 4096;  // two 4 KB staging buffers per epilogue warp
 
-  static __device__ int num_work(const Params& p) { return p.BH * p.n_js * p.groups * (p.q + p.k + p.h); }
+  // items per (b, h, 128-wide hidden slice, token group): one query tile, two
+  // key-hidden tiles, two key tiles (those the launch computes)
+  static __device__ int n_sub(const Params& p) { return p.q + 2 * p.h + 2 * p.k; }
+  static __device__ int num_work(const Params& p) { return p.BH * p.n_jq * p.groups * n_sub(p); }
   static __device__ void tile_of(const Params& p, int w, int rank, Tile& t) {
-    const int kinds = p.q + p.k + p.h;
-    const int kind = w % kinds;
-    w /= kinds;
-    // the kind-th enabled kind, in the order query, key, key-hidden
-    int c = 0;
-    t.kind = 0;
-    if (p.q) { if (c == kind) t.kind = 0; ++c; }
-    if (p.k) { if (c == kind) t.kind = 1; ++c; }
-    if (p.h) { if (c == kind) t.kind = 2; ++c; }
-    t.is_k = t.kind == 1;
+    const int ns = n_sub(p);
+    int c = w % ns;
+    w /= ns;
     const int g = w % p.groups;
     w /= p.groups;
-    t.js = w % p.n_js;
-    t.bh = w / p.n_js;
+    const int jq = w % p.n_jq;
+    t.bh = w / p.n_jq;
+    t.hid0 = jq * 128;
+    if (c < p.q) {
+      t.kind = 0;
+    } else {
+      c -= p.q;
+      t.kind = (p.h && c < 2) ? 2 : 1;
+      t.hid0 += 64 * (c & 1);
+    }
+    t.is_k = t.kind == 1;
     t.tok = g * p.cs + rank;
     t.real = t.tok < p.n_tok;
   }
   static __device__ int num_kblocks(const Params& p, const Tile& t) { return (t.is_k ? 2 : 1) * (p.d / BK); }
-  // weight boxes of k-block kb: queries [W1, W3] (hi); keys and key hiddens,
-  // segment 0 [W1 hi, W3 hi, W1 lo, W3 lo]; keys, segment 1 [W2 hi, W2 lo]
+  // weight boxes of k-block kb: queries [W1, W1', W3, W3'] (hi; ' = the next
+  // 64 hidden); keys and key hiddens, segment 0 [W1 hi, W3 hi, W1 lo, W3 lo];
+  // keys, segment 1 [W2 hi, W2 lo]
   static __device__ int n_boxes(const Params& p, const Tile& t, int kb) {
-    if (t.kind == 0) return 2;
+    if (t.kind == 0) return 4;
     return (kb < p.d / BK ? 2 : 1) * (p.w_split ? 2 : 1);
   }
   static __device__ bool y_seg(const Params& p, const Tile& t, int kb) { return p.mse && t.is_k && kb >= p.d / BK; }
@@ -127,15 +138,22 @@ struct FwdMcOp {
     const int z = t.bh * 3;
     const int nb = n_boxes(p, t, kb);
     for (int b = rank; b < nb; b += cs) {
-      const bool lo = seg1 ? b == 1 : b >= 2;
-      const int zz = seg1 ? z + 1 : z + ((b & 1) ? 2 : 0);
-      ptx::tma_load_3d_shared(st + kABytes + (b + wslot) * kBox, lo ? &p.mWl : &p.mW, bar, t.js * 64, k, zz, mask);
+      const bool q = t.kind == 0;
+      const bool lo = q ? false : seg1 ? b == 1 : b >= 2;
+      const int zz = q ? z + (b >= 2 ? 2 : 0) : seg1 ? z + 1 : z + ((b & 1) ? 2 : 0);
+      const int col = t.hid0 + (q ? 64 * (b & 1) : 0);
+      ptx::tma_load_3d_shared(st + kABytes + (b + wslot) * kBox, lo ? &p.mWl : &p.mW, bar, col, k, zz, mask);
     }
   }
   static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
     const int nk = p.d / BK;
     const uint32_t a = st, b = st + kABytes;
-    if (!t.is_k || kb < nk) {
+    if (t.kind == 0) {
+      // [A|B] over 128 hidden: one N = 256 MMA per 16 of K
+      constexpr uint32_t id = ptx::idesc_bf16(128, 256, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b, kk), id, (kb | kk) != 0);
+    } else if (kb < nk) {
       constexpr uint32_t id = ptx::idesc_bf16(128, 128, false, true);
       const bool two = t.kind != 0 && p.w_split;
 #pragma unroll
@@ -144,23 +162,28 @@ struct FwdMcOp {
         if (two) ptx::mma_bf16(tmem, kdesc(a, kk), mdesc(b + 2 * kBox, kk), id, 1u);
       }
     } else if (p.mse) {
-      // Dm = Y W2 with both split: Yh W2h + Yh W2l + Yl W2h
+      // Dm = Y W2 with both split: Yh [W2h | W2l] (N = 128: the hi part in
+      // columns 128-191, the lo part in 192-255) + Yl W2h (into the hi part)
       const int k2 = kb - nk;
-      constexpr uint32_t id = ptx::idesc_bf16(128, 64, false, true);
-      const uint32_t yl = st + kABytes, wh = st + kABytes + 2 * kBox, wl = wh + kBox;
+      constexpr uint32_t id2 = ptx::idesc_bf16(128, 128, false, true);
+      constexpr uint32_t id1 = ptx::idesc_bf16(128, 64, false, true);
+      const uint32_t yl = st + kABytes, wh = st + kABytes + 2 * kBox;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(wh, kk), id, (k2 | kk) != 0);
-        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(wl, kk), id, 1u);
-        ptx::mma_bf16(tmem + 128, kdesc(yl, kk), mdesc(wh, kk), id, 1u);
+        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(wh, kk), id2, (k2 | kk) != 0);
+        ptx::mma_bf16(tmem + 128, kdesc(yl, kk), mdesc(wh, kk), id1, 1u);
       }
     } else {
+      // Dm = V [W2h | W2l] (N = 128, hi and lo parts side by side), or V W2h
       const int k2 = kb - nk;
-      constexpr uint32_t id = ptx::idesc_bf16(128, 64, false, true);
+      if (p.w_split) {
+        constexpr uint32_t id = ptx::idesc_bf16(128, 128, false, true);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
-        if (p.w_split) ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b + kBox, kk), id, 1u);
+        for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
+      } else {
+        constexpr uint32_t id = ptx::idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) ptx::mma_bf16(tmem + 128, kdesc(a, kk), mdesc(b, kk), id, (k2 | kk) != 0);
       }
     }
   }
@@ -191,7 +214,7 @@ struct FwdMcOp {
     const int tl = t.tok * BM + r;        // token index inside the chunk
     const int row0 = tl - lane;           // this warp's first row (warp-uniform)
     const bool valid = tl < p.valid;
-    const int j0 = t.js * 64;
+    const int j0 = t.hid0;
     // stage one 32 x 32 block and store it at (column x, this warp's rows, plane z)
     auto put = [&](const float* v, bool lo, const CUtensorMap* mh, const CUtensorMap* ml, int x, int z) {
       uint8_t* buf = epi + (es & 1u) * 4096u;
@@ -213,9 +236,10 @@ struct FwdMcOp {
     float va[32], vb[32];
     if (!t.is_k) {
       const bool hk = t.kind == 2;  // key hiddens: split operands of the MSE's Y = H_k W2^T - V
-      for (int c = 0; c < 64; c += 32) {
+      const int wa = hk ? 64 : 128;  // hidden columns of the tile: A in [0, wa), B in [wa, 2 wa)
+      for (int c = 0; c < wa; c += 32) {
         ptx::tmem_ld32(tm + c, va);
-        ptx::tmem_ld32(tm + 64 + c, vb);
+        ptx::tmem_ld32(tm + wa + c, vb);
 #pragma unroll
         for (int i = 0; i < 32; ++i) va[i] = valid ? va[i] * sigmoid_fast(va[i]) * vb[i] : 0.f;
         if (hk)
@@ -233,6 +257,11 @@ struct FwdMcOp {
         ptx::tmem_ld32(tm + 64 + c, vb);
         ptx::tmem_ld32(tm + 128 + c, vd);
         float oh[32];
+        if (p.w_split) {  // Dm's lo part
+          ptx::tmem_ld32(tm + 192 + c, oh);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) vd[i] += oh[i];
+        }
         // inner product: Dm = V W2 and dl/dh = -Dm, G2 = V^T (-lr2 H);
         // MSE: Dm = Y W2 = dl/dh, G2 = Y^T (lr2 H)
         const float sgn = p.mse ? 1.f : -1.f;
@@ -1161,7 +1190,7 @@ class TcLayer {
     // build without multicast runs clusters of one
     p.cs = (TTT_HAS_MULTICAST && p.n_tok >= 2) ? 2 : 1;
     p.groups = (p.n_tok + p.cs - 1) / p.cs;
-    p.n_js = g_.dh / 64;
+    p.n_jq = g_.dh / 128;
     p.BH = P.BH;
     p.q = q ? 1 : 0;
     p.k = k ? 1 : 0;
@@ -1174,7 +1203,7 @@ class TcLayer {
     p.e_split = split_grad ? 1 : 0;
     p.cm = cm;
     p.cm.stall = g_stall_next_fwd.exchange(0);
-    const int n_work = P.BH * p.n_js * p.groups * (p.q + p.k + p.h);
+    const int n_work = P.BH * p.n_jq * p.groups * (p.q + 2 * p.h + 2 * p.k);
     return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
   }
 
