@@ -79,6 +79,13 @@ TTT_API void ttt_dbg_stall_next_linear(void);
  * starts from W0 again and is unaffected. */
 TTT_API void ttt_dbg_stall_next_fwd(void);
 
+/* Whether the chunk gradient runs on CTA pairs (1, the default; cta_group::2
+ * MMAs of 256 x 256, each CTA holding half of E's columns) or on clusters of
+ * one-CTA tiles that share E by multicast (0). Only the single-GPU build has
+ * the pair kernel; the other build ignores the setting. Process-global, for
+ * tests and tuning. Returns TTT_OK or TTT_ERR_ARG. */
+TTT_API int ttt_dbg_grad_pairs(int on);
+
 /* Failure-detection test: in the next launch of the fused Muon kernel CTA 0
  * never signals the completion of its first item, so the items of that
  * matrix's next phase wait until their bounded waits run out; TTT_ERR_TIMEOUT

@@ -44,7 +44,8 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_dbg_split_mask", "ttt_dbg_stall_next_linear", "ttt_dbg_ns_trace",
             "ttt_dbg_ns_trace_read", "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns", "ttt_build_features",
             "ttt_dbg_ns_symmetric", "ttt_cp_workspace_bytes", "ttt_cp_begin", "ttt_cp_grad", "ttt_cp_update",
-            "ttt_cp_apply", "ttt_cp_end", "ttt_dbg_ns_tiles", "ttt_bwd_workspace_bytes", "ttt_bwd")
+            "ttt_cp_apply", "ttt_cp_end", "ttt_dbg_ns_tiles", "ttt_bwd_workspace_bytes", "ttt_bwd",
+            "ttt_dbg_grad_pairs")
 TTT_FEATURE_CLUSTER_MULTICAST = 1
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
@@ -120,6 +121,8 @@ def _load():
     lib.ttt_dbg_ns_tiles.restype = c_int
     lib.ttt_dbg_ns_symmetric.argtypes = [c_int]
     lib.ttt_dbg_ns_symmetric.restype = c_int
+    lib.ttt_dbg_grad_pairs.argtypes = [c_int]
+    lib.ttt_dbg_grad_pairs.restype = c_int
     lib.ttt_dbg_ns_trace.argtypes = [c_int]
     lib.ttt_dbg_ns_trace.restype = c_int
     lib.ttt_dbg_ns_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), c_int]
@@ -328,6 +331,14 @@ def ttt_dbg_ns_symmetric(on: int) -> int:
     """Test hook: symmetric (upper-triangle) tiles in the fused Muon kernel:
     1 always, 0 never, -1 chosen by the shape (the default)."""
     return _lib.ttt_dbg_ns_symmetric(int(on))
+
+
+def ttt_dbg_grad_pairs(on: bool) -> None:
+    """Test hook: the chunk gradient on CTA pairs (on, the default in the
+    single-GPU build) or on one-CTA clusters sharing E by multicast (off)."""
+    rc = _lib.ttt_dbg_grad_pairs(int(bool(on)))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_dbg_grad_pairs")
 
 
 def ttt_dbg_ns_tiles(bns: int, bnx: int) -> None:

@@ -26,6 +26,7 @@
 #include "../../include/ttt_debug.h"
 #include "tc_kernel.cuh"
 #include "tc_mc.cuh"
+#include "tc_pair.cuh"
 #include "tc_util.cuh"
 #include "ttt_internal.h"
 #include "ttt_ns.h"
@@ -37,6 +38,7 @@ using namespace tcu;
 
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
 std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch withholds its loads
+bool g_grad_pairs = true;               // test hook: the chunk gradient on CTA pairs (single-GPU build)
 
 
 // ============================================================ forward, multicast
@@ -562,6 +564,74 @@ struct GradMcOp {
   }
 };
 
+#if TTT_HAS_MULTICAST
+// ============================================================ chunk gradients on CTA pairs
+// The gradient of GradMcOp<256, MSE> on CTA pairs: a pair computes rows
+// [256 g, +256) of G_z^T (each CTA its 128, row group g of ceil(d / 256)) and
+// 256 columns; each CTA holds its 128 rows of the K / V (or Y) operand and
+// half of E's 256 columns, so it takes 24 KB (MSE's G2: 32 KB) per 32 tokens
+// instead of the 40 KB of a one-CTA tile, and every pair MMA is 256 x 256 x 16.
+// The row groups, token splits and the epilogue are GradMcOp's (with cs = 2).
+template <bool MSE = false>
+struct GradPairOp {
+  using Base = GradMcOp<256, MSE>;
+  using Params = typename Base::Params;
+  using Tile = typename Base::Tile;
+  using Pre = typename Base::Pre;
+  static constexpr int kTok = Base::kTok;
+  static constexpr uint32_t kBoxG = Base::kBoxG;  // one 64 x 32 box
+  static constexpr uint32_t kAB = 2 * kBoxG;      // this CTA's 128 rows of A
+  static constexpr uint32_t kEH = 2 * kBoxG;      // this CTA's 128 columns of one half of E
+  static constexpr int kStageBytes = kAB + 2 * kEH + (MSE ? kAB : 0);
+  static constexpr int kStages = MSE ? 6 : 8;  // 192 KB
+  static constexpr int kAccCols = 256;
+  static constexpr uint32_t kEpiBytes = 0;
+
+  static __device__ int num_work(const Params& p) { return Base::num_work(p); }
+  static __device__ void tile_of(const Params& p, int w, int prank, Tile& t) { Base::tile_of(p, w, prank, t); }
+  static __device__ int num_kblocks(const Params& p, const Tile& t) { return t.nkb; }
+  static __device__ uint32_t stage_tx(const Params& p, const Tile& t, int) {
+    return kAB + (p.e_split ? 2u : 1u) * kEH + ((MSE && t.j == 1) ? kAB : 0u);
+  }
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint32_t fb, int prank) {
+    const int tok = (t.kb0 + kb) * kTok;
+    for (int g = 0; g < 2; ++g) {
+      if (MSE && t.j == 1) {
+        ptx::tma_load_3d_pair(st + g * kBoxG, &p.mY, fb, t.m0 + g * 64, tok, t.bh);
+        ptx::tma_load_3d_pair(st + kAB + 2 * kEH + g * kBoxG, &p.mYl, fb, t.m0 + g * 64, tok, t.bh);
+      } else if (p.use4d) {
+        ptx::tma_load_4d_pair(st + g * kBoxG, t.j == 1 ? &p.mV4 : &p.mK4, fb, t.m0 + g * 64, tok, p.chunk_idx, t.bh);
+      } else {
+        ptx::tma_load_3d_pair(st + g * kBoxG, t.j == 1 ? &p.mV3 : &p.mK3, fb, t.m0 + g * 64, p.chunk_start + tok,
+                              t.bh);
+      }
+      // this CTA's half of E: columns n0 + 128 prank + [0, 128)
+      const int col = t.n0 + 128 * prank + 64 * g;
+      ptx::tma_load_3d_pair(st + kAB + g * kBoxG, &p.mE, fb, col, tok, t.z);
+      if (p.e_split) ptx::tma_load_3d_pair(st + kAB + kEH + g * kBoxG, &p.mEl, fb, col, tok, t.z);
+    }
+  }
+  static __device__ void consume(const Params& p, const Tile& t, int kb, uint32_t st, uint32_t tmem) {
+    constexpr uint32_t id = ptx::idesc_bf16(256, 256, true, true);
+    const uint32_t eh = st + kAB, el = eh + kEH;
+    const bool ylo = MSE && t.j == 1;
+#pragma unroll
+    for (int kk = 0; kk < kTok / 16; ++kk) {
+      const uint64_t a = ptx::sdesc(st + kk * 2048, kBoxG, 1024);
+      const uint64_t bh = ptx::sdesc(eh + kk * 2048, kBoxG, 1024);
+      ptx::mma2_bf16(tmem, a, bh, id, (kb | kk) != 0);
+      if (p.e_split) ptx::mma2_bf16(tmem, a, ptx::sdesc(el + kk * 2048, kBoxG, 1024), id, 1u);
+      if (ylo) ptx::mma2_bf16(tmem, ptx::sdesc(st + kAB + 2 * kEH + kk * 2048, kBoxG, 1024), bh, id, 1u);
+    }
+  }
+  static __device__ Pre pre(const Params& p, const Tile& t, int r) { return Base::pre(p, t, r); }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t* epi, uint32_t& es,
+                                  const Pre& pr) {
+    Base::epilogue(p, t, tm, r, epi, es, pr);
+  }
+};
+#endif  // TTT_HAS_MULTICAST
+
 // ============================================================ plain GEMM (test hook)
 template <bool AMN, bool BMN>
 struct PlainOp {
@@ -888,6 +958,69 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
   prof_after(kind, st);
   return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
+
+#if TTT_HAS_MULTICAST
+// CTA pairs of the pair engine that fit on the device at once (cached per operation).
+template <class Op>
+int pair_max(int* out) {
+  static int cached = 0, cached_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TTT_ERR_CUDA;
+  if (cached_dev != dev) {
+    auto kern = tc_pair_kernel<Op>;
+    const size_t smem = tc_pair_smem_bytes<Op>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return TTT_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return TTT_ERR_CUDA;
+    }
+    cached = n;
+    cached_dev = dev;
+  }
+  *out = cached;
+  return TTT_OK;
+}
+
+// Persistent pair launch: one pair per work item up to the device's capacity.
+template <class Op>
+int launch_pair(int kind, const typename Op::Params& p, int n_work, cudaStream_t st) {
+  auto kern = tc_pair_kernel<Op>;
+  const size_t smem = tc_pair_smem_bytes<Op>();
+  int max_pairs = 0;
+  const int rc = pair_max<Op>(&max_pairs);
+  if (rc != TTT_OK) return rc;
+  const int n_pairs = std::max(1, std::min(n_work, max_pairs));
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2 * n_pairs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  prof_before(kind, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  prof_after(kind, st);
+  return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+#endif  // TTT_HAS_MULTICAST
 
 // A side stream (and two events) per device and host thread, created on first
 // use, for the apply that overlaps the gradient. Returns NULL if it cannot be
@@ -1265,6 +1398,49 @@ class TcLayer {
       TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, dst, splits, n));
       return TTT_OK;
     };
+#if TTT_HAS_MULTICAST
+    // CTA pairs when the columns come in 256-wide tiles and the rows in pairs
+    // of 128 (a pair half past d would idle; d = 640 runs faster on clusters)
+    if (g_grad_pairs && P.g_bn == 256 && d % (2 * BM) == 0) {
+      auto launch2 = [&](auto op) -> int {
+        using Op = decltype(op);
+        int max_pairs = 0;
+        const int rc = pair_max<Op>(&max_pairs);
+        if (rc != TTT_OK) return rc;
+        const int mg2 = (d + 2 * BM - 1) / (2 * BM);
+        const int items2 = Z * P.g_nt * mg2;
+        int splits = std::max(1, std::min({P.g_splits_max, kbs / 16, max_pairs / items2}));
+        const int kb_per_split = (kbs + splits - 1) / splits;
+        splits = (kbs + kb_per_split - 1) / kb_per_split;
+        typename Op::Params p{};
+        p.mK4 = mK4; p.mV4 = mV4; p.mK3 = mK3; p.mV3 = mV3; p.mE = mE[0]; p.mEl = mE[1];
+        p.G = dst; p.split_out = splitbuf;
+        p.d = d; p.dh = dh; p.Z = Z; p.chunk_idx = ci; p.chunk_start = s; p.valid = valid; p.use4d = full ? 1 : 0;
+        p.nt = P.g_nt; p.splits = splits; p.kb_per_split = kb_per_split; p.e_split = split_grad ? 1 : 0; p.cm = cm;
+        p.mg = mg2; p.cs = 2;
+        if (mse) {
+          p.mY = mYg[0];
+          p.mYl = mYg[1];
+        }
+        if (to_ns) {
+          p.Xh = static_cast<bf16*>(nsa.Xh[0]);
+          p.Xl = static_cast<bf16*>(nsa.Xl[0]);
+          p.mom = mom;
+          p.mu = g_.momentum;
+          p.nsq = nsqg;
+        }
+        const int r = launch_pair<Op>(TTT_KERNEL_GRAD, p, items2 * splits, st_);
+        if (r != TTT_OK || splits == 1) return r;
+        const size_t n = (size_t)Z * d * dh;
+        cudaStream_t st = st_;
+        if (to_ns)
+          return ns_input_launch(splitbuf, splits, Z, d, dh, P.g_bn, mom, g_.momentum, nsa.Xh[0], nsa.Xl[0], nsqg, st);
+        TTT_LAUNCH(TTT_KERNEL_GRAD, st, gsplit_reduce_kernel<<<4 * kNumSmsHint, 256, 0, st>>>(splitbuf, dst, splits, n));
+        return TTT_OK;
+      };
+      return mse ? launch2(GradPairOp<true>{}) : launch2(GradPairOp<false>{});
+    }
+#endif
     if (mse) return P.g_bn == 256 ? launch(GradMcOp<256, true>{}) : launch(GradMcOp<128, true>{});
     return P.g_bn == 256 ? launch(GradMcOp<256>{}) : launch(GradMcOp<128>{});
   }
@@ -1526,4 +1702,10 @@ extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, i
 extern "C" int ttt_build_features(void) { return TTT_HAS_MULTICAST ? TTT_FEATURE_CLUSTER_MULTICAST : 0; }
 
 extern "C" void ttt_dbg_stall_next_fwd(void) { ttt::g_stall_next_fwd.store(1); }
+
+extern "C" int ttt_dbg_grad_pairs(int on) {
+  if (on != 0 && on != 1) return TTT_ERR_ARG;
+  ttt::g_grad_pairs = on != 0;
+  return TTT_OK;
+}
 

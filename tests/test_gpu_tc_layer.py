@@ -58,6 +58,12 @@ CASES = {
     # (rate 0), the input views' tokens update
     "nvs_strided": BASE.replace(name="nvs_strided", d=128, dh=256, T=4096, chunk=4096, mode="single",
                                 lr_a=0.005, seed=62),
+    # the chunk gradient on CTA pairs (256-wide column tiles, row pairs): MSE's
+    # computed operand and token splits; d = 384 stays on the one-CTA tiles
+    "mse_pair_d256": BASE.replace(name="mse_pair_d256", loss="mse", d=256, dh=512, T=1024, chunk=256, seed=63),
+    "pair_d384_ragged": BASE.replace(name="pair_d384_ragged", d=384, dh=512, T=900, chunk=256, seed=64),
+    "pair_split_k": BASE.replace(name="pair_split_k", d=256, dh=512, T=8192, chunk=8192, mode="single",
+                                 lr_a=0.005, seed=65),
 }
 
 # token rate masks of the cases above (1 = the token updates)
@@ -132,6 +138,21 @@ def test_tc_is_deterministic():
     a = run_gpu(spec, x, impl=TC)
     b = run_gpu(spec, x, impl=TC)
     assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
+
+
+@pytest.mark.parametrize("name", ["pair_d256", "mse_pair_d256", "pair_d384_ragged", "pair_split_k"])
+def test_gradient_pairs_equal_one_cta_tiles(name):
+    """The chunk gradient on CTA pairs (the default) gives bit for bit what the
+    one-CTA tiles sharing E by multicast give: the same products, accumulated
+    in the same order."""
+    spec, x = _inputs(name)
+    got = run_gpu(spec, x, impl=TC)
+    try:
+        abi.ttt_dbg_grad_pairs(False)
+        ref = run_gpu(spec, x, impl=TC)
+    finally:
+        abi.ttt_dbg_grad_pairs(True)
+    assert np.array_equal(got[0], ref[0]) and all(np.array_equal(p, q) for p, q in zip(got[1], ref[1])), name
 
 
 @pytest.mark.parametrize("ctas", [5, 37])
