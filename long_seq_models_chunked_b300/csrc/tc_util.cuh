@@ -44,12 +44,26 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Two values as a bf16 pair (hi = bf16(x), rounded to nearest) and the pair of
+// their remainders (lo = bf16(x - hi)); hi is read back from its packed bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& h, uint32_t& l) {
+  h = pack_bf16(a, b);
+  l = pack_bf16(a - __uint_as_float(h << 16), b - __uint_as_float(h & 0xffff0000u));
+}
+
 __device__ __forceinline__ void st_bf16pair32(bf16* hi, bf16* lo, const float* v) {
-  float l[32];
+  uint4* dh = reinterpret_cast<uint4*>(hi);
+  uint4* dl = reinterpret_cast<uint4*>(lo);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
-  st_bf16x32(hi, v);
-  st_bf16x32(lo, l);
+  for (int q = 0; q < 4; ++q) {
+    uint4 h, l;
+    split_bf16x2(v[8 * q + 0], v[8 * q + 1], h.x, l.x);
+    split_bf16x2(v[8 * q + 2], v[8 * q + 3], h.y, l.y);
+    split_bf16x2(v[8 * q + 4], v[8 * q + 5], h.z, l.z);
+    split_bf16x2(v[8 * q + 6], v[8 * q + 7], h.w, l.w);
+    dh[q] = h;
+    dl[q] = l;
+  }
 }
 
 __device__ __forceinline__ void st_f32x32(float* dst, const float* v) {
@@ -70,20 +84,20 @@ template <bool LO>
 __device__ __forceinline__ void stage_bf16x32(uint8_t* buf, int lane, const float* v) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint4 h;
-    h.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-    h.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    h.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    h.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(buf + stage_off64(lane, q)) = h;
+    uint4 h, l;
     if (LO) {
-      uint4 l;
-      l.x = pack_bf16(bf_rest(v[8 * q + 0]), bf_rest(v[8 * q + 1]));
-      l.y = pack_bf16(bf_rest(v[8 * q + 2]), bf_rest(v[8 * q + 3]));
-      l.z = pack_bf16(bf_rest(v[8 * q + 4]), bf_rest(v[8 * q + 5]));
-      l.w = pack_bf16(bf_rest(v[8 * q + 6]), bf_rest(v[8 * q + 7]));
+      split_bf16x2(v[8 * q + 0], v[8 * q + 1], h.x, l.x);
+      split_bf16x2(v[8 * q + 2], v[8 * q + 3], h.y, l.y);
+      split_bf16x2(v[8 * q + 4], v[8 * q + 5], h.z, l.z);
+      split_bf16x2(v[8 * q + 6], v[8 * q + 7], h.w, l.w);
       *reinterpret_cast<uint4*>(buf + 2048 + stage_off64(lane, q)) = l;
+    } else {
+      h.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+      h.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+      h.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+      h.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
     }
+    *reinterpret_cast<uint4*>(buf + stage_off64(lane, q)) = h;
   }
 }
 
