@@ -12,7 +12,9 @@
 // tiles, so the epilogue of one tile overlaps the MMAs of the next.
 //
 //   warp 0 (one lane)  TMA producer;  warp 1 (one lane)  MMA issuer (and TMEM
-//   allocation);  warps 2..5  epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+//   allocation);  warps 2..(1 + kEpiWarps)  epilogue (warp w reads TMEM lanes
+//   32*(w%4)..+31; with eight epilogue warps, two per lane quarter, each takes
+//   one half of the tile's columns).
 //
 // Every wait is bounded by the caller's timeout; after an abort each role
 // stops, the producer waits (bounded) for its own copies, the MMA warp for its
@@ -21,7 +23,7 @@
 //
 // An operation `Op` provides:
 //   Params (with a `TcCommon cm` member), Tile;
-//   static constexpr int kStages, kStageBytes, kAccCols (<= 256);
+//   static constexpr int kStages, kStageBytes, kAccCols (<= 256), kEpiWarps (4 or 8);
 //   static __device__ int  num_work(const Params&);
 //   static __device__ void tile_of(const Params&, int item, int rank, Tile&);
 //   static __device__ int  num_kblocks(const Params&, const Tile&)   (same for every rank of an item)
@@ -36,9 +38,10 @@
 //        values the epilogue needs from global memory, loaded before the
 //        accumulator wait (so their latency hides under the tile's MMAs)
 //   static __device__ void epilogue(const Params&, const Tile&, uint32_t tmem_lane_base, int row,
-//                                   uint8_t* epi, uint32_t& es, const Pre&)
-//        warp-uniform control flow around tcgen05.ld is required; epi = this warp's
-//        kEpiBytes / 4 of staging, es = a per-warp counter the epilogue may use for
+//                                   uint8_t* epi, uint32_t& es, const Pre&, int half)
+//        warp-uniform control flow around tcgen05.ld is required; half = which half
+//        of the columns this warp takes (always 0 with four epilogue warps); epi =
+//        this warp's kEpiBytes / kEpiWarps of staging, es = a per-warp counter the epilogue may use for
 //        its buffers; TMA stores it issues (lane 0, bulk groups) complete before
 //        the CTA exits
 #pragma once
@@ -53,7 +56,13 @@ __host__ __device__ constexpr size_t tc_mc_smem_bytes() {
 }
 
 template <class Op>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_constant__ typename Op::Params p) {
+__host__ __device__ constexpr int tc_mc_threads() {
+  return 64 + 32 * Op::kEpiWarps;
+}
+
+template <class Op>
+__global__ void __launch_bounds__(tc_mc_threads<Op>(), 1) tc_mc_kernel(const __grid_constant__ typename Op::Params p) {
+  static_assert(Op::kEpiWarps == 4 || Op::kEpiWarps == 8, "four or eight epilogue warps");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + (size_t)Op::kStages * Op::kStageBytes;  // epilogue staging (kEpiBytes)
@@ -87,7 +96,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&accf[s], 1);
-      ptx::mbar_init(&acce[s], 4);  // one arrival per epilogue warp
+      ptx::mbar_init(&acce[s], Op::kEpiWarps);  // one arrival per epilogue warp
     }
     ptx::mbar_init(drainb, 1);
     *abort_flag = 0;
@@ -158,8 +167,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
     }
   } else {
     const int g = warp & 3;
+    const int half = (warp - 2) >> 2;
     uint32_t et = 0, es = 0;
-    uint8_t* epi_w = epi + (size_t)g * (Op::kEpiBytes / 4);
+    uint8_t* epi_w = epi + (size_t)(warp - 2) * (Op::kEpiBytes / Op::kEpiWarps);
     for (int w = cluster; w < n_work; w += n_clusters) {
       if (*abort_flag) break;
       typename Op::Tile t;
@@ -172,7 +182,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_mc_kernel(const __grid_const
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane, epi_w, es, pre);
+      Op::epilogue(p, t, tmem + acc * Op::kAccCols + ((uint32_t)(32 * g) << 16), 32 * g + lane, epi_w, es, pre,
+                   half);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acce[acc]);

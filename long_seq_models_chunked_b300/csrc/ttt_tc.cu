@@ -58,26 +58,35 @@ bool g_grad_pairs = true;               // test hook: the chunk gradient on CTA 
 // the issuing thread between k-blocks.
 // TMEM of one 256-column accumulator: query [A|B] in columns 0-255; key and
 // key-hidden [A|B] in 0-127, Dm (hi part, lo part) in 128-191 and 192-255.
-struct FwdMcOp {
-  struct Params {
-    CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
-    CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
-    CUtensorMap sHq;         // stores: H_q {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
-    CUtensorMap sE, sEl;     //         E (hi, lo) {dh, Cp, 3BH}, box {32, 32, 1}
-    const float* lr;
-    bf16* Hq;                // [BH][Cp][dh]
-    bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
-    bf16* El;                // low halves of E (split precision)
-    int d, dh, T, Cp, chunk_start, valid;
-    int n_tok, groups, n_jq, BH, cs;  // n_jq: 128-wide hidden slices
-    int q, k, h;             // which kinds of tiles this launch computes (query, key, key-hidden)
-    int w_split, e_split;
-    int lr_stride;           // 1: one rate per token; 3: one per token and matrix (W1, W2, W3)
-    int mse;                 // key tiles: Dm = Y W2 with Y (hi, lo) from mY / mYl (MSE loss)
-    CUtensorMap mY, mYl;     // Y (hi, lo) {d, Cp, BH}, box {64, 128, 1}: tokens relative to the chunk
-    CUtensorMap sHk, sHkl;   // stores: H_k (hi, lo) {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
-    TcCommon cm;
-  };
+struct FwdMcParams {
+  CUtensorMap mQ, mK, mV;  // 3D {d, T, BH}, box {64, 128, 1}
+  CUtensorMap mW, mWl;     // bf16 shadows (hi, lo) [3BH][d][dh] as 3D {dh, d, 3BH}, box {64, 64, 1}
+  CUtensorMap sHq;         // stores: H_q {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
+  CUtensorMap sE, sEl;     //         E (hi, lo) {dh, Cp, 3BH}, box {32, 32, 1}
+  const float* lr;
+  bf16* Hq;                // [BH][Cp][dh]
+  bf16* E;                 // [BH][3][Cp][dh]: DA, He, DB
+  bf16* El;                // low halves of E (split precision)
+  int d, dh, T, Cp, chunk_start, valid;
+  int n_tok, groups, n_jq, BH, cs;  // n_jq: 128-wide hidden slices
+  int q, k, h;             // which kinds of tiles this launch computes (query, key, key-hidden)
+  int w_split, e_split;
+  int lr_stride;           // 1: one rate per token; 3: one per token and matrix (W1, W2, W3)
+  int mse;                 // key tiles: Dm = Y W2 with Y (hi, lo) from mY / mYl (MSE loss)
+  CUtensorMap mY, mYl;     // Y (hi, lo) {d, Cp, BH}, box {64, 128, 1}: tokens relative to the chunk
+  CUtensorMap sHk, sHkl;   // stores: H_k (hi, lo) {dh, Cp, BH}, box {32, 32, 1}, 64-byte swizzle
+  TcCommon cm;
+};
+
+// EW: epilogue warps (4, or 8 = two per TMEM lane quarter, each taking half of
+// a tile's hidden columns). Eight pay where the epilogue bounds the tile (a
+// short K = d loop: d < 512; imageset_1m's forward 5.71 -> 4.47 ms); where d
+// is larger the tile is bound by its operand ingest and the four extra warps
+// only compete with the one thread that issues the MMAs (lm_chunk2k 128 -> 134 us).
+template <int EW>
+struct FwdMcOpT {
+  using Params = FwdMcParams;
+
   struct Tile {
     int bh, hid0, tok, kind;  // kind: 0 query (128 hidden), 1 key, 2 key-hidden (64 hidden)
     bool is_k, real;
@@ -85,7 +94,8 @@ struct FwdMcOp {
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = kABytes + 4 * kBox;
   static constexpr int kAccCols = 256;
-  static constexpr uint32_t kEpiBytes = 4 * 2 * 4096;  // two 4 KB staging buffers per epilogue warp
+  static constexpr int kEpiWarps = EW;
+  static constexpr uint32_t kEpiBytes = 8 * 4096;  // 4 x 8 KB or 8 x 4 KB of staging (two or one 4 KB buffers per warp)
 
   // items per (b, h, 128-wide hidden slice, token group): one query tile, two
   // key-hidden tiles, two key tiles (those the launch computes)
@@ -189,8 +199,9 @@ struct FwdMcOp {
       }
     }
   }
-  // The SwiGLU (backward) epilogue through shared memory: each warp stages its
-  // 32 x 32 blocks (64-byte swizzle) in one of its two buffers and writes them
+  // The SwiGLU (backward) epilogue through shared memory: eight warps, two per
+  // TMEM lane quarter, each taking half of the tile's hidden columns; each
+  // stages its 32 x 32 blocks (64-byte swizzle) in its buffer and writes them
   // with TMA stores, hi and lo halves alike. Rows past the chunk's tokens get
   // lr 0 (zero E rows) and zero H_q rows.
   // the key rows' rates (W1, W2, W3), loaded before the accumulator wait;
@@ -210,7 +221,7 @@ struct FwdMcOp {
     return x;
   }
   static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t* epi,
-                                  uint32_t& es, const Pre& pr) {
+                                  uint32_t& es, const Pre& pr, int half) {
     if (!t.real) return;  // a CTA past the chunk's last token tile stores nothing
     const int lane = r & 31;
     const int tl = t.tok * BM + r;        // token index inside the chunk
@@ -219,8 +230,13 @@ struct FwdMcOp {
     const int j0 = t.hid0;
     // stage one 32 x 32 block and store it at (column x, this warp's rows, plane z)
     auto put = [&](const float* v, bool lo, const CUtensorMap* mh, const CUtensorMap* ml, int x, int z) {
-      uint8_t* buf = epi + (es & 1u) * 4096u;
-      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that used this buffer has read it
+      uint8_t* buf = epi + (EW == 4 ? (es & 1u) * 4096u : 0u);
+      if (lane == 0) {  // the store that used this buffer has read it
+        if (EW == 4)
+          ptx::bulk_wait_read<1>();
+        else
+          ptx::bulk_wait_read<0>();
+      }
       __syncwarp();
       if (lo)
         stage_bf16x32<true>(buf, lane, v);
@@ -239,7 +255,8 @@ struct FwdMcOp {
     if (!t.is_k) {
       const bool hk = t.kind == 2;  // key hiddens: split operands of the MSE's Y = H_k W2^T - V
       const int wa = hk ? 64 : 128;  // hidden columns of the tile: A in [0, wa), B in [wa, 2 wa)
-      for (int c = 0; c < wa; c += 32) {
+      const int cw = EW == 8 ? wa / 2 : wa;  // this warp's columns
+      for (int c = half * cw; c < (half + 1) * cw; c += 32) {
         ptx::tmem_ld32(tm + c, va);
         ptx::tmem_ld32(tm + wa + c, vb);
 #pragma unroll
@@ -254,7 +271,7 @@ struct FwdMcOp {
       const float e1 = pr.e1, e2 = pr.e2, e3 = pr.e3;
       const bool lo = p.e_split != 0;
       float vd[32];
-      for (int c = 0; c < 64; c += 32) {
+      for (int c = 32 * half; c < 64; c += (EW == 8 ? 64 : 32)) {
         ptx::tmem_ld32(tm + c, va);
         ptx::tmem_ld32(tm + 64 + c, vb);
         ptx::tmem_ld32(tm + 128 + c, vd);
@@ -462,6 +479,7 @@ struct GradMcOp {
   static constexpr int kStages = MSE ? 4 : 5;
   static constexpr int kStageBytes = kAB + 2 * kEB + (MSE ? kAB : 0);
   static constexpr int kAccCols = BN;
+  static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kEpiBytes = 0;
 
   static __device__ int num_work(const Params& p) { return p.Z * p.nt * p.mg * p.splits; }
@@ -527,7 +545,7 @@ struct GradMcOp {
   struct Pre {};
   static __device__ Pre pre(const Params&, const Tile&, int) { return {}; }
   static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&,
-                                  const Pre&) {
+                                  const Pre&, int) {
     const int m = t.m0 + r;
     float v[32];
     if (p.Xh && p.splits == 1) {
@@ -627,7 +645,7 @@ struct GradPairOp {
   static __device__ Pre pre(const Params& p, const Tile& t, int r) { return Base::pre(p, t, r); }
   static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t* epi, uint32_t& es,
                                   const Pre& pr) {
-    Base::epilogue(p, t, tm, r, epi, es, pr);
+    Base::epilogue(p, t, tm, r, epi, es, pr, 0);
   }
 };
 #endif  // TTT_HAS_MULTICAST
@@ -912,7 +930,7 @@ int mc_max_clusters(int cs) {
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(cs);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(tc_mc_threads<Op>());
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -944,7 +962,7 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(n_cl * cs);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(tc_mc_threads<Op>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -1311,7 +1329,7 @@ class TcLayer {
   }
 
   int fwd_launch(int s, int valid, bool q, bool k, bool h) {
-    FwdMcOp::Params p{};
+    FwdMcParams p{};
     p.mQ = mQ; p.mK = mK; p.mV = mV; p.mW = mW[0]; p.mWl = mW[1];
     p.sHq = sHq; p.sE = sE[0]; p.sEl = sE[1];
     p.lr = lr_; p.Hq = Hq; p.E = E; p.El = El;
@@ -1337,7 +1355,8 @@ class TcLayer {
     p.cm = cm;
     p.cm.stall = g_stall_next_fwd.exchange(0);
     const int n_work = P.BH * p.n_jq * p.groups * (p.q + 2 * p.h + 2 * p.k);
-    return launch_mc<FwdMcOp>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
+    if (g_.d < 512) return launch_mc<FwdMcOpT<8>>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
+    return launch_mc<FwdMcOpT<4>>(TTT_KERNEL_FWD, p, p.cs, n_work, st_);
   }
 
   // O[s, s + valid) = H_q W2^T on stream `os`.
