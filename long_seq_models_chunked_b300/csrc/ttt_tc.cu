@@ -39,6 +39,7 @@ using namespace tcu;
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
 std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch withholds its loads
 bool g_grad_pairs = true;               // test hook: the chunk gradient on CTA pairs (single-GPU build)
+bool g_apply_pairs = true;              // test hook: the apply on CTA pairs (single-GPU build)
 
 
 // ============================================================ forward, multicast
@@ -648,6 +649,62 @@ struct GradPairOp {
     Base::epilogue(p, t, tm, r, epi, es, pr, 0);
   }
 };
+
+// ============================================================ apply-2 on CTA pairs
+// O = H_q W2^T on CTA pairs: a pair computes 256 token rows (each CTA its 128)
+// by a 256-wide column tile of O, each CTA holding its 128 rows of H_q and 128
+// of the tile's W2 rows: 32 KB per CTA per 64 of K for 256 x 256 x 16 MMAs,
+// where a one-CTA 128 x 256 tile takes 48 KB.
+struct OPairOp {
+  struct Params {
+    CUtensorMap mH;   // Hq 3D {dh, Cp, BH}, box {64, 128, 1}
+    CUtensorMap mW2;  // shadows 3D {dh, d, 3BH}, box {64, 128, 1}
+    bf16* O;
+    int d, dh, T, chunk_start, valid, m_pairs, n_tiles, BH;
+    TcCommon cm;
+  };
+  struct Tile {
+    int bh, row0, n0;
+  };
+  struct Pre {};
+  static constexpr int kStages = 6;
+  static constexpr int kStageBytes = 2 * kABytes;  // 128 rows of H_q + 128 rows of W2, 64 of K each
+  static constexpr int kAccCols = 256;
+  static constexpr uint32_t kEpiBytes = 0;
+
+  static __device__ int num_work(const Params& p) { return p.BH * p.m_pairs * p.n_tiles; }
+  static __device__ void tile_of(const Params& p, int w, int prank, Tile& t) {
+    const int nt = w % p.n_tiles;
+    w /= p.n_tiles;
+    const int mp = w % p.m_pairs;
+    t.bh = w / p.m_pairs;
+    t.n0 = nt * 256;
+    t.row0 = (2 * mp + prank) * BM;
+  }
+  static __device__ int num_kblocks(const Params& p, const Tile&) { return p.dh / BK; }
+  static __device__ uint32_t stage_tx(const Params&, const Tile&, int) { return 2 * kABytes; }
+  static __device__ void produce(const Params& p, const Tile& t, int kb, uint8_t* st, uint32_t fb, int prank) {
+    ptx::tma_load_3d_pair(st, &p.mH, fb, kb * BK, t.row0, t.bh);
+    ptx::tma_load_3d_pair(st + kABytes, &p.mW2, fb, kb * BK, t.n0 + 128 * prank, t.bh * 3 + 1);
+  }
+  static __device__ void consume(const Params&, const Tile&, int kb, uint32_t st, uint32_t tmem) {
+    constexpr uint32_t id = ptx::idesc_bf16(256, 256, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) ptx::mma2_bf16(tmem, kdesc(st, kk), kdesc(st + kABytes, kk), id, (kb | kk) != 0);
+  }
+  static __device__ Pre pre(const Params&, const Tile&, int) { return {}; }
+  static __device__ void epilogue(const Params& p, const Tile& t, uint32_t tm, int r, uint8_t*, uint32_t&,
+                                  const Pre&) {
+    const int tl = t.row0 + r;
+    const bool valid = tl < p.valid;
+    bf16* dst = p.O + ((size_t)t.bh * p.T + p.chunk_start + tl) * p.d + t.n0;
+    float v[32];
+    for (int c = 0; c < 256; c += 32) {
+      ptx::tmem_ld32(tm + c, v);
+      if (valid && t.n0 + c < p.d) st_bf16x32(dst + c, v);
+    }
+  }
+};
 #endif  // TTT_HAS_MULTICAST
 
 // ============================================================ plain GEMM (test hook)
@@ -1195,6 +1252,7 @@ class TcLayer {
     ok &= map3(&mW[1], split_fwd ? Msl : Ms, dh, d, Z, 64, 64);
     ok &= map3(&mHq, Hq, dh, P.Cp, BH, 64, 128);
     ok &= map3(&mW2o, Ms, dh, d, Z, 64, P.bn_o);
+    ok &= map3(&mW2p, Ms, dh, d, Z, 64, 128);
     ok &= map3(&mE[0], E, dh, P.Cp, Z, 64, 32);
     ok &= map3(&mE[1], split_grad ? El : E, dh, P.Cp, Z, 64, 32);
     ok &= map3(&sHq, Hq, dh, P.Cp, BH, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1368,6 +1426,16 @@ class TcLayer {
       p.d = d; p.dh = g_.dh; p.T = T_; p.chunk_start = s; p.valid = valid; p.m_tiles = mt; p.n_tiles = nt;
       p.cm = cm;
     };
+#if TTT_HAS_MULTICAST
+    if (g_apply_pairs && mt >= 2) {
+      OPairOp::Params p{};
+      p.mH = mHq; p.mW2 = mW2p; p.O = static_cast<bf16*>(O_);
+      p.d = d; p.dh = g_.dh; p.T = T_; p.chunk_start = s; p.valid = valid;
+      p.m_pairs = (mt + 1) / 2; p.n_tiles = (d + 255) / 256; p.BH = P.BH;
+      p.cm = cm;
+      return launch_pair<OPairOp>(TTT_KERNEL_APPLY, p, P.BH * p.m_pairs * p.n_tiles, os);
+    }
+#endif
     const dim3 grid(mt * nt, P.BH);
     if (P.bn_o == 256) { typename OOp<256>::Params p{}; fill(p); return launch_op<OOp<256>>(TTT_KERNEL_APPLY, p, grid, os); }
     if (P.bn_o == 192) { typename OOp<192>::Params p{}; fill(p); return launch_op<OOp<192>>(TTT_KERNEL_APPLY, p, grid, os); }
@@ -1505,7 +1573,7 @@ class TcLayer {
   bf16 *Ms, *Msl, *Hq, *E, *El;
   TcCommon cm;
   NsFusedArgs nsa;
-  CUtensorMap mW[2], mHq, mW2o, mE[2], sHq, sE[2];
+  CUtensorMap mW[2], mHq, mW2o, mW2p, mE[2], sHq, sE[2];
   CUtensorMap mQ, mK, mV, mK3, mV3, mK4, mV4;
   const float* lr_ = nullptr;
   void* O_ = nullptr;
