@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/ttt_debug.h"
 #include "tc_kernel.cuh"
@@ -977,6 +978,8 @@ template <class Op>
 int mc_max_clusters(int cs) {
   static int cached[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
   static int cached_dev[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  static std::mutex mu;  // host threads may launch at once
+  std::lock_guard<std::mutex> lk(mu);
   if (cs < 1 || cs > 8) return -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -1039,6 +1042,8 @@ int launch_mc(int kind, const typename Op::Params& p, int cs, int n_work, cudaSt
 template <class Op>
 int pair_max(int* out) {
   static int cached = 0, cached_dev = -1;
+  static std::mutex mu;  // host threads may launch at once
+  std::lock_guard<std::mutex> lk(mu);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TTT_ERR_CUDA;
   if (cached_dev != dev) {

@@ -130,3 +130,10 @@ def test_backward_covers_the_linear_net_with_plain_steps():
         with pytest.raises(abi.TTTError) as err:
             abi.ttt_bwd_workspace_bytes(c)
         assert err.value.code == abi.TTT_ERR_UNSUPPORTED
+
+def test_test_hooks_reject_bad_arguments():
+    assert abi.lib().ttt_dbg_grad_pairs(2) == abi.TTT_ERR_ARG
+    assert abi.lib().ttt_dbg_grad_pairs(-1) == abi.TTT_ERR_ARG
+    assert abi.lib().ttt_dbg_grad_pairs(1) == abi.TTT_OK
+    assert abi.lib().ttt_dbg_ns_tiles(64, 0) == abi.TTT_ERR_ARG
+    assert abi.lib().ttt_dbg_ns_tiles(0, 0) == abi.TTT_OK
