@@ -271,6 +271,17 @@ TTT_API int ttt_select_impl(const ttt_cfg* cfg);
 /* Static description of a status code. */
 TTT_API const char* ttt_strerror(int status);
 
+/* Host-thread resources. In shifted mode the tensor-core path runs each
+ * chunk's apply on a side stream beside that chunk's gradient (ordered by two
+ * events after the forward and before the next weight update); the library
+ * creates that stream and its events once per host thread and device, on the
+ * thread's first such call, and keeps them for its later calls.
+ * ttt_thread_release() waits for and destroys the calling thread's (every
+ * device it used). Call it before a host thread that used the library exits
+ * when the process outlives the thread; later calls create them again.
+ * Returns TTT_OK (also when there is nothing to release) or TTT_ERR_CUDA. */
+TTT_API int ttt_thread_release(void);
+
 /* Build features, as bit flags.
  * TTT_FEATURE_CLUSTER_MULTICAST: the tensor-core kernels share operand tiles
  * across the CTAs of a thread-block cluster with TMA multicast loads (and

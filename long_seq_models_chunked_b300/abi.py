@@ -45,7 +45,7 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_dbg_ns_trace_read", "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns", "ttt_build_features",
             "ttt_dbg_ns_symmetric", "ttt_cp_workspace_bytes", "ttt_cp_begin", "ttt_cp_grad", "ttt_cp_update",
             "ttt_cp_apply", "ttt_cp_end", "ttt_dbg_ns_tiles", "ttt_bwd_workspace_bytes", "ttt_bwd",
-            "ttt_dbg_grad_pairs")
+            "ttt_dbg_grad_pairs", "ttt_thread_release")
 TTT_FEATURE_CLUSTER_MULTICAST = 1
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
@@ -121,6 +121,8 @@ def _load():
     lib.ttt_dbg_ns_tiles.restype = c_int
     lib.ttt_dbg_ns_symmetric.argtypes = [c_int]
     lib.ttt_dbg_ns_symmetric.restype = c_int
+    lib.ttt_thread_release.argtypes = []
+    lib.ttt_thread_release.restype = c_int
     lib.ttt_dbg_grad_pairs.argtypes = [c_int]
     lib.ttt_dbg_grad_pairs.restype = c_int
     lib.ttt_dbg_ns_trace.argtypes = [c_int]
@@ -331,6 +333,13 @@ def ttt_dbg_ns_symmetric(on: int) -> int:
     """Test hook: symmetric (upper-triangle) tiles in the fused Muon kernel:
     1 always, 0 never, -1 chosen by the shape (the default)."""
     return _lib.ttt_dbg_ns_symmetric(int(on))
+
+
+def ttt_thread_release() -> int:
+    """Waits for and destroys the calling thread's side streams and events
+    (created by the tensor-core path's shifted-mode calls); later calls create
+    them again. Returns the status."""
+    return _lib.ttt_thread_release()
 
 
 def ttt_dbg_grad_pairs(on: bool) -> None:

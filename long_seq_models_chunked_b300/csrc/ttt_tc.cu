@@ -1110,23 +1110,49 @@ struct SideStream {
   cudaEvent_t fwd_done, apply_done;
 };
 
+constexpr int kMaxSideDev = 64;
+struct SideStreams {
+  SideStream slot[kMaxSideDev];
+  bool made[kMaxSideDev];
+};
+thread_local SideStreams t_side = {};
+
 SideStream* side_stream() {
-  constexpr int kMaxDev = 64;
-  thread_local SideStream slots[kMaxDev];
-  thread_local bool made[kMaxDev] = {};
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  if (!made[dev]) {
-    SideStream& x = slots[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDev) return nullptr;
+  if (!t_side.made[dev]) {
+    SideStream& x = t_side.slot[dev];
     if (cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&x.fwd_done, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&x.apply_done, cudaEventDisableTiming) != cudaSuccess) {
+    if (cudaEventCreateWithFlags(&x.fwd_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaStreamDestroy(x.stream);
       cudaGetLastError();
       return nullptr;
     }
-    made[dev] = true;
+    if (cudaEventCreateWithFlags(&x.apply_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(x.fwd_done);
+      cudaStreamDestroy(x.stream);
+      cudaGetLastError();
+      return nullptr;
+    }
+    t_side.made[dev] = true;
   }
-  return &slots[dev];
+  return &t_side.slot[dev];
+}
+
+// Destroys the calling thread's side streams and events (every device).
+int side_streams_release() {
+  int rc = TTT_OK;
+  for (int dev = 0; dev < kMaxSideDev; ++dev) {
+    if (!t_side.made[dev]) continue;
+    SideStream& x = t_side.slot[dev];
+    if (cudaStreamSynchronize(x.stream) != cudaSuccess) rc = TTT_ERR_CUDA;
+    if (cudaEventDestroy(x.fwd_done) != cudaSuccess || cudaEventDestroy(x.apply_done) != cudaSuccess ||
+        cudaStreamDestroy(x.stream) != cudaSuccess)
+      rc = TTT_ERR_CUDA;
+    t_side.made[dev] = false;
+  }
+  if (rc != TTT_OK) cudaGetLastError();
+  return rc;
 }
 
 struct Plan {
@@ -1794,6 +1820,8 @@ extern "C" int ttt_dbg_gemm_bf16(const void* A, int a_mn_major, const void* B, i
 extern "C" int ttt_build_features(void) { return TTT_HAS_MULTICAST ? TTT_FEATURE_CLUSTER_MULTICAST : 0; }
 
 extern "C" void ttt_dbg_stall_next_fwd(void) { ttt::g_stall_next_fwd.store(1); }
+
+extern "C" int ttt_thread_release(void) { return ttt::side_streams_release(); }
 
 extern "C" int ttt_dbg_grad_pairs(int on) {
   if (on != 0 && on != 1) return TTT_ERR_ARG;

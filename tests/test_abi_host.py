@@ -137,3 +137,7 @@ def test_test_hooks_reject_bad_arguments():
     assert abi.lib().ttt_dbg_grad_pairs(1) == abi.TTT_OK
     assert abi.lib().ttt_dbg_ns_tiles(64, 0) == abi.TTT_ERR_ARG
     assert abi.lib().ttt_dbg_ns_tiles(0, 0) == abi.TTT_OK
+
+
+def test_thread_release_with_nothing_to_release():
+    assert abi.ttt_thread_release() == abi.TTT_OK

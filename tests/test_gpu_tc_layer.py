@@ -155,6 +155,17 @@ def test_gradient_pairs_equal_one_cta_tiles(name):
     assert np.array_equal(got[0], ref[0]) and all(np.array_equal(p, q) for p, q in zip(got[1], ref[1])), name
 
 
+def test_thread_release_between_calls():
+    """ttt_thread_release destroys the side stream the shifted-mode apply runs
+    on; the next call creates it again and gives the same bits."""
+    spec, x = _inputs("small_odd_ragged")
+    a = run_gpu(spec, x, impl=TC)
+    assert abi.ttt_thread_release() == abi.TTT_OK
+    assert abi.ttt_thread_release() == abi.TTT_OK  # nothing left to release
+    b = run_gpu(spec, x, impl=TC)
+    assert np.array_equal(a[0], b[0]) and all(np.array_equal(p, q) for p, q in zip(a[1], b[1]))
+
+
 @pytest.mark.parametrize("ctas", [5, 37])
 def test_muon_on_a_small_grid_matches_oracle(ctas):
     """The fused Muon kernel's item list on a grid far smaller than its items
