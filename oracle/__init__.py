@@ -30,7 +30,11 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
   linear_head_backward        - pinned (central finite differences of the forward
                                 oracle, every input, inner product and MSE, masks and
                                 ragged chunks)
+  swiglu_head_backward        - pinned (central finite differences of the forward
+                                oracle ttt_head, every input, inner product and MSE,
+                                masks and ragged chunks)
 """
 from .ttt_oracle import (OracleCfg, apply_inclusive, chunk_grad, linear_apply,  # noqa: F401
                          linear_grad, linear_head_backward, newton_schulz, row_norms, sigmoid,
-                         swiglu_apply, swiglu_grad, ttt_head, ttt_layer, update, weight_norm)
+                         swiglu_apply, swiglu_grad, swiglu_head_backward, ttt_head, ttt_layer,
+                         update, weight_norm)

@@ -379,3 +379,68 @@ def linear_head_backward(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.nda
                 Lc += E.T @ K[s:e]
         Lnext = Lc
     return dQ, dK, dV, dlr, Lnext
+
+
+def swiglu_head_backward(cfg: OracleCfg, Q: np.ndarray, K: np.ndarray, V: np.ndarray, lr: np.ndarray,
+                         W0: Weights, dO: np.ndarray, dWf: Weights):
+    """Gradients of a scalar loss L through the layer on one head for the
+    SwiGLU net with plain gradient steps in shifted mode, given dL/dO (dO) and
+    dL/dW_final (dWf, one per matrix): returns (dQ, dK, dV, dlr, dW0) with dW0 a
+    tuple (dW1, dW2, dW3).
+
+    The outer loop of the TTT-E2E news page (§2.2: the model's loss is
+    differentiated through the inner updates). The forward is the same as
+    ttt_head's for this configuration, written with fp64 torch operations so that
+    reverse-mode automatic differentiation (a library routine) gives every
+    gradient: per chunk c, O_t = f(q_t; W_c) for the chunk's queries, then
+    W_{c+1} = W_c - step * sum_t lr_t grad_W l_t(W_c) with swiglu_grad's
+    hand-derived gradient (which the automatic differentiation goes through, so
+    the second-order terms of the update come out of it), and
+    L = sum dO * O + sum_j <dWf_j, W_final_j>.
+    """
+    import torch  # fp64 CPU tensors only
+
+    if cfg.fast_net != "swiglu" or cfg.muon or cfg.wnorm or cfg.momentum != 0.0 or cfg.mode != "shifted":
+        raise ValueError("the SwiGLU backward covers plain steps in shifted mode")
+    f64 = torch.float64
+    tq, tk, tv = (torch.tensor(np.asarray(x, dtype=np.float64), dtype=f64, requires_grad=True) for x in (Q, K, V))
+    tl = torch.tensor(np.asarray(lr, dtype=np.float64), dtype=f64, requires_grad=True)
+    tw = [torch.tensor(np.asarray(w, dtype=np.float64), dtype=f64, requires_grad=True) for w in W0]
+
+    def apply(W, X):
+        A = X @ W[0].T
+        return (A * torch.sigmoid(A) * (X @ W[2].T)) @ W[1].T
+
+    def grad(W, Kc, Vc, eta):
+        A = Kc @ W[0].T
+        Bm = Kc @ W[2].T
+        sg = torch.sigmoid(A)
+        S = A * sg
+        H = S * Bm
+        Y = -Vc if cfg.loss == "ip" else H @ W[1].T - Vc
+        Yh = eta[:, None] * Y
+        DH = Yh @ W[1]
+        DA = DH * Bm * sg * (1.0 + A * (1.0 - sg))
+        DB = DH * S
+        return DA.T @ Kc, Yh.T @ H, DB.T @ Kc
+
+    T = Q.shape[0]
+    C = cfg.chunk
+    n = (T + C - 1) // C
+    mask = cfg.mask if cfg.mask is not None else [1] * n
+    W = list(tw)
+    outs = []
+    for ci in range(n):
+        s, e = ci * C, min(T, (ci + 1) * C)
+        outs.append(apply(W, tq[s:e]))
+        if mask[ci]:
+            G = grad(W, tk[s:e], tv[s:e], tl[s:e])
+            W = [w - cfg.step * g for w, g in zip(W, G)]
+    O = torch.cat(outs, dim=0)
+    L = (O * torch.tensor(np.asarray(dO, dtype=np.float64), dtype=f64)).sum()
+    for w, dw in zip(W, dWf):
+        L = L + (w * torch.tensor(np.asarray(dw, dtype=np.float64), dtype=f64)).sum()
+    gq, gk, gv, gl, g1, g2, g3 = torch.autograd.grad(L, [tq, tk, tv, tl] + tw, allow_unused=True)
+    z = lambda g, like: (np.zeros_like(like) if g is None else g.detach().numpy())
+    return (z(gq, Q), z(gk, K), z(gv, V), z(gl, np.asarray(lr, dtype=np.float64)),
+            (z(g1, W0[0]), z(g2, W0[1]), z(g3, W0[2])))

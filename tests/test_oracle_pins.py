@@ -631,3 +631,38 @@ def test_linear_backward_matches_central_differences(loss, C, mask):
             dn[i][idx] -= h
             num[idx] = (L(*up) - L(*dn)) / (2 * h)
         assert np.abs(g - num).max() <= 1e-6 * max(1.0, np.abs(num).max()), (i, np.abs(g - num).max())
+
+
+@pytest.mark.parametrize("loss", ["ip", "mse"])
+@pytest.mark.parametrize("C,mask", [(3, None), (5, [1, 0, 1])])
+def test_swiglu_backward_matches_central_differences(loss, C, mask):
+    """The SwiGLU backward (automatic differentiation of an fp64 torch forward)
+    against central finite differences of the NumPy forward oracle ttt_head:
+    every input, a ragged last chunk, an update mask."""
+    rng = np.random.default_rng(43)
+    d, dh, T = 3, 4, 13
+    step = 0.7 if loss == "ip" else 0.3  # MSE's inner loop diverges at larger steps
+    W0 = _rand_weights("swiglu", d, dh, rng)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    lr = rng.uniform(0.05, 0.3, T)
+    dO = rng.standard_normal((T, d))
+    dWf = tuple(rng.standard_normal(w.shape) for w in W0)
+    cfg = orc.OracleCfg(chunk=C, fast_net="swiglu", loss=loss, muon=False, wnorm=False, step=step, mask=mask)
+
+    def L(Q_, K_, V_, lr_, W1_, W2_, W3_):
+        O, Wf = orc.ttt_head(cfg, Q_, K_, V_, lr_, (W1_, W2_, W3_))
+        return float((dO * O).sum() + sum((a * b).sum() for a, b in zip(dWf, Wf)))
+
+    dQ, dK, dV, dlr, dW0 = orc.swiglu_head_backward(cfg, Q, K, V, lr, W0, dO, dWf)
+    got = [dQ, dK, dV, dlr, *dW0]
+    args = [Q, K, V, lr, *W0]
+    h = 1e-6
+    for i, g in enumerate(got):
+        num = np.zeros_like(g)
+        for idx in np.ndindex(*g.shape):
+            up = [a.copy() for a in args]
+            dn = [a.copy() for a in args]
+            up[i][idx] += h
+            dn[i][idx] -= h
+            num[idx] = (L(*up) - L(*dn)) / (2 * h)
+        assert np.abs(g - num).max() <= 1e-6 * max(1.0, np.abs(num).max()), (i, np.abs(g - num).max())
