@@ -223,6 +223,21 @@ TTT_API int ttt_bwd(const ttt_cfg* cfg, const void* Q, const void* K, const void
                     const float* W0, const void* dO, const float* dWf, void* dQ, void* dK, void* dV,
                     float* dlr, float* dW0, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same for the SwiGLU fast net with plain gradient steps (muon = wnorm = 0,
+ * momentum = 0, one rate per token: lr_per_matrix = 0) in shifted mode with
+ * the inner-product loss: W0_j, dWf_j and dW0_j as the three matrices of
+ * ttt_fwd (W1 [dh, d], W2 [d, dh], W3 [dh, d] per head; W0 and dW0 shared over
+ * the batch unless w0_per_batch, dWf per (batch, head)). The second-order terms
+ * of the inner updates (the derivative of each token's gradient along the
+ * adjoint of the weights it updates) come out exactly. Other configurations
+ * return TTT_ERR_UNSUPPORTED. Checks and errors as for ttt_bwd. */
+TTT_API int ttt_bwd_swiglu_workspace_bytes(const ttt_cfg* cfg, size_t* bytes);
+TTT_API int ttt_bwd_swiglu(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+                           const float* W0_1, const float* W0_2, const float* W0_3, const void* dO,
+                           const float* dWf_1, const float* dWf_2, const float* dWf_3, void* dQ, void* dK,
+                           void* dV, float* dlr, float* dW0_1, float* dW0_2, float* dW0_3, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* ---- context parallelism (LaCT page §2.2.2) -------------------------------
  * The tokens of one chunk are split into shards held by different GPUs (or
  * handled by different calls). Every shard computes its partial gradient with

@@ -45,7 +45,7 @@ EXPORTED = ("ttt_cfg_default", "ttt_workspace_bytes", "ttt_fwd", "ttt_status",
             "ttt_dbg_ns_trace_read", "ttt_dbg_stall_next_fwd", "ttt_dbg_stall_next_ns", "ttt_build_features",
             "ttt_dbg_ns_symmetric", "ttt_cp_workspace_bytes", "ttt_cp_begin", "ttt_cp_grad", "ttt_cp_update",
             "ttt_cp_apply", "ttt_cp_end", "ttt_dbg_ns_tiles", "ttt_bwd_workspace_bytes", "ttt_bwd",
-            "ttt_dbg_grad_pairs", "ttt_thread_release")
+            "ttt_dbg_grad_pairs", "ttt_thread_release", "ttt_bwd_swiglu_workspace_bytes", "ttt_bwd_swiglu")
 TTT_FEATURE_CLUSTER_MULTICAST = 1
 TTT_KERNEL_FWD, TTT_KERNEL_APPLY, TTT_KERNEL_GRAD, TTT_KERNEL_GRAM, TTT_KERNEL_POLY = 0, 1, 2, 3, 4
 TTT_KERNEL_XUPD, TTT_KERNEL_UPDATE, TTT_KERNEL_AUX, TTT_KERNEL_LINEAR, TTT_KERNEL_SIMT = 5, 6, 7, 8, 9
@@ -115,6 +115,10 @@ def _load():
     lib.ttt_bwd_workspace_bytes.restype = c_int
     lib.ttt_bwd.argtypes = [P] + [c_void_p] * 12 + [c_void_p, c_size_t, c_void_p]
     lib.ttt_bwd.restype = c_int
+    lib.ttt_bwd_swiglu_workspace_bytes.argtypes = [P, ctypes.POINTER(c_size_t)]
+    lib.ttt_bwd_swiglu_workspace_bytes.restype = c_int
+    lib.ttt_bwd_swiglu.argtypes = [P] + [c_void_p] * 18 + [c_void_p, c_size_t, c_void_p]
+    lib.ttt_bwd_swiglu.restype = c_int
     lib.ttt_build_features.argtypes = []
     lib.ttt_build_features.restype = c_int
     lib.ttt_dbg_ns_tiles.argtypes = [c_int, c_int]
@@ -273,6 +277,27 @@ def ttt_bwd(cfg: ttt_cfg, Q, K, V, lr, W0, dO, dWf, dQ, dK, dV, dlr, dW0, worksp
                       workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if check and rc != TTT_OK:
         raise TTTError(rc, "ttt_bwd")
+    return rc
+
+
+def ttt_bwd_swiglu_workspace_bytes(cfg: ttt_cfg) -> int:
+    n = c_size_t(0)
+    rc = _lib.ttt_bwd_swiglu_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n))
+    if rc != TTT_OK:
+        raise TTTError(rc, "ttt_bwd_swiglu_workspace_bytes")
+    return n.value
+
+
+def ttt_bwd_swiglu(cfg: ttt_cfg, Q, K, V, lr, W0, dO, dWf, dQ, dK, dV, dlr, dW0, workspace, stream=None,
+                   check: bool = True) -> int:
+    """Enqueue the outer-loop backward of the SwiGLU net (include/ttt.h) on
+    `stream`; W0, dWf and dW0 are sequences of the three matrices."""
+    rc = _lib.ttt_bwd_swiglu(ctypes.byref(cfg), _ptr(Q), _ptr(K), _ptr(V), _ptr(lr), _ptr(W0[0]), _ptr(W0[1]),
+                             _ptr(W0[2]), _ptr(dO), _ptr(dWf[0]), _ptr(dWf[1]), _ptr(dWf[2]), _ptr(dQ), _ptr(dK),
+                             _ptr(dV), _ptr(dlr), _ptr(dW0[0]), _ptr(dW0[1]), _ptr(dW0[2]), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if check and rc != TTT_OK:
+        raise TTTError(rc, "ttt_bwd_swiglu")
     return rc
 
 

@@ -494,6 +494,57 @@ int ttt_bwd(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, con
   return bwd_run(g, Q, K, V, lr, W0, dO, dWf, dQ, dK, dV, dlr, dW0, static_cast<char*>(workspace), st);
 }
 
+int ttt_bwd_swiglu_workspace_bytes(const ttt_cfg* cfg, size_t* bytes) {
+  if (!bytes) return TTT_ERR_ARG;
+  const int v = validate_cfg(cfg);
+  if (v != TTT_OK) return v;
+  if (!bwd_swiglu_supported(*cfg)) return TTT_ERR_UNSUPPORTED;
+  *bytes = bwd_swiglu_workspace_bytes(*cfg);
+  return TTT_OK;
+}
+
+int ttt_bwd_swiglu(const ttt_cfg* cfg, const void* Q, const void* K, const void* V, const float* lr,
+                   const float* W0_1, const float* W0_2, const float* W0_3, const void* dO, const float* dWf_1,
+                   const float* dWf_2, const float* dWf_3, void* dQ, void* dK, void* dV, float* dlr, float* dW0_1,
+                   float* dW0_2, float* dW0_3, void* workspace, size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  int v = ttt_bwd_swiglu_workspace_bytes(cfg, &need);
+  if (v != TTT_OK) return v;
+  const ttt_cfg& g = *cfg;
+  const Sizes s = tensor_sizes(g);
+  const void* in[11] = {Q, K, V, lr, W0_1, W0_2, W0_3, dO, dWf_1, dWf_2, dWf_3};
+  void* out[7] = {dQ, dK, dV, dlr, dW0_1, dW0_2, dW0_3};
+  for (const void* p : in)
+    if (!p || !aligned16(p)) return TTT_ERR_ARG;
+  for (const void* p : out)
+    if (!p || !aligned16(p)) return TTT_ERR_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return TTT_ERR_WORKSPACE;
+  // outputs may not overlap the inputs, the workspace or each other
+  const size_t in_n[11] = {s.tok_bytes,    s.tok_bytes,    s.tok_bytes, s.lr_bytes,     s.w0_bytes[0], s.w0_bytes[1],
+                           s.w0_bytes[2], s.tok_bytes,    s.wf_bytes[0], s.wf_bytes[1], s.wf_bytes[2]};
+  const size_t out_n[7] = {s.tok_bytes, s.tok_bytes, s.tok_bytes, s.lr_bytes, s.w0_bytes[0], s.w0_bytes[1],
+                           s.w0_bytes[2]};
+  for (int i = 0; i < 7; ++i) {
+    const Range o{(const char*)out[i], out_n[i]};
+    for (int k = 0; k < 11; ++k)
+      if (overlap(o, Range{(const char*)in[k], in_n[k]})) return TTT_ERR_ARG;
+    if (overlap(o, Range{(const char*)workspace, need})) return TTT_ERR_ARG;
+    for (int k = i + 1; k < 7; ++k)
+      if (overlap(o, Range{(const char*)out[k], out_n[k]})) return TTT_ERR_ARG;
+  }
+  const void* ptrs[19] = {Q, K, V, lr, W0_1, W0_2, W0_3, dO, dWf_1, dWf_2, dWf_3,
+                          dQ, dK, dV, dlr, dW0_1, dW0_2, dW0_3, workspace};
+  v = check_device_ptrs(ptrs, 19);
+  if (v != TTT_OK) return v;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return TTT_ERR_CUDA;
+  const float* const w0[3] = {W0_1, W0_2, W0_3};
+  const float* const dwf[3] = {dWf_1, dWf_2, dWf_3};
+  float* const dw0[3] = {dW0_1, dW0_2, dW0_3};
+  return bwd_swiglu_run(g, Q, K, V, lr, w0, dO, dwf, dQ, dK, dV, dlr, dw0, static_cast<char*>(workspace), st);
+}
+
 const char* ttt_strerror(int status) {
   switch (status) {
     case TTT_OK: return "ok";

@@ -207,6 +207,308 @@ __global__ void sum_over_batch_kernel(const float* dW, float* dW0, int B, int H,
   }
 }
 
+// ---------------------------------------------------------------- SwiGLU net
+// The SwiGLU net f(x) = W2 (silu(W1 x) * (W3 x)) with plain gradient steps in
+// shifted mode and the inner-product loss l = -<f(k), v>; one rate per token
+// (lr_t) for all three matrices. Per chunk c: o_t = f(q_t; W_c) for its
+// queries and W_{c+1} = W_c - s sum_t lr_t grad_W l_t(W_c). With Lh = dL/dW_{c+1}
+// (the adjoint reaching W_{c+1}) and phi_t = <Lh, grad_W l_t(W_c)>:
+//   dL/dW_c = Lh - s sum_t lr_t grad_W phi_t + sum_t grad_W <dO_t, f(q_t; W_c)>
+//   dlr_t = -s phi_t,  dk_t = -s lr_t grad_k phi_t,  dv_t = -s lr_t grad_v phi_t,
+// phi_t being the derivative of l_t along Lh. With a = W1 k, b = W3 k, s = silu(a),
+// h = s b, u = W2^T v and the tangents along Lh (dots): a' = Lh1 k, b' = Lh3 k,
+// s' = silu'(a) a', h' = s' b + s b', f' = Lh2 h + W2 h', u' = Lh2^T v:
+//   phi = -v . f';  grad_v phi = -f';  grad_W2 phi = -v h'^T;
+//   gs = -u' b - u b',  gb = -u' s - u s',  gs' = -u b,  gb' = -u s,
+//   ga = gs silu'(a) + gs' silu''(a) a',  ga' = gs' silu'(a),
+//   grad_W1 phi = ga k^T,  grad_W3 phi = gb k^T,
+//   grad_k phi = W1^T ga + W3^T gb + Lh1^T ga' + Lh3^T gb',
+// with silu'(a) = sig (1 + a (1 - sig)) and silu''(a) = sig (1 - sig) (2 + a (1 - 2 sig)).
+// fp32 SIMT, one CTA per (batch, head), every sum in a fixed order.
+constexpr int kSwTb = 16;  // tokens per block
+
+struct SwArgs {
+  int B, H, T, d, dh, chunk, dtype, w0_per_batch, has_mask;
+  float step;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const float* lr;
+  const float* W0[3];
+  const void* dO;
+  const float* dWf[3];
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* dlr;
+  float* dW[3];    // per-(b, h) dW0 of each matrix
+  float* scratch;  // per head: W_c of every chunk, two adjoints, the token block's vectors
+  size_t head_floats;
+  MaskBits mask;
+};
+
+struct SwLayout {
+  size_t mat, Wc, L0, L1, vec, fd, phi, total;  // mat: floats of one matrix (padded)
+};
+
+__host__ __device__ inline SwLayout sw_layout(int d, int dh, int n_chunks) {
+  SwLayout L{};
+  L.mat = align_up((size_t)d * dh, 64);
+  L.Wc = 0;
+  L.L0 = (size_t)n_chunks * 3 * L.mat;
+  L.L1 = L.L0 + 3 * L.mat;
+  L.vec = L.L1 + 3 * L.mat;                                    // 12 vectors of [kSwTb][dh]
+  L.fd = L.vec + 12 * align_up((size_t)kSwTb * dh, 64);       // [kSwTb][d]
+  L.phi = L.fd + align_up((size_t)kSwTb * d, 64);              // [kSwTb]
+  L.total = L.phi + 64;
+  return L;
+}
+
+__device__ __forceinline__ float sw_sig(float x) { return 1.f / (1.f + expf(-x)); }
+
+__global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_constant__ SwArgs a) {
+  const size_t head = blockIdx.x;
+  const int h = (int)(head % a.H);
+  const int d = a.d, dh = a.dh;
+  const size_t dd = (size_t)d * dh;
+  const int n_chunks = (a.T + a.chunk - 1) / a.chunk;
+  const SwLayout L = sw_layout(d, dh, n_chunks);
+  float* ws = a.scratch + head * a.head_floats;
+  // matrix j of the weights at the start of chunk c; W1, W3: [dh][d]; W2: [d][dh]
+  auto Wc = [&](int c, int j) { return ws + L.Wc + ((size_t)c * 3 + j) * L.mat; };
+  const size_t vs = align_up((size_t)kSwTb * dh, 64);
+  auto vec = [&](int i) { return ws + L.vec + (size_t)i * vs; };
+  float* FD = ws + L.fd;
+  float* PHI = ws + L.phi;
+  const float st = a.step;
+  auto tok = [&](const void* p, size_t t, int i) { return ld_val(p, (head * a.T + t) * (size_t)d + i, a.dtype); };
+
+  // ---- forward: every chunk's starting weights
+  for (int j = 0; j < 3; ++j) {
+    const float* w0 = a.W0[j] + (a.w0_per_batch ? head : (size_t)h) * dd;
+    for (size_t i = threadIdx.x; i < dd; i += blockDim.x) Wc(0, j)[i] = w0[i];
+  }
+  __syncthreads();
+  for (int c = 0; c + 1 < n_chunks; ++c) {
+    const int s = c * a.chunk, e = min(a.T, s + a.chunk);
+    for (int j = 0; j < 3; ++j)
+      for (size_t i = threadIdx.x; i < dd; i += blockDim.x) Wc(c + 1, j)[i] = Wc(c, j)[i];
+    __syncthreads();
+    if (a.has_mask && !mask_bit(a.mask, c)) continue;
+    const float *W1 = Wc(c, 0), *W2 = Wc(c, 1), *W3 = Wc(c, 2);
+    float *N1 = Wc(c + 1, 0), *N2 = Wc(c + 1, 1), *N3 = Wc(c + 1, 2);
+    float *DA = vec(0), *DB = vec(1), *HH = vec(2);
+    for (int t0 = s; t0 < e; t0 += kSwTb) {
+      const int nt = min(kSwTb, e - t0);
+      // a, b, u = W2^T (lr v): DA = -u b silu'(a) (the rate folded in), DB = -u s, HH = h
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const int t = idx / dh, jj = idx % dh;
+        float av = 0.f, bv = 0.f, u = 0.f;
+        for (int i = 0; i < d; ++i) {
+          const float k = tok(a.K, t0 + t, i);
+          av = fmaf(W1[(size_t)jj * d + i], k, av);
+          bv = fmaf(W3[(size_t)jj * d + i], k, bv);
+        }
+        for (int r = 0; r < d; ++r) u = fmaf(W2[(size_t)r * dh + jj], tok(a.V, t0 + t, r), u);
+        const float lt = a.lr[head * a.T + t0 + t];
+        const float sg = sw_sig(av), sa = av * sg;
+        DA[idx] = -lt * u * bv * sg * (1.f + av * (1.f - sg));
+        DB[idx] = -lt * u * sa;
+        HH[idx] = sa * bv;
+      }
+      __syncthreads();
+      // W1 -= s sum_t DA k^T;  W3 -= s sum_t DB k^T;  W2 -= s sum_t (-lr v) h^T
+      for (size_t idx = threadIdx.x; idx < dd; idx += blockDim.x) {
+        const int jj = (int)(idx / d), i = (int)(idx % d);
+        float g1 = 0.f, g3 = 0.f;
+        for (int t = 0; t < nt; ++t) {
+          const float k = tok(a.K, t0 + t, i);
+          g1 = fmaf(DA[(size_t)t * dh + jj], k, g1);
+          g3 = fmaf(DB[(size_t)t * dh + jj], k, g3);
+        }
+        N1[idx] -= st * g1;
+        N3[idx] -= st * g3;
+        const int r = (int)(idx / dh), jq = (int)(idx % dh);
+        float g2 = 0.f;
+        for (int t = 0; t < nt; ++t)
+          g2 = fmaf(-a.lr[head * a.T + t0 + t] * tok(a.V, t0 + t, r), HH[(size_t)t * dh + jq], g2);
+        N2[idx] -= st * g2;
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- reverse: Ln = dL/dW_{c+1}, Lc accumulates dL/dW_c
+  float* Ln[3] = {ws + L.L0, ws + L.L0 + L.mat, ws + L.L0 + 2 * L.mat};
+  float* Lc[3] = {ws + L.L1, ws + L.L1 + L.mat, ws + L.L1 + 2 * L.mat};
+  for (int j = 0; j < 3; ++j) {
+    const float* dwf = a.dWf[j] + head * dd;
+    for (size_t i = threadIdx.x; i < dd; i += blockDim.x) Ln[j][i] = dwf[i];
+  }
+  __syncthreads();
+  for (int c = n_chunks - 1; c >= 0; --c) {
+    const int s = c * a.chunk, e = min(a.T, s + a.chunk);
+    const float *W1 = Wc(c, 0), *W2 = Wc(c, 1), *W3 = Wc(c, 2);
+    const bool upd = !a.has_mask || mask_bit(a.mask, c);
+    for (int j = 0; j < 3; ++j)
+      for (size_t i = threadIdx.x; i < dd; i += blockDim.x) Lc[j][i] = Ln[j][i];
+    __syncthreads();
+    for (int t0 = s; t0 < e; t0 += kSwTb) {
+      const int nt = min(kSwTb, e - t0);
+      // -- queries: GA = gh b silu'(a), GB = gh s, HQ = h with gh = W2^T dO
+      float *GA = vec(0), *GB = vec(1), *HQ = vec(2);
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const int t = idx / dh, jj = idx % dh;
+        float av = 0.f, bv = 0.f, gh = 0.f;
+        for (int i = 0; i < d; ++i) {
+          const float q = tok(a.Q, t0 + t, i);
+          av = fmaf(W1[(size_t)jj * d + i], q, av);
+          bv = fmaf(W3[(size_t)jj * d + i], q, bv);
+        }
+        for (int r = 0; r < d; ++r) gh = fmaf(W2[(size_t)r * dh + jj], tok(a.dO, t0 + t, r), gh);
+        const float sg = sw_sig(av), sa = av * sg;
+        GA[idx] = gh * bv * sg * (1.f + av * (1.f - sg));
+        GB[idx] = gh * sa;
+        HQ[idx] = sa * bv;
+      }
+      __syncthreads();
+      // dq = W1^T GA + W3^T GB
+      for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+        const int t = idx / d, i = idx % d;
+        float g = 0.f;
+        for (int jj = 0; jj < dh; ++jj) {
+          g = fmaf(W1[(size_t)jj * d + i], GA[(size_t)t * dh + jj], g);
+          g = fmaf(W3[(size_t)jj * d + i], GB[(size_t)t * dh + jj], g);
+        }
+        st_val(a.dQ, (head * a.T + t0 + t) * (size_t)d + i, a.dtype, g);
+      }
+      // Lc1 += GA q^T, Lc3 += GB q^T, Lc2 += dO HQ^T
+      for (size_t idx = threadIdx.x; idx < dd; idx += blockDim.x) {
+        const int jj = (int)(idx / d), i = (int)(idx % d);
+        float g1 = 0.f, g3 = 0.f;
+        for (int t = 0; t < nt; ++t) {
+          const float q = tok(a.Q, t0 + t, i);
+          g1 = fmaf(GA[(size_t)t * dh + jj], q, g1);
+          g3 = fmaf(GB[(size_t)t * dh + jj], q, g3);
+        }
+        Lc[0][idx] += g1;
+        Lc[2][idx] += g3;
+        const int r = (int)(idx / dh), jq = (int)(idx % dh);
+        float g2 = 0.f;
+        for (int t = 0; t < nt; ++t) g2 = fmaf(tok(a.dO, t0 + t, r), HQ[(size_t)t * dh + jq], g2);
+        Lc[1][idx] += g2;
+      }
+      __syncthreads();
+      if (!upd) {
+        for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+          const int t = idx / d;
+          const size_t o = (head * a.T + t0 + t) * (size_t)d + idx % d;
+          st_val(a.dK, o, a.dtype, 0.f);
+          st_val(a.dV, o, a.dtype, 0.f);
+          if (idx % d == 0) a.dlr[head * a.T + t0 + t] = 0.f;
+        }
+        continue;
+      }
+      // -- keys: the vectors of phi_t along Ln
+      float *AV = vec(0), *BV = vec(1), *AD = vec(2), *BD = vec(3), *U = vec(4), *UH = vec(5);
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const int t = idx / dh, jj = idx % dh;
+        float av = 0.f, bv = 0.f, ad = 0.f, bd = 0.f, u = 0.f, uh = 0.f;
+        for (int i = 0; i < d; ++i) {
+          const float k = tok(a.K, t0 + t, i);
+          av = fmaf(W1[(size_t)jj * d + i], k, av);
+          bv = fmaf(W3[(size_t)jj * d + i], k, bv);
+          ad = fmaf(Ln[0][(size_t)jj * d + i], k, ad);
+          bd = fmaf(Ln[2][(size_t)jj * d + i], k, bd);
+        }
+        for (int r = 0; r < d; ++r) {
+          const float v = tok(a.V, t0 + t, r);
+          u = fmaf(W2[(size_t)r * dh + jj], v, u);
+          uh = fmaf(Ln[1][(size_t)r * dh + jj], v, uh);
+        }
+        AV[idx] = av; BV[idx] = bv; AD[idx] = ad; BD[idx] = bd; U[idx] = u; UH[idx] = uh;
+      }
+      __syncthreads();
+      float *HK = vec(6), *HD = vec(7), *XA = vec(8), *XB = vec(9), *XAD = vec(10), *XBD = vec(11);
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const float av = AV[idx], bv = BV[idx], ad = AD[idx], bd = BD[idx], u = U[idx], uh = UH[idx];
+        const float sg = sw_sig(av), sa = av * sg;
+        const float s1 = sg * (1.f + av * (1.f - sg));
+        const float s2 = sg * (1.f - sg) * (2.f + av * (1.f - 2.f * sg));
+        const float sd = s1 * ad;
+        const float gs = -uh * bv - u * bd, gsd = -u * bv;
+        HK[idx] = sa * bv;
+        HD[idx] = sd * bv + sa * bd;
+        XA[idx] = gs * s1 + gsd * s2 * ad;  // grad_a phi
+        XB[idx] = -uh * sa - u * sd;        // grad_b phi
+        XAD[idx] = gsd * s1;                // grad_a' phi
+        XBD[idx] = -u * sa;                 // grad_b' phi
+      }
+      __syncthreads();
+      // f' = Ln2 h + W2 h';  dv = -s lr (-f')
+      for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+        const int t = idx / d, r = idx % d;
+        float f = 0.f;
+        for (int jj = 0; jj < dh; ++jj) {
+          f = fmaf(Ln[1][(size_t)r * dh + jj], HK[(size_t)t * dh + jj], f);
+          f = fmaf(W2[(size_t)r * dh + jj], HD[(size_t)t * dh + jj], f);
+        }
+        FD[idx] = f;
+        const float lt = a.lr[head * a.T + t0 + t];
+        st_val(a.dV, (head * a.T + t0 + t) * (size_t)d + r, a.dtype, st * lt * f);
+      }
+      // dk = -s lr (W1^T XA + W3^T XB + Ln1^T XAD + Ln3^T XBD)
+      for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+        const int t = idx / d, i = idx % d;
+        float g = 0.f;
+        for (int jj = 0; jj < dh; ++jj) {
+          const size_t o = (size_t)t * dh + jj, w = (size_t)jj * d + i;
+          g = fmaf(W1[w], XA[o], g);
+          g = fmaf(W3[w], XB[o], g);
+          g = fmaf(Ln[0][w], XAD[o], g);
+          g = fmaf(Ln[2][w], XBD[o], g);
+        }
+        const float lt = a.lr[head * a.T + t0 + t];
+        st_val(a.dK, (head * a.T + t0 + t) * (size_t)d + i, a.dtype, -st * lt * g);
+      }
+      __syncthreads();
+      // phi_t = -v . f';  dlr = -s phi
+      for (int t = threadIdx.x; t < nt; t += blockDim.x) {
+        float ph = 0.f;
+        for (int r = 0; r < d; ++r) ph = fmaf(-tok(a.V, t0 + t, r), FD[(size_t)t * d + r], ph);
+        PHI[t] = ph;
+        a.dlr[head * a.T + t0 + t] = -st * ph;
+      }
+      // Lc1 += -s sum lr XA k^T;  Lc3 += -s sum lr XB k^T;  Lc2 += -s sum lr (-v) h'^T
+      for (size_t idx = threadIdx.x; idx < dd; idx += blockDim.x) {
+        const int jj = (int)(idx / d), i = (int)(idx % d);
+        float g1 = 0.f, g3 = 0.f;
+        for (int t = 0; t < nt; ++t) {
+          const float lk = a.lr[head * a.T + t0 + t] * tok(a.K, t0 + t, i);
+          g1 = fmaf(XA[(size_t)t * dh + jj], lk, g1);
+          g3 = fmaf(XB[(size_t)t * dh + jj], lk, g3);
+        }
+        Lc[0][idx] -= st * g1;
+        Lc[2][idx] -= st * g3;
+        const int r = (int)(idx / dh), jq = (int)(idx % dh);
+        float g2 = 0.f;
+        for (int t = 0; t < nt; ++t)
+          g2 = fmaf(-a.lr[head * a.T + t0 + t] * tok(a.V, t0 + t, r), HD[(size_t)t * dh + jq], g2);
+        Lc[1][idx] -= st * g2;
+      }
+      __syncthreads();
+    }
+    for (int j = 0; j < 3; ++j) {
+      float* tmp = Ln[j];
+      Ln[j] = Lc[j];
+      Lc[j] = tmp;
+    }
+    __syncthreads();
+  }
+  for (int j = 0; j < 3; ++j)
+    for (size_t i = threadIdx.x; i < dd; i += blockDim.x) a.dW[j][head * dd + i] = Ln[j][i];
+}
+
 }  // namespace
 
 bool bwd_supported(const ttt_cfg& g) {
@@ -255,6 +557,64 @@ int bwd_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const
     sum_over_batch_kernel<<<256, 256, 0, st>>>(a.dW, dW0, g.B, g.H, dd);
     prof_after(TTT_KERNEL_AUX, st);
     if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+  }
+  return TTT_OK;
+}
+
+}  // namespace ttt
+
+namespace ttt {
+
+bool bwd_swiglu_supported(const ttt_cfg& g) {
+  return g.fast_net == TTT_NET_SWIGLU && g.mode == TTT_MODE_SHIFTED && g.loss == TTT_LOSS_IP && !g.muon &&
+         !g.wnorm && g.momentum == 0.f && !g.lr_per_matrix;
+}
+
+size_t bwd_swiglu_workspace_bytes(const ttt_cfg& g) {
+  const int n_chunks = (g.T + g.chunk - 1) / g.chunk;
+  const size_t heads = (size_t)g.B * g.H, dd = (size_t)g.d * g.dh;
+  const size_t per_head = sw_layout(g.d, g.dh, n_chunks).total;
+  return kStatusBytes + 3 * align_up(heads * dd * sizeof(float), 256) + heads * per_head * sizeof(float);
+}
+
+int bwd_swiglu_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const float* lr,
+                   const float* const W0[3], const void* dO, const float* const dWf[3], void* dQ, void* dK, void* dV,
+                   float* dlr, float* const dW0[3], char* ws, cudaStream_t st) {
+  const int n_chunks = (g.T + g.chunk - 1) / g.chunk;
+  if (g.update_mask && n_chunks > kMaxMaskChunks) return TTT_ERR_UNSUPPORTED;
+  SwArgs a{};
+  a.B = g.B; a.H = g.H; a.T = g.T; a.d = g.d; a.dh = g.dh; a.chunk = g.chunk; a.dtype = g.dtype;
+  a.w0_per_batch = g.w0_per_batch;
+  a.step = g.step;
+  a.Q = Q; a.K = K; a.V = V; a.lr = lr; a.dO = dO;
+  a.dQ = dQ; a.dK = dK; a.dV = dV; a.dlr = dlr;
+  const size_t heads = (size_t)g.B * g.H, dd = (size_t)g.d * g.dh;
+  const size_t per = align_up(heads * dd * sizeof(float), 256);
+  for (int j = 0; j < 3; ++j) {
+    a.W0[j] = W0[j];
+    a.dWf[j] = dWf[j];
+    a.dW[j] = g.w0_per_batch ? dW0[j] : reinterpret_cast<float*>(ws + kStatusBytes + j * per);
+  }
+  a.scratch = reinterpret_cast<float*>(ws + kStatusBytes + 3 * per);
+  a.head_floats = sw_layout(g.d, g.dh, n_chunks).total;
+  a.has_mask = 0;
+  if (g.update_mask) {
+    for (int i = 0; i < n_chunks; ++i)
+      if (!g.update_mask[i]) a.has_mask = 1;
+    for (int i = 0; i < n_chunks; ++i)
+      if (g.update_mask[i]) a.mask.w[i >> 5] |= 1u << (i & 31);
+  }
+  prof_before(TTT_KERNEL_SIMT, st);
+  swiglu_bwd_kernel<<<(unsigned)heads, kBwThreads, 0, st>>>(a);
+  prof_after(TTT_KERNEL_SIMT, st);
+  if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+  if (!g.w0_per_batch) {
+    for (int j = 0; j < 3; ++j) {
+      prof_before(TTT_KERNEL_AUX, st);
+      sum_over_batch_kernel<<<256, 256, 0, st>>>(a.dW[j], dW0[j], g.B, g.H, dd);
+      prof_after(TTT_KERNEL_AUX, st);
+      if (cudaGetLastError() != cudaSuccess) return TTT_ERR_CUDA;
+    }
   }
   return TTT_OK;
 }

@@ -57,6 +57,11 @@ size_t bwd_workspace_bytes(const ttt_cfg& cfg);
 int bwd_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const float* lr, const float* W0,
             const void* dO, const float* dWf, void* dQ, void* dK, void* dV, float* dlr, float* dW0, char* ws,
             cudaStream_t st);
+bool bwd_swiglu_supported(const ttt_cfg& cfg);
+size_t bwd_swiglu_workspace_bytes(const ttt_cfg& cfg);
+int bwd_swiglu_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const float* lr,
+                   const float* const W0[3], const void* dO, const float* const dWf[3], void* dQ, void* dK, void* dV,
+                   float* dlr, float* const dW0[3], char* ws, cudaStream_t st);
 
 // ---- misc ------------------------------------------------------------------
 // TTT_OK or TTT_ERR_ARG: field ranges and sizes of *cfg (host only).
