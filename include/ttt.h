@@ -224,8 +224,8 @@ TTT_API int ttt_bwd(const ttt_cfg* cfg, const void* Q, const void* K, const void
                     float* dlr, float* dW0, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The same for the SwiGLU fast net with plain gradient steps (muon = wnorm = 0,
- * momentum = 0, one rate per token: lr_per_matrix = 0) in shifted mode with
- * the inner-product loss: W0_j, dWf_j and dW0_j as the three matrices of
+ * momentum = 0, one rate per token: lr_per_matrix = 0) in shifted mode,
+ * inner-product or MSE loss: W0_j, dWf_j and dW0_j as the three matrices of
  * ttt_fwd (W1 [dh, d], W2 [d, dh], W3 [dh, d] per head; W0 and dW0 shared over
  * the batch unless w0_per_batch, dWf per (batch, head)). The second-order terms
  * of the inner updates (the derivative of each token's gradient along the

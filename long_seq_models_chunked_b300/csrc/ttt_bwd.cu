@@ -209,17 +209,19 @@ __global__ void sum_over_batch_kernel(const float* dW, float* dW0, int B, int H,
 
 // ---------------------------------------------------------------- SwiGLU net
 // The SwiGLU net f(x) = W2 (silu(W1 x) * (W3 x)) with plain gradient steps in
-// shifted mode and the inner-product loss l = -<f(k), v>; one rate per token
-// (lr_t) for all three matrices. Per chunk c: o_t = f(q_t; W_c) for its
+// shifted mode, the inner-product loss l = -<f(k), v> or the MSE loss
+// l = |f(k) - v|^2 / 2; one rate per token (lr_t) for all three matrices. Per chunk c: o_t = f(q_t; W_c) for its
 // queries and W_{c+1} = W_c - s sum_t lr_t grad_W l_t(W_c). With Lh = dL/dW_{c+1}
 // (the adjoint reaching W_{c+1}) and phi_t = <Lh, grad_W l_t(W_c)>:
 //   dL/dW_c = Lh - s sum_t lr_t grad_W phi_t + sum_t grad_W <dO_t, f(q_t; W_c)>
 //   dlr_t = -s phi_t,  dk_t = -s lr_t grad_k phi_t,  dv_t = -s lr_t grad_v phi_t,
 // phi_t being the derivative of l_t along Lh. With a = W1 k, b = W3 k, s = silu(a),
-// h = s b, u = W2^T v and the tangents along Lh (dots): a' = Lh1 k, b' = Lh3 k,
-// s' = silu'(a) a', h' = s' b + s b', f' = Lh2 h + W2 h', u' = Lh2^T v:
-//   phi = -v . f';  grad_v phi = -f';  grad_W2 phi = -v h'^T;
-//   gs = -u' b - u b',  gb = -u' s - u s',  gs' = -u b,  gb' = -u s,
+// h = s b, f = W2 h, the loss's dl/df = y (y = -v for the inner product, f - v for
+// MSE) and the tangents along Lh (dots): a' = Lh1 k, b' = Lh3 k, s' = silu'(a) a',
+// h' = s' b + s b', f' = Lh2 h + W2 h':
+//   phi = y . f';  grad_v phi = -f';  grad_W2 phi = y h'^T [+ f' h^T for MSE];
+//   gh = Lh2^T y [+ W2^T f' for MSE],  gh' = W2^T y,
+//   gs = gh b + gh' b',  gb = gh s + gh' s',  gs' = gh' b,  gb' = gh' s,
 //   ga = gs silu'(a) + gs' silu''(a) a',  ga' = gs' silu'(a),
 //   grad_W1 phi = ga k^T,  grad_W3 phi = gb k^T,
 //   grad_k phi = W1^T ga + W3^T gb + Lh1^T ga' + Lh3^T gb',
@@ -228,7 +230,7 @@ __global__ void sum_over_batch_kernel(const float* dW, float* dW0, int B, int H,
 constexpr int kSwTb = 16;  // tokens per block
 
 struct SwArgs {
-  int B, H, T, d, dh, chunk, dtype, w0_per_batch, has_mask;
+  int B, H, T, d, dh, chunk, dtype, w0_per_batch, has_mask, loss;
   float step;
   const void* Q;
   const void* K;
@@ -248,7 +250,7 @@ struct SwArgs {
 };
 
 struct SwLayout {
-  size_t mat, Wc, L0, L1, vec, fd, phi, total;  // mat: floats of one matrix (padded)
+  size_t mat, Wc, L0, L1, vec, fd, cv, total;  // mat: floats of one matrix (padded)
 };
 
 __host__ __device__ inline SwLayout sw_layout(int d, int dh, int n_chunks) {
@@ -257,10 +259,10 @@ __host__ __device__ inline SwLayout sw_layout(int d, int dh, int n_chunks) {
   L.Wc = 0;
   L.L0 = (size_t)n_chunks * 3 * L.mat;
   L.L1 = L.L0 + 3 * L.mat;
-  L.vec = L.L1 + 3 * L.mat;                                    // 12 vectors of [kSwTb][dh]
-  L.fd = L.vec + 12 * align_up((size_t)kSwTb * dh, 64);       // [kSwTb][d]
-  L.phi = L.fd + align_up((size_t)kSwTb * d, 64);              // [kSwTb]
-  L.total = L.phi + 64;
+  L.vec = L.L1 + 3 * L.mat;                                    // 13 vectors of [kSwTb][dh]
+  L.fd = L.vec + 13 * align_up((size_t)kSwTb * dh, 64);       // f' of the block: [kSwTb][d]
+  L.cv = L.fd + align_up((size_t)kSwTb * d, 64);               // y (dl/df) of the block: [kSwTb][d]
+  L.total = L.cv + align_up((size_t)kSwTb * d, 64);
   return L;
 }
 
@@ -279,7 +281,8 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
   const size_t vs = align_up((size_t)kSwTb * dh, 64);
   auto vec = [&](int i) { return ws + L.vec + (size_t)i * vs; };
   float* FD = ws + L.fd;
-  float* PHI = ws + L.phi;
+  float* CV = ws + L.cv;
+  const bool mse = a.loss == TTT_LOSS_MSE;
   const float st = a.step;
   auto tok = [&](const void* p, size_t t, int i) { return ld_val(p, (head * a.T + t) * (size_t)d + i, a.dtype); };
 
@@ -297,27 +300,43 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
     if (a.has_mask && !mask_bit(a.mask, c)) continue;
     const float *W1 = Wc(c, 0), *W2 = Wc(c, 1), *W3 = Wc(c, 2);
     float *N1 = Wc(c + 1, 0), *N2 = Wc(c + 1, 1), *N3 = Wc(c + 1, 2);
-    float *DA = vec(0), *DB = vec(1), *HH = vec(2);
+    float *AA = vec(0), *BB = vec(1), *HH = vec(2), *DA = vec(3), *DB = vec(4);
     for (int t0 = s; t0 < e; t0 += kSwTb) {
       const int nt = min(kSwTb, e - t0);
-      // a, b, u = W2^T (lr v): DA = -u b silu'(a) (the rate folded in), DB = -u s, HH = h
+      // a, b, h
       for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
         const int t = idx / dh, jj = idx % dh;
-        float av = 0.f, bv = 0.f, u = 0.f;
+        float av = 0.f, bv = 0.f;
         for (int i = 0; i < d; ++i) {
           const float k = tok(a.K, t0 + t, i);
           av = fmaf(W1[(size_t)jj * d + i], k, av);
           bv = fmaf(W3[(size_t)jj * d + i], k, bv);
         }
-        for (int r = 0; r < d; ++r) u = fmaf(W2[(size_t)r * dh + jj], tok(a.V, t0 + t, r), u);
-        const float lt = a.lr[head * a.T + t0 + t];
-        const float sg = sw_sig(av), sa = av * sg;
-        DA[idx] = -lt * u * bv * sg * (1.f + av * (1.f - sg));
-        DB[idx] = -lt * u * sa;
-        HH[idx] = sa * bv;
+        AA[idx] = av;
+        BB[idx] = bv;
+        HH[idx] = av * sw_sig(av) * bv;
       }
       __syncthreads();
-      // W1 -= s sum_t DA k^T;  W3 -= s sum_t DB k^T;  W2 -= s sum_t (-lr v) h^T
+      // CV = lr y: y = -v (inner product) or W2 h - v (MSE)
+      for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+        const int t = idx / d, r = idx % d;
+        float y = -tok(a.V, t0 + t, r);
+        if (mse)
+          for (int jj = 0; jj < dh; ++jj) y = fmaf(W2[(size_t)r * dh + jj], HH[(size_t)t * dh + jj], y);
+        CV[idx] = a.lr[head * a.T + t0 + t] * y;
+      }
+      __syncthreads();
+      // DA = (W2^T CV) b silu'(a),  DB = (W2^T CV) s
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const int t = idx / dh, jj = idx % dh;
+        float dhv = 0.f;
+        for (int r = 0; r < d; ++r) dhv = fmaf(W2[(size_t)r * dh + jj], CV[(size_t)t * d + r], dhv);
+        const float av = AA[idx], sg = sw_sig(av);
+        DA[idx] = dhv * BB[idx] * sg * (1.f + av * (1.f - sg));
+        DB[idx] = dhv * av * sg;
+      }
+      __syncthreads();
+      // W1 -= s sum_t DA k^T;  W3 -= s sum_t DB k^T;  W2 -= s sum_t CV h^T
       for (size_t idx = threadIdx.x; idx < dd; idx += blockDim.x) {
         const int jj = (int)(idx / d), i = (int)(idx % d);
         float g1 = 0.f, g3 = 0.f;
@@ -330,8 +349,7 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
         N3[idx] -= st * g3;
         const int r = (int)(idx / dh), jq = (int)(idx % dh);
         float g2 = 0.f;
-        for (int t = 0; t < nt; ++t)
-          g2 = fmaf(-a.lr[head * a.T + t0 + t] * tok(a.V, t0 + t, r), HH[(size_t)t * dh + jq], g2);
+        for (int t = 0; t < nt; ++t) g2 = fmaf(CV[(size_t)t * d + r], HH[(size_t)t * dh + jq], g2);
         N2[idx] -= st * g2;
       }
       __syncthreads();
@@ -411,9 +429,10 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
       }
       // -- keys: the vectors of phi_t along Ln
       float *AV = vec(0), *BV = vec(1), *AD = vec(2), *BD = vec(3), *U = vec(4), *UH = vec(5);
+      float *HK = vec(6), *HD = vec(7), *XA = vec(8), *XB = vec(9), *XAD = vec(10), *XBD = vec(11), *WF = vec(12);
       for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
         const int t = idx / dh, jj = idx % dh;
-        float av = 0.f, bv = 0.f, ad = 0.f, bd = 0.f, u = 0.f, uh = 0.f;
+        float av = 0.f, bv = 0.f, ad = 0.f, bd = 0.f;
         for (int i = 0; i < d; ++i) {
           const float k = tok(a.K, t0 + t, i);
           av = fmaf(W1[(size_t)jj * d + i], k, av);
@@ -421,28 +440,33 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
           ad = fmaf(Ln[0][(size_t)jj * d + i], k, ad);
           bd = fmaf(Ln[2][(size_t)jj * d + i], k, bd);
         }
-        for (int r = 0; r < d; ++r) {
-          const float v = tok(a.V, t0 + t, r);
-          u = fmaf(W2[(size_t)r * dh + jj], v, u);
-          uh = fmaf(Ln[1][(size_t)r * dh + jj], v, uh);
-        }
-        AV[idx] = av; BV[idx] = bv; AD[idx] = ad; BD[idx] = bd; U[idx] = u; UH[idx] = uh;
+        AV[idx] = av; BV[idx] = bv; AD[idx] = ad; BD[idx] = bd;
+        HK[idx] = av * sw_sig(av) * bv;
       }
       __syncthreads();
-      float *HK = vec(6), *HD = vec(7), *XA = vec(8), *XB = vec(9), *XAD = vec(10), *XBD = vec(11);
+      // y = dl/df: -v, or W2 h - v (MSE)
+      for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+        const int t = idx / d, r = idx % d;
+        float y = -tok(a.V, t0 + t, r);
+        if (mse)
+          for (int jj = 0; jj < dh; ++jj) y = fmaf(W2[(size_t)r * dh + jj], HK[(size_t)t * dh + jj], y);
+        CV[idx] = y;
+      }
+      __syncthreads();
+      // u = W2^T y, u' = Ln2^T y; h' = s' b + s b'
       for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
-        const float av = AV[idx], bv = BV[idx], ad = AD[idx], bd = BD[idx], u = U[idx], uh = UH[idx];
-        const float sg = sw_sig(av), sa = av * sg;
+        const int t = idx / dh, jj = idx % dh;
+        float u = 0.f, uh = 0.f;
+        for (int r = 0; r < d; ++r) {
+          const float y = CV[(size_t)t * d + r];
+          u = fmaf(W2[(size_t)r * dh + jj], y, u);
+          uh = fmaf(Ln[1][(size_t)r * dh + jj], y, uh);
+        }
+        U[idx] = u;
+        UH[idx] = uh;
+        const float av = AV[idx], sg = sw_sig(av);
         const float s1 = sg * (1.f + av * (1.f - sg));
-        const float s2 = sg * (1.f - sg) * (2.f + av * (1.f - 2.f * sg));
-        const float sd = s1 * ad;
-        const float gs = -uh * bv - u * bd, gsd = -u * bv;
-        HK[idx] = sa * bv;
-        HD[idx] = sd * bv + sa * bd;
-        XA[idx] = gs * s1 + gsd * s2 * ad;  // grad_a phi
-        XB[idx] = -uh * sa - u * sd;        // grad_b phi
-        XAD[idx] = gsd * s1;                // grad_a' phi
-        XBD[idx] = -u * sa;                 // grad_b' phi
+        HD[idx] = s1 * AD[idx] * BV[idx] + av * sg * BD[idx];
       }
       __syncthreads();
       // f' = Ln2 h + W2 h';  dv = -s lr (-f')
@@ -457,6 +481,26 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
         const float lt = a.lr[head * a.T + t0 + t];
         st_val(a.dV, (head * a.T + t0 + t) * (size_t)d + r, a.dtype, st * lt * f);
       }
+      __syncthreads();
+      // gh = u' [+ W2^T f' for MSE], gh' = u: the gradients of phi along a, b, a', b'
+      for (int idx = threadIdx.x; idx < nt * dh; idx += blockDim.x) {
+        const int t = idx / dh, jj = idx % dh;
+        float wf = 0.f;
+        if (mse)
+          for (int r = 0; r < d; ++r) wf = fmaf(W2[(size_t)r * dh + jj], FD[(size_t)t * d + r], wf);
+        WF[idx] = wf;
+        const float av = AV[idx], bv = BV[idx], ad = AD[idx], bd = BD[idx];
+        const float sg = sw_sig(av), sa = av * sg;
+        const float s1 = sg * (1.f + av * (1.f - sg));
+        const float s2 = sg * (1.f - sg) * (2.f + av * (1.f - 2.f * sg));
+        const float gh = UH[idx] + wf, ghd = U[idx];
+        const float gs = gh * bv + ghd * bd, gsd = ghd * bv;
+        XA[idx] = gs * s1 + gsd * s2 * ad;   // grad_a phi
+        XB[idx] = gh * sa + ghd * s1 * ad;   // grad_b phi
+        XAD[idx] = gsd * s1;                 // grad_a' phi
+        XBD[idx] = ghd * sa;                 // grad_b' phi
+      }
+      __syncthreads();
       // dk = -s lr (W1^T XA + W3^T XB + Ln1^T XAD + Ln3^T XBD)
       for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
         const int t = idx / d, i = idx % d;
@@ -471,15 +515,13 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
         const float lt = a.lr[head * a.T + t0 + t];
         st_val(a.dK, (head * a.T + t0 + t) * (size_t)d + i, a.dtype, -st * lt * g);
       }
-      __syncthreads();
-      // phi_t = -v . f';  dlr = -s phi
+      // phi_t = y . f';  dlr = -s phi
       for (int t = threadIdx.x; t < nt; t += blockDim.x) {
         float ph = 0.f;
-        for (int r = 0; r < d; ++r) ph = fmaf(-tok(a.V, t0 + t, r), FD[(size_t)t * d + r], ph);
-        PHI[t] = ph;
+        for (int r = 0; r < d; ++r) ph = fmaf(CV[(size_t)t * d + r], FD[(size_t)t * d + r], ph);
         a.dlr[head * a.T + t0 + t] = -st * ph;
       }
-      // Lc1 += -s sum lr XA k^T;  Lc3 += -s sum lr XB k^T;  Lc2 += -s sum lr (-v) h'^T
+      // Lc1 -= s sum lr XA k^T;  Lc3 -= s sum lr XB k^T;  Lc2 -= s sum lr (y h'^T [+ f' h^T])
       for (size_t idx = threadIdx.x; idx < dd; idx += blockDim.x) {
         const int jj = (int)(idx / d), i = (int)(idx % d);
         float g1 = 0.f, g3 = 0.f;
@@ -492,8 +534,12 @@ __global__ void __launch_bounds__(kBwThreads) swiglu_bwd_kernel(const __grid_con
         Lc[2][idx] -= st * g3;
         const int r = (int)(idx / dh), jq = (int)(idx % dh);
         float g2 = 0.f;
-        for (int t = 0; t < nt; ++t)
-          g2 = fmaf(-a.lr[head * a.T + t0 + t] * tok(a.V, t0 + t, r), HD[(size_t)t * dh + jq], g2);
+        for (int t = 0; t < nt; ++t) {
+          const float lt = a.lr[head * a.T + t0 + t];
+          float gw = CV[(size_t)t * d + r] * HD[(size_t)t * dh + jq];
+          if (mse) gw = fmaf(FD[(size_t)t * d + r], HK[(size_t)t * dh + jq], gw);
+          g2 = fmaf(lt, gw, g2);
+        }
         Lc[1][idx] -= st * g2;
       }
       __syncthreads();
@@ -566,8 +612,8 @@ int bwd_run(const ttt_cfg& g, const void* Q, const void* K, const void* V, const
 namespace ttt {
 
 bool bwd_swiglu_supported(const ttt_cfg& g) {
-  return g.fast_net == TTT_NET_SWIGLU && g.mode == TTT_MODE_SHIFTED && g.loss == TTT_LOSS_IP && !g.muon &&
-         !g.wnorm && g.momentum == 0.f && !g.lr_per_matrix;
+  return g.fast_net == TTT_NET_SWIGLU && g.mode == TTT_MODE_SHIFTED && !g.muon && !g.wnorm &&
+         g.momentum == 0.f && !g.lr_per_matrix;
 }
 
 size_t bwd_swiglu_workspace_bytes(const ttt_cfg& g) {
@@ -583,7 +629,7 @@ int bwd_swiglu_run(const ttt_cfg& g, const void* Q, const void* K, const void* V
   const int n_chunks = (g.T + g.chunk - 1) / g.chunk;
   if (g.update_mask && n_chunks > kMaxMaskChunks) return TTT_ERR_UNSUPPORTED;
   SwArgs a{};
-  a.B = g.B; a.H = g.H; a.T = g.T; a.d = g.d; a.dh = g.dh; a.chunk = g.chunk; a.dtype = g.dtype;
+  a.B = g.B; a.H = g.H; a.T = g.T; a.d = g.d; a.dh = g.dh; a.chunk = g.chunk; a.dtype = g.dtype; a.loss = g.loss;
   a.w0_per_batch = g.w0_per_batch;
   a.step = g.step;
   a.Q = Q; a.K = K; a.V = V; a.lr = lr; a.dO = dO;

@@ -1,8 +1,8 @@
 """The outer-loop backward of the SwiGLU net (ttt_bwd_swiglu) against the fp64
 oracle's reverse mode (automatic differentiation of the forward, pinned to
 central finite differences): plain gradient steps in shifted mode, the
-inner-product loss, fp32 storage (tolerance 1e-4, max relative error per
-tensor) and bf16 storage (2e-2); W0 shared over the batch or one per batch."""
+inner-product and MSE losses, fp32 storage (tolerance 1e-4, max relative error
+per tensor) and bf16 storage (2e-2); W0 shared over the batch or one per batch."""
 import numpy as np
 import pytest
 
@@ -21,6 +21,12 @@ CASES = {
     "fp32_chunk1": (TINY.replace(name="sbwd_c1", B=1, H=1, T=24, chunk=1, d=8, dh=16, step=0.5, seed=113), 1e-4),
     "bf16": (TINY.replace(name="sbwd_bf16", B=2, H=1, T=128, chunk=32, d=32, dh=64, dtype="bf16", step=0.8,
                           seed=114), 2e-2),
+    "mse_fp32": (TINY.replace(name="sbwd_mse", B=2, H=2, T=150, chunk=32, d=16, dh=32, loss="mse", step=0.5,
+                              seed=115), 1e-4),
+    "mse_fp32_ragged_odd": (TINY.replace(name="sbwd_mse_odd", B=1, H=2, T=97, chunk=20, d=8, dh=24, loss="mse",
+                                         update="odd", step=0.5, seed=116), 1e-4),
+    "mse_bf16": (TINY.replace(name="sbwd_mse_bf16", B=1, H=2, T=128, chunk=32, d=32, dh=64, loss="mse",
+                              dtype="bf16", step=0.5, seed=117), 2e-2),
 }
 
 
