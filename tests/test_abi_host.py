@@ -152,3 +152,31 @@ def test_swiglu_backward_support():
         with pytest.raises(abi.TTTError) as e:
             abi.ttt_bwd_swiglu_workspace_bytes(abi.cfg_from_spec(bad).cfg)
         assert e.value.code == abi.TTT_ERR_UNSUPPORTED
+
+
+def _swbwd_call(c, **over):
+    # fake, well-separated device-like addresses (the checks here run before any CUDA call)
+    p = {n: _fake(i + 1) for i, n in enumerate(
+        ["Q", "K", "V", "lr", "W1", "W2", "W3", "dO", "F1", "F2", "F3",
+         "dQ", "dK", "dV", "dlr", "G1", "G2", "G3", "ws"])}
+    need = c_size = ctypes.c_size_t(0)
+    assert abi.lib().ttt_bwd_swiglu_workspace_bytes(ctypes.byref(c), ctypes.byref(c_size)) == abi.TTT_OK
+    p["ws_bytes"] = need.value
+    p.update(over)
+    return abi.lib().ttt_bwd_swiglu(ctypes.byref(c), p["Q"], p["K"], p["V"], p["lr"], p["W1"], p["W2"], p["W3"],
+                                    p["dO"], p["F1"], p["F2"], p["F3"], p["dQ"], p["dK"], p["dV"], p["dlr"],
+                                    p["G1"], p["G2"], p["G3"], p["ws"], p["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Q=0), abi.TTT_ERR_ARG),
+    (dict(W2=_fake(6) + 4), abi.TTT_ERR_ARG),         # misaligned
+    (dict(dQ=_fake(1)), abi.TTT_ERR_ARG),             # an output on an input
+    (dict(G3=_fake(17)), abi.TTT_ERR_ARG),            # two outputs alias
+    (dict(ws=0), abi.TTT_ERR_WORKSPACE),
+    (dict(ws_bytes=255), abi.TTT_ERR_WORKSPACE),
+])
+def test_swiglu_backward_rejects_before_launch(over, code):
+    spec = synth.WORKLOADS["tiny_fp32"].replace(wnorm=False, muon=False)
+    c = abi.cfg_from_spec(spec).cfg
+    assert _swbwd_call(c, **over) == code
