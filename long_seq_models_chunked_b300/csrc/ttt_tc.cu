@@ -40,7 +40,7 @@ using namespace tcu;
 int g_split_mask = 7;  // test hook: stages that carry split operands in SPLIT precision
 std::atomic<int> g_stall_next_fwd{0};  // test hook: the next forward launch withholds its loads
 bool g_grad_pairs = true;               // test hook: the chunk gradient on CTA pairs (single-GPU build)
-bool g_apply_pairs = true;              // test hook: the apply on CTA pairs (single-GPU build)
+// (the apply runs on CTA pairs in the single-GPU build whenever a chunk has two token tiles)
 
 
 // ============================================================ forward, multicast
@@ -1458,7 +1458,7 @@ class TcLayer {
       p.cm = cm;
     };
 #if TTT_HAS_MULTICAST
-    if (g_apply_pairs && mt >= 2) {
+    if (mt >= 2) {
       OPairOp::Params p{};
       p.mH = mHq; p.mW2 = mW2p; p.O = static_cast<bf16*>(O_);
       p.d = d; p.dh = g_.dh; p.T = T_; p.chunk_start = s; p.valid = valid;
