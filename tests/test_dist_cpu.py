@@ -1,4 +1,4 @@
-"""Multi-process host logic on CPU ranks (gloo, world size 2).
+"""Multi-process host logic on CPU ranks (gloo, world sizes 2 and 4).
 
 * Context parallelism (LaCT page, "Large Chunk Test-Time Training", §2.2.2):
   each rank computes the gradient of its shard of a chunk's tokens with the
@@ -6,7 +6,7 @@
   (the chunk gradient is a sum over tokens, §2.1), so every rank can then run
   the same Newton-Schulz step and update.
 * The context-parallel driver (long_seq_models_chunked_b300.cp: one rank's chunk
-  loop, an all-reduce at every update) over two gloo ranks, with each rank's
+  loop, an all-reduce at every update) over two and four gloo ranks, with each rank's
   steps computed by the fp64 oracle, equals the unsharded layer.
 * The benchmark's N-GPU reduction helpers (max of the per-rank step time, sum
   of the tokens) give the whole-job figures.
@@ -189,9 +189,10 @@ def test_context_parallel_gradient_sum_equals_whole_chunk():
     assert all(v <= 1e-12 for v in res.values()), res
 
 
-def test_context_parallel_driver_equals_unsharded_layer():
-    res = _run(_cp_driver_worker)
-    assert all(v <= 1e-10 for v in res.values()), res
+@pytest.mark.parametrize("world", [2, 4])
+def test_context_parallel_driver_equals_unsharded_layer(world):
+    res = _run(_cp_driver_worker, world=world)
+    assert len(res) == world and all(v <= 1e-10 for v in res.values()), res
 
 
 def test_bench_reductions_over_ranks():
