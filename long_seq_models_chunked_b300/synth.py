@@ -25,6 +25,7 @@ workload table below states):
 from __future__ import annotations
 
 import dataclasses
+import functools
 import math
 from typing import Dict, List, Optional, Sequence, Tuple
 
@@ -153,13 +154,22 @@ def to_storage(x64: np.ndarray, dtype: str) -> Tuple[np.ndarray, np.ndarray]:
 
 
 # ---------------------------------------------------------------- per-head draws
+@functools.lru_cache(maxsize=6)
+def _block_normals(seed: int, tensor: int, b: int, h: int, blk: int, width: int) -> np.ndarray:
+    """One block of TOKEN_BLOCK tokens' standard normals (read-only). The last few
+    blocks are kept, so walking a head chunk by chunk draws each block once."""
+    z = _rng(seed, tensor, b, h, blk).standard_normal((TOKEN_BLOCK, width))
+    z.setflags(write=False)
+    return z
+
+
 def _token_draw(spec: LayerSpec, tensor: int, b: int, h: int, t0: int, t1: int,
                 width: int) -> np.ndarray:
     """Standard normals for tokens [t0, t1) of one head, shape [t1-t0, width]."""
     out = np.empty((t1 - t0, width), dtype=np.float64)
     blk0, blk1 = t0 // TOKEN_BLOCK, (t1 - 1) // TOKEN_BLOCK
     for blk in range(blk0, blk1 + 1):
-        z = _rng(spec.seed, tensor, b, h, blk).standard_normal((TOKEN_BLOCK, width))
+        z = _block_normals(spec.seed, tensor, b, h, blk, width)
         s = max(t0, blk * TOKEN_BLOCK)
         e = min(t1, (blk + 1) * TOKEN_BLOCK)
         out[s - t0:e - t0] = z[s - blk * TOKEN_BLOCK:e - blk * TOKEN_BLOCK]
