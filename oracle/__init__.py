@@ -18,6 +18,7 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
                                 column leaves its matrix unchanged)
   ttt_head / ttt_layer        - pinned in the special cases with closed forms
                                 (delta rule, block-shifted linear attention,
+                                a chunk of orthonormal keys memorised under MSE,
                                 single-chunk linear attention, zero update) and by
                                 invariants (causality, resume, permutation);
                                 the full SwiGLU + Muon + weight-norm chain has no

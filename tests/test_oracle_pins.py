@@ -129,6 +129,33 @@ def test_linear_mse_chunk1_is_delta_rule():
     assert np.abs(Wf - W).max() <= 1e-12
 
 
+def test_linear_mse_chunk_of_orthonormal_keys_memorises_it():
+    """Linear net, MSE, SGD, unit rates, each chunk's keys orthonormal (C <= d):
+    the chunk-summed step is then an exact least-squares solve on the keys' span,
+    so the updated W sends every key of the chunk to its value and leaves the
+    orthogonal complement untouched. In shifted order the next chunk's queries
+    read that W: queries equal to the previous chunk's keys return its values."""
+    rng = np.random.default_rng(33)
+    d, C, n = 8, 4, 3
+    T = C * n
+    W0 = rng.standard_normal((d, d)) / np.sqrt(d)
+    K = np.concatenate([np.linalg.qr(rng.standard_normal((d, C)))[0].T for _ in range(n)])
+    V = rng.standard_normal((T, d))
+    Q = rng.standard_normal((T, d))
+    Q[C:] = K[:-C]                     # chunk c+1 asks for chunk c's keys
+    cfg = orc.OracleCfg(chunk=C, fast_net="linear", loss="mse", muon=False, wnorm=False)
+    O, (Wf,) = orc.ttt_head(cfg, Q, K, V, np.ones(T), (W0,))
+    assert np.abs(O[:C] - Q[:C] @ W0.T).max() <= 1e-12
+    assert np.abs(O[C:] - V[:-C]).max() <= 1e-12
+    Kl = K[-C:]
+    assert np.abs(Kl @ Wf.T - V[-C:]).max() <= 1e-12
+    # the last step moved W only on the span of the last chunk's keys
+    _, (Wp,) = orc.ttt_head(cfg, Q[:-C], K[:-C], V[:-C], np.ones(T - C), (W0,))
+    u = rng.standard_normal(d)
+    u -= Kl.T @ (Kl @ u)
+    assert np.abs(Wf @ u - Wp @ u).max() <= 1e-12
+
+
 @pytest.mark.parametrize("mask", [None, [1, 0, 1, 1, 0], [0, 1, 0, 1, 0]])
 def test_linear_ip_is_block_shifted_linear_attention(mask):
     """Linear net, inner-product loss, SGD: o_t = W0 q_t + sum over tokens s of
