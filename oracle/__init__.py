@@ -21,9 +21,12 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
                                 a chunk of orthonormal keys memorised under MSE,
                                 single-chunk linear attention, zero update) and by
                                 invariants (causality, resume, permutation);
-                                the full SwiGLU + Muon + weight-norm chain has no
-                                printed values to check against: parity unpinned
-                                beyond those compositions.
+                                the full SwiGLU + Muon + weight-norm chain (no page
+                                prints values for it) by its equivariance under input
+                                rotations, output sign-permutations and hidden-unit
+                                permutations, with momentum and a mask, and by the
+                                closed form of a one-token Muon step (the unit
+                                rank-one gradient times the quintic iterated from 1).
   apply_inclusive (inclusive  - pinned (chunk-1 linear MSE = the delta rule read after
   order)                        the update; linear inner product = causal linear
                                 attention for every chunk size; chunk-1 SwiGLU = the

@@ -256,6 +256,87 @@ def test_weight_norm_restores_row_norms_and_keeps_directions(shape):
     assert np.abs(ratio - ratio[:, :1]).max() <= 1e-12   # one positive scale per row
 
 
+def _orthogonal(n, rng):
+    q, r = np.linalg.qr(rng.standard_normal((n, n)))
+    return q * np.sign(np.diag(r))
+
+
+@pytest.mark.parametrize("loss", ["ip", "mse"])
+@pytest.mark.parametrize("momentum", [0.0, 0.5])
+def test_muon_layer_is_equivariant_under_rotations_and_hidden_permutations(loss, momentum):
+    """The whole SwiGLU + Muon + weight-norm chain, over several chunks with a mask.
+    Rotate the input space (R, any orthogonal), sign-permute the output space (S) and
+    permute the hidden units (P): q, k -> R q, R k;  v -> S v;  W1, W3 -> P W (R^T);
+    W2 -> S W2 P^T. Then f'(R x) = S f(x), both losses are unchanged, every gradient
+    moves the same way as its matrix, Newton-Schulz commutes with orthogonal factors on
+    either side, and the rows of every matrix keep their norms (up to the order), so
+    O' = O S^T and each final matrix is the transformed final matrix. A weight norm over
+    the wrong axis, or a Newton-Schulz scaling by anything but an orthogonally invariant
+    norm, breaks it."""
+    rng = np.random.default_rng(77)
+    d, dh, C, T = 6, 10, 5, 17
+    W = _rand_weights("swiglu", d, dh, rng, scale=2.0)
+    Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
+    eta = rng.uniform(0.0, 0.3, T)
+    R = _orthogonal(d, rng)
+    S = np.eye(d)[rng.permutation(d)] * rng.choice([-1.0, 1.0], d)[:, None]
+    P = np.eye(dh)[rng.permutation(dh)]
+    cfg = orc.OracleCfg(chunk=C, loss=loss, muon=True, wnorm=True, step=0.7, mask=[1, 0, 1, 1],
+                        momentum=momentum)
+    O, (W1, W2, W3) = orc.ttt_head(cfg, Q, K, V, eta, W)
+    Wt = (P @ W[0] @ R.T, S @ W[1] @ P.T, P @ W[2] @ R.T)
+    Ot, (W1t, W2t, W3t) = orc.ttt_head(cfg, Q @ R.T, K @ R.T, V @ S.T, eta, Wt)
+    assert np.abs(Ot - O @ S.T).max() <= 1e-10 * np.abs(O).max()
+    assert np.abs(W1t - P @ W1 @ R.T).max() <= 1e-10
+    assert np.abs(W2t - S @ W2 @ P.T).max() <= 1e-10
+    assert np.abs(W3t - P @ W3 @ R.T).max() <= 1e-10
+
+
+def _quintic_at_one(iters, a, b, c, x=1.0):
+    for _ in range(iters):
+        x = a * x + b * x ** 3 + c * x ** 5
+    return x
+
+
+@pytest.mark.parametrize("wnorm", [False, True])
+def test_muon_step_on_one_token_moves_along_the_unit_gradient(wnorm):
+    """A one-token chunk gives a rank-one gradient G = sigma u v^T for each matrix, and
+    Newton-Schulz of a rank-one matrix is its unit direction times the scalar quintic
+    iterated from 1: W <- W - step * phi^5(1) * G / ||G||_F (then the row norm). The
+    rate scales G but not the step (Muon discards the gradient's size). G here is torch
+    autograd of eta * l(f(k), v) on the oracle-independent torch forward."""
+    rng = np.random.default_rng(78)
+    d, dh = 7, 12
+    W = _rand_weights("swiglu", d, dh, rng, scale=2.0)
+    Q, K, V = (rng.standard_normal((2, d)) for _ in range(3))
+    eta = np.array([0.37, 0.2])
+    step = 0.05
+    cfg = orc.OracleCfg(chunk=1, loss="ip", muon=True, wnorm=wnorm, step=step, ns_eps=0.0)
+    O, Wf = orc.ttt_head(cfg, Q, K, V, eta, W)
+
+    tw = [torch.tensor(w, dtype=torch.float64, requires_grad=True) for w in W]
+    k, v = (torch.tensor(x[0], dtype=torch.float64) for x in (K, V))
+    f = F.linear(F.silu(F.linear(k, tw[0])) * F.linear(k, tw[2]), tw[1])
+    (-eta[0] * (f * v).sum()).backward()
+    s = _quintic_at_one(cfg.ns_iters, *cfg.ns_coef)
+    W1 = []
+    for w, t in zip(W, tw):
+        g = t.grad.numpy()
+        assert np.linalg.matrix_rank(g) == 1
+        nw = w - step * s * g / np.linalg.norm(g)
+        if wnorm:
+            nw = nw * (np.linalg.norm(w, axis=1) / np.linalg.norm(nw, axis=1))[:, None]
+        W1.append(nw)
+    _, Wk = orc.ttt_head(cfg, Q[:1], K[:1], V[:1], eta[:1], W)
+    for a, b in zip(Wk, W1):
+        assert np.abs(a - b).max() <= 1e-12
+    # the second token reads the once-updated weights (shifted order)
+    t1 = [torch.tensor(w, dtype=torch.float64) for w in W1]
+    q = torch.tensor(Q[1], dtype=torch.float64)
+    o1 = F.linear(F.silu(F.linear(q, t1[0])) * F.linear(q, t1[2]), t1[1]).numpy()
+    assert np.abs(O[1] - o1).max() <= 1e-12 * np.abs(o1).max()
+
+
 @pytest.mark.parametrize("muon", [False, True])
 def test_layer_keeps_every_row_norm_of_w0(muon):
     rng = np.random.default_rng(6)
