@@ -72,8 +72,10 @@ enum { TTT_IMPL_AUTO = 0, TTT_IMPL_SIMT = 1, TTT_IMPL_TC = 2, TTT_IMPL_LINEAR = 
  *          keep ~16 significant bits; the fast weights, whose updates feed back
  *          chunk after chunk, stay within the bf16 tier's tolerance of an exact
  *          computation over long sequences of updates (default);
- *   SINGLE one bf16 (fp16 inside Newton-Schulz) operand per product: fewer MMAs,
- *          but the rounding is amplified from chunk to chunk. */
+ *   SINGLE one bf16 (fp16 inside Newton-Schulz) operand per product: fewer MMAs
+ *          and half the traffic of the intermediate operands, but the rounding is
+ *          amplified from chunk to chunk (about 1.3x per update on a 512 x 1024
+ *          Muon layer), so it suits few updates, such as single-chunk mode. */
 enum { TTT_PREC_SPLIT = 0, TTT_PREC_SINGLE = 1 };
 
 /* Layer configuration. Fill it with ttt_cfg_default() and override fields. */
