@@ -1,6 +1,6 @@
 """Host-side measurement logic (no GPU): the fixed FLOP accounting, its split
-over the kernel classes, the CPU baseline's scaling to layer tokens/s, and the
-reading of committed ncu traffic figures."""
+over the kernel classes, the CPU baseline's scaling to layer tokens/s, the
+reading of committed ncu traffic figures and the roofline object."""
 import math
 
 import pytest
@@ -82,3 +82,30 @@ def test_read_traffic_uses_committed_profiles():
     v = bench.read_traffic("ns_fused", "lm_chunk2k")
     assert isinstance(v, float) and v > 1e8
     assert bench.read_traffic("no_such_kernel", "lm_chunk2k") is None
+
+
+def test_roofline_of_the_top_kernel_class():
+    """The benchmark's roofline object from per-kernel-class device times: the class
+    with the most time, its algorithmic FLOP per launch over its mean launch time,
+    against the burst bf16 peak (the sustained one beside it); the linear kernel's
+    bytes against the copy bandwidth."""
+    import bench
+    from long_seq_models_chunked_b300 import abi
+    peaks = {"hbm_gbs": 6500.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+    spec = synth.WORKLOADS["lm_chunk2k"]
+    steps, per_step = 20, 16
+    kinds = {"ns_fused": (abi.TTT_KERNEL_NS, 0.35 * per_step * steps, per_step * steps, per_step * steps),
+             "fwd": (abi.TTT_KERNEL_FWD, 0.13 * per_step * steps, per_step * steps, per_step * steps)}
+    r = bench.roofline(spec, kinds, steps, peaks, "test")
+    fl = bench.kernel_flops_per_launch(spec, abi.TTT_KERNEL_NS, per_step)
+    assert r["kernel"] == "ns_fused" and r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert math.isclose(r["achieved"], fl / 0.35e-3 / 1e12, rel_tol=1e-12)
+    assert r["peak"] == 1800.0 and math.isclose(r["frac"], r["achieved"] / 1800.0, rel_tol=1e-12)
+    assert math.isclose(r["frac_of_sustained"], r["achieved"] / 1400.0, rel_tol=1e-12)
+    assert math.isclose(r["share"], 0.35 / 0.48, rel_tol=1e-12) and math.isclose(r["launch_ms"], 0.35)
+    assert r["traffic"] == bench.read_traffic("ns_fused", "lm_chunk2k")
+
+    lin = synth.WORKLOADS["linear_chunk64"]
+    r = bench.roofline(lin, {"linear": (abi.TTT_KERNEL_LINEAR, 0.43 * steps, steps, steps)}, steps, peaks, "test")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6500.0
+    assert math.isclose(r["achieved"], bench.linear_bytes_per_step(lin) / 0.43e-3 / 1e9, rel_tol=1e-12)
