@@ -203,10 +203,16 @@ def ttt_host_arena_bytes(cfg: ttt_cfg) -> int:
 
 
 def _ptr(t) -> Optional[int]:
+    """The address of a tensor's first element (None and plain ints pass through).
+    The C ABI reads every tensor as dense row-major memory, so a strided view is
+    refused here rather than read as if it were dense."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {tuple(t.stride())} is not "
+                         "contiguous; the C ABI reads dense row-major memory (pass .contiguous())")
     return t.data_ptr()
 
 

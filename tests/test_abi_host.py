@@ -180,3 +180,18 @@ def test_swiglu_backward_rejects_before_launch(over, code):
     spec = synth.WORKLOADS["tiny_fp32"].replace(wnorm=False, muon=False)
     c = abi.cfg_from_spec(spec).cfg
     assert _swbwd_call(c, **over) == code
+
+
+def test_binding_refuses_a_strided_view_before_the_call():
+    """The C ABI reads dense row-major memory: a transposed or sliced-with-step
+    view is refused by the binding (ValueError) before any library call."""
+    import torch
+    c = abi.cfg_from_spec(synth.WORKLOADS["tiny_fp32"]).cfg
+    dense = torch.zeros(4, 8)
+    n0 = abi.ttt_launch_count()
+    for view in (dense.t(), dense[:, ::2]):
+        with pytest.raises(ValueError, match="not contiguous"):
+            abi.ttt_fwd(c, view, dense, dense, dense, dense, dense, dense, dense, dense, dense, dense,
+                        torch.zeros(256, dtype=torch.uint8), stream=0)
+    assert abi.ttt_launch_count() == n0
+    assert abi._ptr(dense) == dense.data_ptr() and abi._ptr(None) is None and abi._ptr(64) == 64
