@@ -513,6 +513,27 @@ def weight_shapes(cfg: ttt_cfg) -> Sequence[tuple]:
     return [(cfg.d, cfg.d)]
 
 
+def _check_layer_tensors(cfg: ttt_cfg, Q, K, V, lr, W0: Sequence) -> None:
+    """Shapes, dtypes and device of the layer's inputs against the configuration
+    (the C ABI sees only addresses): Q, K, V [B, H, T, d] in the storage type;
+    lr [B, H, T] or [B, H, T, n_w] fp32; W0_j [H, out, in] (or [B, H, out, in]) fp32."""
+    import torch
+    tdt = torch.bfloat16 if cfg.dtype == TTT_DTYPE_BF16 else torch.float32
+    shapes = weight_shapes(cfg)
+    want = [("Q", Q, (cfg.B, cfg.H, cfg.T, cfg.d), tdt), ("K", K, (cfg.B, cfg.H, cfg.T, cfg.d), tdt),
+            ("V", V, (cfg.B, cfg.H, cfg.T, cfg.d), tdt),
+            ("lr", lr, (cfg.B, cfg.H, cfg.T) + ((len(shapes),) if cfg.lr_per_matrix else ()), torch.float32)]
+    if len(W0) != len(shapes):
+        raise ValueError(f"W0: {len(shapes)} matrices expected, got {len(W0)}")
+    lead = (cfg.B, cfg.H) if cfg.w0_per_batch else (cfg.H,)
+    want += [(f"W0_{j + 1}", w, lead + s, torch.float32) for j, (w, s) in enumerate(zip(W0, shapes))]
+    for name, t, shape, dt in want:
+        if tuple(t.shape) != shape or t.dtype != dt:
+            raise ValueError(f"{name}: expected {shape} {dt}, got {tuple(t.shape)} {t.dtype}")
+        if t.device != Q.device:
+            raise ValueError(f"{name} is on {t.device}, Q on {Q.device}")
+
+
 def layer(holder: CfgHolder, Q, K, V, lr, W0: Sequence, stream=None, sync: bool = True):
     """Allocate outputs and workspace (torch, on Q's device) and run ttt_fwd.
 
@@ -521,6 +542,7 @@ def layer(holder: CfgHolder, Q, K, V, lr, W0: Sequence, stream=None, sync: bool 
     """
     import torch
     cfg = holder.cfg
+    _check_layer_tensors(cfg, Q, K, V, lr, W0)
     dev = Q.device
     O = torch.empty_like(Q)
     Wf = [torch.empty((cfg.B, cfg.H) + s, dtype=torch.float32, device=dev)

@@ -195,3 +195,23 @@ def test_binding_refuses_a_strided_view_before_the_call():
                         torch.zeros(256, dtype=torch.uint8), stream=0)
     assert abi.ttt_launch_count() == n0
     assert abi._ptr(dense) == dense.data_ptr() and abi._ptr(None) is None and abi._ptr(64) == 64
+
+
+def test_layer_checks_shapes_and_dtypes_before_the_call():
+    """abi.layer compares every input's shape, dtype and device with the
+    configuration before it allocates or calls anything."""
+    import torch
+    spec = synth.WORKLOADS["tiny_fp32"]
+    holder = abi.cfg_from_spec(spec)
+    B, H, T, d, dh = spec.B, spec.H, spec.T, spec.d, spec.dh
+    ok = dict(Q=torch.zeros(B, H, T, d), K=torch.zeros(B, H, T, d), V=torch.zeros(B, H, T, d),
+              lr=torch.zeros(B, H, T), W0=[torch.zeros(H, dh, d), torch.zeros(H, d, dh), torch.zeros(H, dh, d)])
+    abi._check_layer_tensors(holder.cfg, **ok)
+    bad = [dict(Q=torch.zeros(B, H, T, d + 1)), dict(K=torch.zeros(B, H, T, d, dtype=torch.bfloat16)),
+           dict(lr=torch.zeros(B, H, T, 3)), dict(W0=ok["W0"][:2]),
+           dict(W0=[torch.zeros(H, d, dh)] * 3), dict(V=torch.zeros(B, H, T - 1, d))]
+    n0 = abi.ttt_launch_count()
+    for over in bad:
+        with pytest.raises(ValueError):
+            abi.layer(holder, **{**ok, **over})
+    assert abi.ttt_launch_count() == n0
