@@ -261,10 +261,12 @@ def _orthogonal(n, rng):
     return q * np.sign(np.diag(r))
 
 
-@pytest.mark.parametrize("loss", ["ip", "mse"])
-@pytest.mark.parametrize("momentum", [0.0, 0.5])
-def test_muon_layer_is_equivariant_under_rotations_and_hidden_permutations(loss, momentum):
-    """The whole SwiGLU + Muon + weight-norm chain, over several chunks with a mask.
+@pytest.mark.parametrize("loss,momentum,mode,per_matrix", [
+    ("ip", 0.0, "shifted", False), ("mse", 0.0, "shifted", False), ("ip", 0.5, "shifted", False),
+    ("mse", 0.5, "shifted", True), ("ip", 0.0, "single", True), ("mse", 0.0, "single", False)])
+def test_muon_layer_is_equivariant_under_rotations_and_hidden_permutations(loss, momentum, mode, per_matrix):
+    """The whole SwiGLU + Muon + weight-norm chain: shifted chunks under a mask, or one
+    chunk in single mode; one rate per token, or one per token and matrix.
     Rotate the input space (R, any orthogonal), sign-permute the output space (S) and
     permute the hidden units (P): q, k -> R q, R k;  v -> S v;  W1, W3 -> P W (R^T);
     W2 -> S W2 P^T. Then f'(R x) = S f(x), both losses are unchanged, every gradient
@@ -277,12 +279,12 @@ def test_muon_layer_is_equivariant_under_rotations_and_hidden_permutations(loss,
     d, dh, C, T = 6, 10, 5, 17
     W = _rand_weights("swiglu", d, dh, rng, scale=2.0)
     Q, K, V = (rng.standard_normal((T, d)) for _ in range(3))
-    eta = rng.uniform(0.0, 0.3, T)
+    eta = rng.uniform(0.0, 0.3, (T, 3) if per_matrix else T)
     R = _orthogonal(d, rng)
     S = np.eye(d)[rng.permutation(d)] * rng.choice([-1.0, 1.0], d)[:, None]
     P = np.eye(dh)[rng.permutation(dh)]
-    cfg = orc.OracleCfg(chunk=C, loss=loss, muon=True, wnorm=True, step=0.7, mask=[1, 0, 1, 1],
-                        momentum=momentum)
+    cfg = orc.OracleCfg(chunk=C if mode == "shifted" else T, loss=loss, mode=mode, muon=True, wnorm=True,
+                        step=0.7, mask=[1, 0, 1, 1] if mode == "shifted" else None, momentum=momentum)
     O, (W1, W2, W3) = orc.ttt_head(cfg, Q, K, V, eta, W)
     Wt = (P @ W[0] @ R.T, S @ W[1] @ P.T, P @ W[2] @ R.T)
     Ot, (W1t, W2t, W3t) = orc.ttt_head(cfg, Q @ R.T, K @ R.T, V @ S.T, eta, Wt)
