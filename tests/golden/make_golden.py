@@ -26,6 +26,11 @@ CASES = {
     "linear_mse_sgd": LayerSpec("g3", B=1, H=1, T=9, d=3, dh=3, chunk=3, fast_net="linear",
                                 loss="mse", muon=False, wnorm=False, dtype="fp32",
                                 lr_a=0.5, seed=103),
+    "swiglu_muon_momentum_rates_odd": LayerSpec("g4", B=1, H=1, T=14, d=4, dh=8, chunk=4, update="odd",
+                                                momentum=0.5, lr_per_matrix=True, dtype="fp32", seed=104),
+    "swiglu_mse_inclusive": LayerSpec("g5", B=1, H=1, T=11, d=4, dh=8, chunk=4, loss="mse",
+                                      mode="inclusive", muon=False, wnorm=False, dtype="fp32",
+                                      seed=105),
 }
 
 
